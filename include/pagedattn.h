@@ -1,0 +1,176 @@
+/*
+ * pagedattn.h: C ABI of libpagedattn.so, paged KV attention for GB300 (sm_103a).
+ *
+ * The operations follow the descriptions of vLLM's PagedAttention in
+ * "vLLM-Ascend 原理" (section 2.1 PagedAttention, 2.3 Prefill, 2.4 Decode) and
+ * "vLLM 在 CANN 上的推理优化" (section "vLLM 的 PagedAttention 数据结构" and
+ * the PagedAttentionKernel sketch in "CANN 上的 PagedAttention 算子").
+ *
+ * Memory layout (all arrays dense, row-major, on the current CUDA device):
+ *   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim]
+ *                     two separate pools, one per K and V, element type
+ *                     `dtype`; physical block p, offset o, head h, dim d lives
+ *                     at ((p * block_size + o) * num_kv_heads + h) * head_dim + d.
+ *   block_tables      int32 [num_seqs, max_blocks_per_seq]; row b maps the
+ *                     logical blocks of sequence b to physical blocks.  Entries
+ *                     at or past ceil(seq_lens[b] / block_size) are never read.
+ *   seq_lens          int32 [num_seqs]; tokens of sequence b, counting the
+ *                     tokens this step appends (so a decode query sits at
+ *                     position seq_lens[b] - 1 and sees itself).
+ *   cu_q_lens         int32 [num_seqs + 1]; sequence b owns query / new-token
+ *                     rows cu_q_lens[b] .. cu_q_lens[b+1]-1; these are its last
+ *                     positions seq_lens[b] - q_len .. seq_lens[b] - 1.
+ *   q, out            [rows, num_q_heads, head_dim], element type `dtype`.
+ *   key, value        [num_tokens, num_kv_heads, head_dim] (new tokens).
+ *
+ * Supported: block_size == 16, head_dim in {64, 128}, dtype fp16 or bf16,
+ * num_q_heads % num_kv_heads == 0 with num_q_heads / num_kv_heads <= 8;
+ * q head h reads kv head h / (num_q_heads / num_kv_heads).
+ *
+ * Ownership: the caller owns every buffer.  The library allocates no device
+ * memory; calls that need scratch space take a caller-provided workspace
+ * whose minimum size the matching *_workspace_bytes function returns.
+ *
+ * Execution: every call only enqueues work on `stream` (a cudaStream_t; NULL
+ * = the legacy default stream) and returns without synchronising, except
+ * pa_get_device_error, which waits for the stream.
+ *
+ * Errors: arguments are validated on the host before anything is launched;
+ * a rejected call returns a nonzero pa_status and enqueues nothing.  A
+ * launch failure returns PA_ERR_CUDA.  The kernels also check every block
+ * table entry and slot they use against the pool; an out-of-range entry is
+ * skipped (its tokens contribute nothing, its write is dropped) and recorded
+ * in a device error word that pa_get_device_error reads.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_BLOCK_SIZE 16
+#define PA_DEFAULT_PARTITION 512
+#define PA_MAX_GROUP 8
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,          /* null pointer, negative size, inconsistent shape */
+    PA_ERR_UNSUPPORTED = 2,          /* dtype, head_dim, block_size or head grouping */
+    PA_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace NULL or below *_workspace_bytes */
+    PA_ERR_CUDA = 4                  /* a CUDA runtime call or kernel launch failed */
+} pa_status;
+
+/* Device error word bits reported by pa_get_device_error. */
+#define PA_DEVERR_BLOCK_ID 1   /* a live block-table entry outside [0, num_blocks) */
+#define PA_DEVERR_SLOT 2       /* a slot at or past num_blocks * block_size */
+#define PA_DEVERR_SEQ_LEN 4    /* seq_len above max_seq_len or the table's capacity */
+
+/* Library ABI version (major * 100 + minor). */
+int pa_version(void);
+
+/* Static, human-readable name of a pa_status value. */
+const char* pa_status_string(int status);
+
+/*
+ * Slot address of every new token ("vLLM 在 CANN 上的推理优化", the read_kv
+ * sketch: logical index -> logical block idx / block_size, offset
+ * idx % block_size, physical block from the table; slot = physical block *
+ * block_size + offset).
+ *   slot_mapping  int64 [num_tokens] (out): slot of new-token row r.
+ *   cu_q_lens     int32 [num_seqs + 1], or NULL meaning one new token per
+ *                 sequence (decode; num_tokens must equal num_seqs).
+ * Rows of a sequence whose table entry is out of range get slot -1 and set
+ * PA_DEVERR_BLOCK_ID.
+ */
+int pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* seq_lens, const int32_t* cu_q_lens, int num_seqs,
+                    int num_tokens, int num_blocks, int block_size, void* stream);
+
+/*
+ * reshape_and_cache: write each new token's k and v into its slot
+ * ("vLLM-Ascend 原理", section 2.3 "KV 写缓存" and section 2.4 "KV 追加写").
+ *   key, value    [num_tokens, num_kv_heads, head_dim]
+ *   k_cache/v_cache are updated in place.
+ *   slot_mapping  int64 [num_tokens]; a negative slot means "no write"
+ *                 (padding); a slot >= num_blocks * block_size is dropped and
+ *                 sets PA_DEVERR_SLOT.
+ * The copy is bit-exact.  Two rows naming one slot race (last writer wins).
+ */
+int pa_paged_kv_write(const void* key, const void* value, void* k_cache, void* v_cache,
+                      const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                      int num_kv_heads, int head_dim, int block_size, int dtype, void* stream);
+
+/*
+ * Workspace for pa_paged_attention_decode: the split-context partials of
+ * num_seqs sequences no longer than max_seq_len, cut into partitions of
+ * partition_size tokens (0 = PA_DEFAULT_PARTITION).  Returns 0 when no
+ * sequence needs more than one partition.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len,
+                                 int partition_size);
+
+/*
+ * Decode attention over the paged cache ("vLLM-Ascend 原理", section 2.4
+ * "分页自注意力"; the block loop of the CANN PagedAttentionKernel sketch).
+ * One query per sequence: out[b, h] = sum_t softmax_t(scale * q[b, h] . k_t) v_t
+ * over positions t = 0 .. seq_lens[b] - 1, k_t and v_t read through the block
+ * table, with the softmax merged block by block (online softmax).  Sequences
+ * longer than partition_size tokens are split into partitions whose partial
+ * (max, sum, accumulator) are merged by a log-sum-exp reduction.
+ *   out, q        [num_seqs, num_q_heads, head_dim]
+ *   max_seq_len   host-side upper bound of seq_lens (sizes the grid).
+ *   num_blocks    pool size in blocks (bounds every table entry).
+ *   partition_size tokens per partition, a positive multiple of block_size,
+ *                 or 0 for PA_DEFAULT_PARTITION.
+ *   workspace     device scratch of at least pa_decode_workspace_bytes(...)
+ *                 bytes, 256-byte aligned; may be NULL when that is 0.
+ * A sequence with seq_len == 0 gets an all-zero output row.
+ */
+int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int max_blocks_per_seq,
+                              const int32_t* seq_lens, int num_seqs, int max_seq_len,
+                              int num_blocks, float scale, int num_q_heads, int num_kv_heads,
+                              int head_dim, int block_size, int partition_size, void* workspace,
+                              size_t workspace_bytes, int dtype, void* stream);
+
+/* Workspace for pa_paged_attention_prefill (the decode rows' partials). */
+size_t pa_prefill_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len);
+
+/*
+ * Causal attention of query chunks appended onto a cached prefix, as in
+ * chunked prefill ("vLLM-Ascend 原理", section 2.3 "因果自注意力": the query
+ * at position i sees positions 0..i; section 2.4: a later chunk reads the KV
+ * that earlier chunks wrote).  Query row cu_q_lens[b] + i of sequence b sits
+ * at position seq_lens[b] - q_len_b + i.  Sequences with q_len == 1 are
+ * decodes and run through the decode kernel; longer chunks run through the
+ * tensor-core prefill kernel.  The new tokens' k/v must already be in the
+ * cache (pa_paged_kv_write first).
+ *   out, q        [num_tokens, num_q_heads, head_dim]; num_tokens = cu_q_lens[num_seqs]
+ *   max_q_len, max_seq_len  host-side upper bounds (grid sizing).
+ *   workspace     >= pa_prefill_workspace_bytes(...) bytes, 256-byte aligned.
+ */
+int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* seq_lens, const int32_t* cu_q_lens, int num_seqs,
+                               int num_tokens, int max_q_len, int max_seq_len, int num_blocks,
+                               float scale, int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, void* workspace, size_t workspace_bytes, int dtype,
+                               void* stream);
+
+/*
+ * Read the device error word (PA_DEVERR_* bits) of the current device after
+ * the work queued on `stream` has finished; `clear` != 0 resets it to 0.
+ * This call synchronises the stream.
+ */
+int pa_get_device_error(int* code, int clear, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDATTN_H */

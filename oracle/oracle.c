@@ -1,0 +1,348 @@
+/*
+ * CPU oracle for paged KV attention.  TEST INFRASTRUCTURE ONLY.
+ *
+ * This file is the slow, obviously correct statement of what the paged
+ * attention path computes.  Only the test suite, the package smoke check and
+ * the benchmark's CPU-baseline leg may load it; the product path never does.
+ * It shares no code, header, table or helper with the CUDA kernels.
+ *
+ * Every value is decoded from its 16-bit storage pattern into fp64 and all
+ * arithmetic is fp64.  Nothing is blocked, fused, partitioned or reordered
+ * beyond the plain definitions below:
+ *
+ *  - Address translation ("vLLM 在 CANN 上的推理优化", section "vLLM 的
+ *    PagedAttention 数据结构", the read_kv sketch): logical token index idx of
+ *    a sequence lives in logical block idx / block_size at offset
+ *    idx % block_size; the block table maps the logical block to a physical
+ *    block of the pool.  The slot of a token is
+ *    physical_block * block_size + offset.
+ *
+ *  - Cache write ("vLLM-Ascend 原理", section 2.3 step "KV 写缓存" and
+ *    section 2.4 step "KV 追加写"): the new k and v of a token are copied into
+ *    its slot; K and V are separate pools (Model Runner V2 notes, section 4.1)
+ *    laid out [num_blocks, block_size, num_kv_heads, head_dim] (CANN page,
+ *    PagedAttentionKernel sketch, "kv_pool" comment).
+ *
+ *  - Attention ("vLLM-Ascend 原理", section 2.3, "因果自注意力"): the query at
+ *    position i attends to the keys at positions 0..i, softmax, weighted sum of
+ *    the values.  For decode (section 2.4, "分页自注意力") the single new query
+ *    sits at position seq_len-1 and attends to the whole prefix read through
+ *    the block table.  With grouped-query attention several q heads share one
+ *    kv head; q head h reads kv head h / (num_q_heads / num_kv_heads).
+ *    The softmax is written in its two-pass form: M = max_t s_t,
+ *    out = sum_t exp(s_t - M) v_t / sum_t exp(s_t - M), s_t = scale * q.k_t.
+ *
+ * Readings where the pages are silent: seq_len counts the new token(s);
+ * slot < 0 means "no write"; a decode row with seq_len == 0 yields zeros;
+ * table entries past ceil(seq_len / block_size) are never read.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+enum { OR_F16 = 0, OR_BF16 = 1 };
+enum { OR_OK = 0, OR_ERR_ARG = 1, OR_ERR_TABLE = 2, OR_ERR_SLOT = 3, OR_ERR_NOMEM = 4 };
+
+/* binary16 (IEEE 754-2008, 3.6): 1 sign bit, 5 exponent bits (bias 15),
+ * 10 fraction bits.  exponent 0: subnormal f * 2^-24; exponent 31: inf/NaN. */
+static double decode_f16(uint16_t h) {
+    int sign = h >> 15;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(0x400 | f), e - 25);
+    return sign ? -v : v;
+}
+
+/* bfloat16: the 16 most significant bits of a binary32 (1 sign, 8 exponent
+ * bits with bias 127, 7 fraction bits).  Decoded here from the fields. */
+static double decode_bf16(uint16_t h) {
+    int sign = h >> 15;
+    int e = (h >> 7) & 0xff;
+    int f = h & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133);            /* f * 2^(1-127-7) */
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(0x80 | f), e - 134); /* (128+f) * 2^(e-127-7) */
+    return sign ? -v : v;
+}
+
+static double g_tab_f16[65536];
+static double g_tab_bf16[65536];
+static pthread_once_t g_once = PTHREAD_ONCE_INIT;
+
+static void build_tables(void) {
+    for (int i = 0; i < 65536; ++i) {
+        g_tab_f16[i] = decode_f16((uint16_t)i);
+        g_tab_bf16[i] = decode_bf16((uint16_t)i);
+    }
+}
+
+static const double* table_for(int dtype) {
+    pthread_once(&g_once, build_tables);
+    return dtype == OR_BF16 ? g_tab_bf16 : g_tab_f16;
+}
+
+static int default_threads(int n) {
+    if (n > 0) return n;
+    long c = sysconf(_SC_NPROCESSORS_ONLN);
+    return c > 0 ? (int)c : 1;
+}
+
+/* ------------------------------------------------------------------------ */
+
+int oracle_decode_values(const uint16_t* in, double* out, int64_t n, int dtype) {
+    if (dtype != OR_F16 && dtype != OR_BF16) return OR_ERR_ARG;
+    const double* tab = table_for(dtype);
+    for (int64_t i = 0; i < n; ++i) out[i] = tab[in[i]];
+    return OR_OK;
+}
+
+/* Slot of every new token.  Sequence b's new tokens are its last q_lens[b]
+ * positions, seq_lens[b]-q_lens[b] .. seq_lens[b]-1, packed sequence after
+ * sequence into slots[]. */
+int oracle_slot_mapping(int64_t* slots, const int32_t* block_tables, int max_blocks,
+                        const int32_t* seq_lens, const int32_t* q_lens, int B,
+                        int block_size, int num_blocks) {
+    if (block_size <= 0 || B < 0) return OR_ERR_ARG;
+    int64_t row = 0;
+    for (int b = 0; b < B; ++b) {
+        int n = seq_lens[b], ql = q_lens[b];
+        if (ql < 0 || ql > n) return OR_ERR_ARG;
+        for (int i = 0; i < ql; ++i) {
+            int64_t idx = (int64_t)n - ql + i;        /* logical token index */
+            int64_t logical_block = idx / block_size;
+            int64_t offset = idx % block_size;
+            if (logical_block >= max_blocks) return OR_ERR_TABLE;
+            int64_t phys = block_tables[(int64_t)b * max_blocks + logical_block];
+            if (phys < 0 || phys >= num_blocks) return OR_ERR_TABLE;
+            slots[row++] = phys * block_size + offset;
+        }
+    }
+    return OR_OK;
+}
+
+/* cache[slot / bs][slot % bs][h][:] = key[t][h][:] for every t with slot >= 0 */
+int oracle_kv_write(const uint16_t* key, const uint16_t* value, uint16_t* k_cache,
+                    uint16_t* v_cache, const int64_t* slots, int64_t T, int num_blocks,
+                    int num_kv_heads, int head_dim, int block_size) {
+    int64_t num_slots = (int64_t)num_blocks * block_size;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t slot = slots[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) return OR_ERR_SLOT;
+        int64_t blk = slot / block_size, off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            for (int d = 0; d < head_dim; ++d) {
+                int64_t dst = ((blk * block_size + off) * num_kv_heads + h) * head_dim + d;
+                int64_t src = (t * num_kv_heads + h) * head_dim + d;
+                k_cache[dst] = key[src];
+                v_cache[dst] = value[src];
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    /* problem */
+    const uint16_t *q, *k_cache, *v_cache;
+    const int32_t *block_tables, *seq_lens;
+    const int64_t *row_seq, *row_pos, *row_qrow; /* per computed row: seq, position, q row */
+    int64_t n_rows;
+    int max_blocks, Hq, Hkv, D, block_size, num_blocks;
+    double scale;
+    const double* tab;
+    double* out;                                /* [n_rows, Hq, D] */
+    int max_len;
+    /* work split */
+    int64_t u_begin, u_end;                     /* units = row * Hq + h */
+    int status;
+} job_t;
+
+/* One query (row, head): walk the block table token by token. */
+static int attend_one(const job_t* J, int64_t r, int h, double* s, double* qd, double* acc) {
+    const int D = J->D, bs = J->block_size;
+    const int G = J->Hq / J->Hkv, g = h / G;
+    const int64_t b = J->row_seq[r];
+    const int64_t pos = J->row_pos[r];
+    double* o = J->out + (r * J->Hq + h) * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (pos < 0) return OR_OK;                   /* empty context: zeros */
+    const int64_t n = pos + 1;                   /* keys 0..pos inclusive */
+    const uint16_t* qp = J->q + (J->row_qrow[r] * J->Hq + h) * D;
+    for (int d = 0; d < D; ++d) qd[d] = J->tab[qp[d]];
+    double M = -INFINITY;
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t lb = t / bs, off = t % bs;
+        if (lb >= J->max_blocks) return OR_ERR_TABLE;
+        int64_t phys = J->block_tables[b * J->max_blocks + lb];
+        if (phys < 0 || phys >= J->num_blocks) return OR_ERR_TABLE;
+        const uint16_t* kp = J->k_cache + ((phys * bs + off) * J->Hkv + g) * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += qd[d] * J->tab[kp[d]];
+        s[t] = J->scale * dot;
+        if (s[t] > M) M = s[t];
+    }
+    for (int d = 0; d < D; ++d) acc[d] = 0.0;
+    double L = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t lb = t / bs, off = t % bs;
+        int64_t phys = J->block_tables[b * J->max_blocks + lb];
+        const uint16_t* vp = J->v_cache + ((phys * bs + off) * J->Hkv + g) * D;
+        double w = exp(s[t] - M);
+        L += w;
+        for (int d = 0; d < D; ++d) acc[d] += w * J->tab[vp[d]];
+    }
+    for (int d = 0; d < D; ++d) o[d] = acc[d] / L;
+    return OR_OK;
+}
+
+static void* worker(void* arg) {
+    job_t* J = (job_t*)arg;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(J->max_len > 0 ? J->max_len : 1));
+    double* qd = (double*)malloc(sizeof(double) * (size_t)J->D);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)J->D);
+    if (!s || !qd || !acc) {
+        J->status = OR_ERR_NOMEM;
+    } else {
+        for (int64_t u = J->u_begin; u < J->u_end; ++u) {
+            int rc = attend_one(J, u / J->Hq, (int)(u % J->Hq), s, qd, acc);
+            if (rc) { J->status = rc; break; }
+        }
+    }
+    free(s); free(qd); free(acc);
+    return NULL;
+}
+
+static int run_rows(const job_t* proto, int num_threads) {
+    int64_t units = proto->n_rows * proto->Hq;
+    int nt = default_threads(num_threads);
+    if (nt > units) nt = units > 0 ? (int)units : 1;
+    job_t* jobs = (job_t*)calloc((size_t)nt, sizeof(job_t));
+    pthread_t* th = (pthread_t*)calloc((size_t)nt, sizeof(pthread_t));
+    if (!jobs || !th) { free(jobs); free(th); return OR_ERR_NOMEM; }
+    for (int i = 0; i < nt; ++i) {
+        jobs[i] = *proto;
+        jobs[i].u_begin = units * i / nt;
+        jobs[i].u_end = units * (i + 1) / nt;
+        jobs[i].status = OR_OK;
+    }
+    int status = OR_OK;
+    if (nt == 1) {
+        worker(&jobs[0]);
+    } else {
+        for (int i = 0; i < nt; ++i) pthread_create(&th[i], NULL, worker, &jobs[i]);
+        for (int i = 0; i < nt; ++i) pthread_join(th[i], NULL);
+    }
+    for (int i = 0; i < nt; ++i) if (jobs[i].status) status = jobs[i].status;
+    free(jobs); free(th);
+    return status;
+}
+
+static int check_common(int B, int Hq, int Hkv, int D, int block_size, int dtype) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || block_size <= 0) return OR_ERR_ARG;
+    if (Hq % Hkv) return OR_ERR_ARG;
+    if (dtype != OR_F16 && dtype != OR_BF16) return OR_ERR_ARG;
+    return OR_OK;
+}
+
+/* Decode: one query per sequence, q [B, Hq, D] -> out [n, Hq, D] fp64.
+ * sel (optional, n entries) picks which sequences to compute; NULL = all B. */
+int oracle_paged_attention_decode(double* out, const uint16_t* q, const uint16_t* k_cache,
+                                  const uint16_t* v_cache, const int32_t* block_tables,
+                                  int max_blocks, const int32_t* seq_lens, int B, int num_blocks,
+                                  int Hq, int Hkv, int D, int block_size, double scale,
+                                  int dtype, const int64_t* sel, int64_t n_sel, int num_threads) {
+    int rc = check_common(B, Hq, Hkv, D, block_size, dtype);
+    if (rc) return rc;
+    int64_t n = sel ? n_sel : B;
+    int64_t* rs = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1) * 3);
+    if (!rs) return OR_ERR_NOMEM;
+    int64_t *row_seq = rs, *row_pos = rs + n, *row_q = rs + 2 * n;
+    int max_len = 1;
+    for (int64_t r = 0; r < n; ++r) {
+        int64_t b = sel ? sel[r] : r;
+        if (b < 0 || b >= B) { free(rs); return OR_ERR_ARG; }
+        row_seq[r] = b;
+        row_pos[r] = (int64_t)seq_lens[b] - 1;
+        row_q[r] = b;
+        if (seq_lens[b] > max_len) max_len = seq_lens[b];
+    }
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k_cache = k_cache; J.v_cache = v_cache; J.block_tables = block_tables;
+    J.seq_lens = seq_lens; J.row_seq = row_seq; J.row_pos = row_pos; J.row_qrow = row_q;
+    J.n_rows = n; J.max_blocks = max_blocks; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
+    J.block_size = block_size; J.num_blocks = num_blocks; J.scale = scale;
+    J.tab = table_for(dtype); J.out = out; J.max_len = max_len;
+    rc = run_rows(&J, num_threads);
+    free(rs);
+    return rc;
+}
+
+/* Varlen causal attention over the paged cache.  q [T, Hq, D], rows packed
+ * per sequence (q_lens[b] rows each).  Row i of sequence b sits at position
+ * seq_lens[b] - q_lens[b] + i and sees positions 0..that position.
+ * sel (optional) lists the q rows to compute; out is [n, Hq, D] fp64. */
+int oracle_paged_attention_prefill(double* out, const uint16_t* q, const uint16_t* k_cache,
+                                   const uint16_t* v_cache, const int32_t* block_tables,
+                                   int max_blocks, const int32_t* seq_lens,
+                                   const int32_t* q_lens, int B, int num_blocks, int Hq, int Hkv,
+                                   int D, int block_size, double scale, int dtype,
+                                   const int64_t* sel, int64_t n_sel, int num_threads) {
+    int rc = check_common(B, Hq, Hkv, D, block_size, dtype);
+    if (rc) return rc;
+    int64_t T = 0;
+    for (int b = 0; b < B; ++b) {
+        if (q_lens[b] < 0 || q_lens[b] > seq_lens[b]) return OR_ERR_ARG;
+        T += q_lens[b];
+    }
+    int64_t* seq_of = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T > 0 ? T : 1) * 2);
+    if (!seq_of) return OR_ERR_NOMEM;
+    int64_t* pos_of = seq_of + T;
+    int64_t r = 0;
+    for (int b = 0; b < B; ++b)
+        for (int i = 0; i < q_lens[b]; ++i, ++r) {
+            seq_of[r] = b;
+            pos_of[r] = (int64_t)seq_lens[b] - q_lens[b] + i;
+        }
+    int64_t n = sel ? n_sel : T;
+    int64_t* rs = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1) * 3);
+    if (!rs) { free(seq_of); return OR_ERR_NOMEM; }
+    int64_t *row_seq = rs, *row_pos = rs + n, *row_q = rs + 2 * n;
+    int max_len = 1;
+    for (int64_t k = 0; k < n; ++k) {
+        int64_t qr = sel ? sel[k] : k;
+        if (qr < 0 || qr >= T) { free(rs); free(seq_of); return OR_ERR_ARG; }
+        row_seq[k] = seq_of[qr];
+        row_pos[k] = pos_of[qr];
+        row_q[k] = qr;
+        if (pos_of[qr] + 1 > max_len) max_len = (int)(pos_of[qr] + 1);
+    }
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k_cache = k_cache; J.v_cache = v_cache; J.block_tables = block_tables;
+    J.seq_lens = seq_lens; J.row_seq = row_seq; J.row_pos = row_pos; J.row_qrow = row_q;
+    J.n_rows = n; J.max_blocks = max_blocks; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
+    J.block_size = block_size; J.num_blocks = num_blocks; J.scale = scale;
+    J.tab = table_for(dtype); J.out = out; J.max_len = max_len;
+    rc = run_rows(&J, num_threads);
+    free(rs); free(seq_of);
+    return rc;
+}
+
+int oracle_num_threads(int requested) { return default_threads(requested); }

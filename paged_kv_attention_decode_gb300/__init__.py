@@ -1,0 +1,19 @@
+"""Paged KV attention for GB300 (sm_103a).
+
+The compute path is the C-ABI library ``libpagedattn.so`` (hand-written CUDA,
+declared in ``include/pagedattn.h``); this package is its thin Python binding.
+Importing the package does not load the library; the first call does, and
+fails loudly if the library has not been built.
+"""
+from ._binding import (  # noqa: F401
+    PagedAttnError,
+    decode_workspace_bytes,
+    library_path,
+    load_library,
+    paged_attention_decode,
+    paged_attention_prefill,
+    paged_kv_write,
+    prefill_workspace_bytes,
+    slot_mapping,
+    device_error,
+)
