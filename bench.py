@@ -1,0 +1,391 @@
+"""Benchmark: one paged-attention decode step (slot mapping -> KV write ->
+decode attention) on the LLaMA-2-7B-shaped workload: B=64 sequences, context
+lengths uniform in [512, 4096], 32 q heads = 32 kv heads, head_dim 128, fp16,
+16-token blocks scattered over a pool 10% larger than needed.
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on the
+host cores instead (the only baseline that exists for this path).
+N > 1 (torchrun) runs independent replicas, one per GPU: the path has no
+exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn decode tokens/s & HBM GB/s (% of GB300 peak), B=64 ctx≤4K"
+UNIT = "tokens/s"
+SPEC_HBM_GBS = 8000.0
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _algorithmic_bytes(w) -> dict:
+    """Bytes the decode attention must move per launch: every live K/V row of
+    every sequence once, the queries, the outputs, the live table entries and
+    the lengths."""
+    n = w.seq_lens.astype(np.int64)
+    kv = int(n.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+    q = w.batch * w.num_q_heads * w.head_dim * 2
+    live_entries = int((-(-n // 16)).sum())
+    meta = live_entries * 4 + w.batch * 4
+    return {"kv": kv, "q": q, "out": q, "meta": meta, "total": kv + 2 * q + meta}
+
+
+def _source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("pa_decode.cu", "pa_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_attention_decode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_per_launch(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("source_hash") != _source_hash() or d.get("workload") != workload:
+            return None
+        return int(d["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        try:
+            sm = [float(r[1]) for r in rows]
+            mx = max(float(r[2]) for r in rows)
+        except ValueError:
+            return None
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def cpu_baseline(w, seconds: float = 10.0, seq_budget: int = 64) -> dict:
+    """Time the fp64 oracle (as it stands) on the host cores over whole
+    sequences of the same workload: slot mapping, KV write and decode
+    attention of each sampled sequence."""
+    import oracle
+    import torch
+
+    rng = np.random.default_rng(7)
+    order = rng.permutation(w.batch)
+    done = 0
+    t_total = 0.0
+    i = 0
+    while (t_total < seconds and done < seq_budget) or done == 0:
+        b = int(order[i % w.batch])
+        i += 1
+        nb = -(-int(w.seq_lens[b]) // 16)
+        idx = torch.from_numpy(w.block_tables[b, :nb].astype(np.int64)).to(w.k_cache.device)
+        kc = w.k_cache.index_select(0, idx).cpu().view(torch.int16).numpy().view(np.uint16)
+        vc = w.v_cache.index_select(0, idx).cpu().view(torch.int16).numpy().view(np.uint16)
+        tables = np.arange(nb, dtype=np.int32)[None, :]
+        sl = w.seq_lens[b:b + 1]
+        q = w.q[b:b + 1].cpu().view(torch.int16).numpy().view(np.uint16)
+        key = w.key[b:b + 1].cpu().view(torch.int16).numpy().view(np.uint16)
+        val = w.value[b:b + 1].cpu().view(torch.int16).numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        slots = oracle.slot_mapping(tables, sl, np.ones(1, np.int32), 16, nb)
+        oracle.kv_write(key, val, kc, vc, slots)
+        oracle.paged_attention_decode(q, kc, vc, tables, sl, w.scale, w.dtype)
+        t_total += time.perf_counter() - t0
+        done += 1
+    return {"value": done / t_total, "unit": UNIT, "cores": oracle.num_threads(0), "kind": "oracle",
+            "sample": f"{done} whole sequences of the workload (all {w.num_q_heads} heads, mean ctx "
+                      f"{int(w.seq_lens.mean())}), slot mapping + KV write + decode attention, fp64, "
+                      f"{t_total:.1f} s of CPU time"}
+
+
+def run_reference(args):
+    """--impl reference: the oracle on the host cores, one whole sequence per step."""
+    import oracle
+
+    ws, rank, _ = _dist()
+    if ws > 1 and rank != 0:
+        return 0
+    from paged_kv_attention_decode_gb300 import workloads as W
+
+    import torch
+
+    w = W.make(args.workload, device="cpu")
+    bt = w.block_tables
+
+    def u16(t):
+        return t.view(torch.int16).numpy().view(np.uint16)
+
+    kcb, vcb, qb, keyb, valb = (u16(t) for t in (w.k_cache, w.v_cache, w.q, w.key, w.value))
+
+    def step(i):
+        b = i % w.batch
+        sl = w.seq_lens[b:b + 1]
+        tables = bt[b:b + 1]
+        slots = oracle.slot_mapping(tables, sl, np.ones(1, np.int32), 16, w.num_blocks)
+        oracle.kv_write(keyb[b:b + 1], valb[b:b + 1], kcb, vcb, slots)
+        oracle.paged_attention_decode(qb[b:b + 1], kcb, vcb, tables, sl, w.scale, w.dtype)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    el = time.perf_counter() - t0
+    value = args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch": w.batch, "ctx": "U[512,4096]",
+                   "heads": f"{w.num_q_heads}/{w.num_kv_heads}", "head_dim": w.head_dim, "block_size": 16,
+                   "step": "one whole sequence per step (rotating through the batch)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(0), "kind": "oracle",
+                         "sample": "one whole sequence of the workload per step: slot mapping + KV write "
+                                   "+ decode attention, fp64"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    import paged_kv_attention_decode_gb300 as pa
+    from paged_kv_attention_decode_gb300 import workloads as W
+
+    ws, rank, local = _dist()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pa.load_library()
+
+    w = W.make(args.workload, device=dev)
+    B = w.batch
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    slots = torch.empty(B, dtype=torch.int64, device=dev)
+    out = torch.empty_like(w.q)
+    nbytes = pa.decode_workspace_bytes(B, w.num_q_heads, w.head_dim, w.max_seq_len, args.partition)
+    wsp = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    max_len = w.max_seq_len
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pa.slot_mapping(bt, sl, None, B, w.num_blocks, out=slots)
+        pa.paged_kv_write(w.key, w.value, w.k_cache, w.v_cache, slots)
+
+    def attend():
+        pa.paged_attention_decode(w.q, w.k_cache, w.v_cache, bt, sl, w.scale, max_len, out=out,
+                                  partition_size=args.partition, workspace=wsp)
+
+    for _ in range(args.warmup):
+        step()
+        attend()
+    torch.cuda.synchronize()
+    launches_per_step = 3 + (1 if nbytes > 0 else 0)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.5)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        attend()
+        e2.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    attn_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / args.steps
+    write_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in ev) / args.steps
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t)
+    value = ws * B * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the public API with host buffers -------------
+    q_h = w.q.cpu().pin_memory()
+    k_h = w.key.cpu().pin_memory()
+    v_h = w.value.cpu().pin_memory()
+    bt_h = torch.from_numpy(w.block_tables).pin_memory()
+    sl_h = torch.from_numpy(w.seq_lens).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, k_d, v_d = torch.empty_like(w.q), torch.empty_like(w.key), torch.empty_like(w.value)
+    bt_d, sl_d = torch.empty_like(bt), torch.empty_like(sl)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, bt_h, sl_h))
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_steps = max(10, min(args.steps, 500))
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        pa.slot_mapping(bt_d, sl_d, None, B, w.num_blocks, out=slots)
+        pa.paged_kv_write(k_d, v_d, w.k_cache, w.v_cache, slots)
+        pa.paged_attention_decode(q_d, w.k_cache, w.v_cache, bt_d, sl_d, w.scale, max_len, out=out,
+                                  partition_size=args.partition, workspace=wsp)
+        out_h.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t)
+    e2e_value = ws * B * e2e_steps / e2e_s
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = _peaks()
+    ab = _algorithmic_bytes(w)
+    achieved = ab["total"] / (attn_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": B, "ctx": f"U[512,4096] (mean {int(w.seq_lens.mean())})"
+                   if args.workload == "llama7b_decode" else f"max {w.max_seq_len}",
+                   "heads": f"{w.num_q_heads}/{w.num_kv_heads}", "head_dim": w.head_dim, "block_size": 16,
+                   "partition": args.partition or 512, "pool_blocks": w.num_blocks,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: {ab['kv'] / 1e9:.2f} GB of KV read per step"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": _traffic_per_launch(args.workload),
+                     "kernel": "decode attention (partition kernel + log-sum-exp reduce)",
+                     "peak_kind": f"{peak_kind} HBM copy", "frac_of_8TBs_spec": achieved / SPEC_HBM_GBS,
+                     "algorithmic_bytes_per_launch": ab["total"], "ms_per_launch": attn_ms},
+        "write_ms_per_step": write_ms,
+        "attention_tokens_per_s": B / (attn_ms / 1e3),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, seconds=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="llama7b_decode")
+    ap.add_argument("--partition", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -70,6 +70,7 @@ typedef enum {
 #define PA_DEVERR_BLOCK_ID 1   /* a live block-table entry outside [0, num_blocks) */
 #define PA_DEVERR_SLOT 2       /* a slot at or past num_blocks * block_size */
 #define PA_DEVERR_SEQ_LEN 4    /* seq_len above max_seq_len or the table's capacity */
+#define PA_DEVERR_TIMEOUT 8    /* a bounded wait for a TMA copy ran out (the work was abandoned) */
 
 /* Library ABI version (major * 100 + minor). */
 int pa_version(void);

@@ -1,0 +1,285 @@
+// C ABI of libpagedattn.so: argument validation, tensor-map set-up, launches.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "pa_internal.h"
+#include "pagedattn.h"
+
+namespace {
+
+// Device error word: kernels OR PA_DEVERR_* bits into it.
+__device__ unsigned int g_pa_device_error;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_err_addr[kMaxDevices] = {};
+
+unsigned int* error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pa_device_error) != cudaSuccess) return nullptr;
+        g_err_addr[dev] = static_cast<unsigned int*>(p);
+    }
+    return g_err_addr[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Tensor map over one pool [num_blocks * 16 token rows, Hkv, D] viewed as 4-D
+// (64-element row piece, D/64 pieces, head, token slot); one box = the 16 rows
+// of one (block, head), 128-byte swizzled.
+bool make_kv_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads, int head_dim, int dtype) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(head_dim / 64), static_cast<cuuint64_t>(num_kv_heads),
+                                static_cast<cuuint64_t>(num_blocks) * 16};
+    const cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(head_dim) * 2,
+                                   static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(head_dim / 64), 1, 16};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
+
+constexpr int kMaxGrid = 65535;
+constexpr int kMaxPoolBlocks = (1 << 27) - 1;  // token-row coordinate stays below 2^31
+
+int check_shape(int num_q_heads, int num_kv_heads, int head_dim, int block_size, int dtype, int num_blocks) {
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (block_size != PA_BLOCK_SIZE) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_kv_heads > kMaxGrid) return PA_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+    if (num_q_heads / num_kv_heads > PA_MAX_GROUP) return PA_ERR_UNSUPPORTED;
+    if (num_blocks <= 0 || num_blocks > kMaxPoolBlocks) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+int parts_for(int max_seq_len, int partition) {
+    return max_seq_len > 0 ? (max_seq_len + partition - 1) / partition : 1;
+}
+
+size_t partials_bytes(int num_seqs, int num_q_heads, int head_dim, int parts) {
+    const size_t n = static_cast<size_t>(num_seqs) * num_q_heads * parts;
+    return 2 * align256(n * sizeof(float)) + align256(n * head_dim * sizeof(float));
+}
+
+void carve_partials(pa::DecodeParams& p, void* ws, int head_dim) {
+    const size_t n = static_cast<size_t>(p.num_seqs) * p.num_q_heads * p.max_parts;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    p.ws_m = reinterpret_cast<float*>(base);
+    p.ws_l = reinterpret_cast<float*>(base + align256(n * sizeof(float)));
+    p.ws_acc = reinterpret_cast<float*>(base + 2 * align256(n * sizeof(float)));
+    (void)head_dim;
+}
+
+float scale_log2(float scale) { return scale * 1.4426950408889634f; }
+
+}  // namespace
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+const char* pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_WORKSPACE_TOO_SMALL: return "PA_ERR_WORKSPACE_TOO_SMALL";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+int pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* seq_lens, const int32_t* cu_q_lens, int num_seqs, int num_tokens,
+                    int num_blocks, int block_size, void* stream) {
+    if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (block_size != PA_BLOCK_SIZE) return PA_ERR_UNSUPPORTED;
+    if (num_blocks <= 0 || num_blocks > kMaxPoolBlocks) return PA_ERR_INVALID_ARG;
+    if (!cu_q_lens && num_tokens != num_seqs) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!slot_mapping || !block_tables || !seq_lens) return PA_ERR_INVALID_ARG;
+    unsigned int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    cudaError_t e = pa::launch_slot_mapping(slot_mapping, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens,
+                                            num_seqs, num_tokens, num_blocks, err,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_paged_kv_write(const void* key, const void* value, void* k_cache, void* v_cache,
+                      const int64_t* slot_mapping, int num_tokens, int num_blocks, int num_kv_heads,
+                      int head_dim, int block_size, int dtype, void* stream) {
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (block_size != PA_BLOCK_SIZE) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0 || num_blocks > kMaxPoolBlocks)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    unsigned int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    cudaError_t e = pa::launch_kv_write(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks,
+                                        num_kv_heads, head_dim, err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len,
+                                 int partition_size) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len <= 0 || partition_size < 0) return 0;
+    const int part = partition_size ? partition_size : PA_DEFAULT_PARTITION;
+    const int parts = parts_for(max_seq_len, part);
+    if (parts <= 1) return 0;
+    return partials_bytes(num_seqs, num_q_heads, head_dim, parts);
+}
+
+static int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                       const int32_t* cu_q_lens, int num_seqs, int max_seq_len, int num_blocks, float scale,
+                       int num_q_heads, int num_kv_heads, int head_dim, int partition_size, void* workspace,
+                       size_t workspace_bytes, int dtype, cudaStream_t stream) {
+    const int part = partition_size ? partition_size : PA_DEFAULT_PARTITION;
+    const int parts = parts_for(max_seq_len, part);
+    const size_t need = parts > 1 ? partials_bytes(num_seqs, num_q_heads, head_dim, parts) : 0;
+    if (need) {
+        if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned256(workspace)) return PA_ERR_INVALID_ARG;
+    }
+    unsigned int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    CUtensorMap kmap, vmap;
+    if (!make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) ||
+        !make_kv_map(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype))
+        return PA_ERR_CUDA;
+    pa::DecodeParams p{};
+    p.out = out;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.cu_q_lens = cu_q_lens;
+    p.err = err;
+    p.num_seqs = num_seqs;
+    p.max_blocks = max_blocks_per_seq;
+    p.max_seq_len = max_seq_len;
+    p.num_blocks = num_blocks;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = num_q_heads / num_kv_heads;
+    p.partition_tokens = part;
+    p.max_parts = parts;
+    p.scale_log2 = scale_log2(scale);
+    if (need) carve_partials(p, workspace, head_dim);
+    cudaError_t e = pa::launch_decode(p, kmap, vmap, head_dim, dtype, stream);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                              int num_seqs, int max_seq_len, int num_blocks, float scale, int num_q_heads,
+                              int num_kv_heads, int head_dim, int block_size, int partition_size,
+                              void* workspace, size_t workspace_bytes, int dtype, void* stream) {
+    int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size, dtype, num_blocks);
+    if (rc) return rc;
+    if (num_seqs < 0 || num_seqs > kMaxGrid || max_seq_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (partition_size < 0 || partition_size % PA_BLOCK_SIZE) return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+    return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
+                       max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, partition_size,
+                       workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream));
+}
+
+size_t pa_prefill_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len) {
+    return pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len, 0);
+}
+
+int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                               const int32_t* cu_q_lens, int num_seqs, int num_tokens, int max_q_len,
+                               int max_seq_len, int num_blocks, float scale, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, void* workspace, size_t workspace_bytes, int dtype,
+                               void* stream) {
+    int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size, dtype, num_blocks);
+    if (rc) return rc;
+    if (num_seqs < 0 || num_seqs > kMaxGrid || num_tokens < 0 || max_q_len < 0 || max_seq_len < 0 ||
+        max_blocks_per_seq <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || num_tokens == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_q_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // decode rows (q_len == 1) through the decode kernel
+    rc = decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens, num_seqs,
+                     max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, 0, workspace,
+                     workspace_bytes, dtype, s);
+    if (rc) return rc;
+    if (max_q_len <= 1) return PA_OK;
+    unsigned int* err = error_word();
+    CUtensorMap kmap, vmap;
+    if (!make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) ||
+        !make_kv_map(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype))
+        return PA_ERR_CUDA;
+    pa::PrefillParams p{};
+    p.out = out;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.cu_q_lens = cu_q_lens;
+    p.err = err;
+    p.num_seqs = num_seqs;
+    p.max_blocks = max_blocks_per_seq;
+    p.max_seq_len = max_seq_len;
+    p.num_blocks = num_blocks;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = num_q_heads / num_kv_heads;
+    p.q_per_tile = 64 / p.group;
+    p.scale_log2 = scale_log2(scale);
+    cudaError_t e = pa::launch_prefill(p, kmap, vmap, head_dim, dtype, max_q_len, s);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_get_device_error(int* code, int clear, void* stream) {
+    if (!code) return PA_ERR_INVALID_ARG;
+    unsigned int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int v = 0;
+    if (cudaMemcpyAsync(&v, err, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (clear && cudaMemsetAsync(err, 0, sizeof v, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+    *code = static_cast<int>(v);
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,111 @@
+// Slot addressing and the KV-cache write (reshape_and_cache).
+//
+// "vLLM 在 CANN 上的推理优化", section "vLLM 的 PagedAttention 数据结构":
+// a token's logical index splits into logical block (index / block_size) and
+// offset (index % block_size); the block table gives the physical block; the
+// token's slot is physical block * block_size + offset.  "vLLM-Ascend 原理"
+// section 2.3 ("KV 写缓存") and 2.4 ("KV 追加写"): each new token's k and v are
+// stored into that slot of the separate K and V pools.
+#include "pa_device.cuh"
+
+namespace pa {
+
+// One warp per sequence; lanes stride over the sequence's new tokens.
+__global__ void __launch_bounds__(128) slot_mapping_kernel(int64_t* __restrict__ slots,
+                                                           const int32_t* __restrict__ block_tables,
+                                                           int max_blocks, const int32_t* __restrict__ seq_lens,
+                                                           const int32_t* __restrict__ cu_q_lens, int num_seqs,
+                                                           int num_blocks, unsigned int* err) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= num_seqs) return;
+    const int b = warp;
+    const int n = seq_lens[b];
+    int row0, ql;
+    if (cu_q_lens) {
+        row0 = cu_q_lens[b];
+        ql = cu_q_lens[b + 1] - row0;
+    } else {
+        row0 = b;
+        ql = 1;
+    }
+    if (ql <= 0) return;
+    const bool seq_ok = n >= ql && n <= max_blocks * 16;
+    if (!seq_ok && lane == 0) record_error(err, PA_DEVERR_SEQ_LEN_);
+    for (int i = lane; i < ql; i += 32) {
+        int64_t slot = -1;
+        if (seq_ok) {
+            const int pos = n - ql + i;
+            const int blk = block_tables[static_cast<int64_t>(b) * max_blocks + (pos >> 4)];
+            if (blk >= 0 && blk < num_blocks)
+                slot = static_cast<int64_t>(blk) * 16 + (pos & 15);
+            else
+                record_error(err, PA_DEVERR_BLOCK_ID_);
+        }
+        slots[row0 + i] = slot;
+    }
+}
+
+// Each thread moves 16-byte chunks; chunk index = ((t * H) + h) * (D / 8) + c.
+// K and V are handled by the same thread (two independent streams of loads).
+template <int D>
+__global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__ key,
+                                                       const uint4* __restrict__ value,
+                                                       uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                                       const int64_t* __restrict__ slots, int num_tokens,
+                                                       int num_kv_heads, int64_t num_slots, unsigned int* err) {
+    constexpr int CPR = D / 8;  // 16-byte chunks per (token, head) row
+    const int64_t row_chunks = static_cast<int64_t>(num_kv_heads) * CPR;
+    const int64_t total = static_cast<int64_t>(num_tokens) * row_chunks;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / row_chunks;
+        const int64_t within = i - t * row_chunks;  // h * CPR + c
+        const int64_t slot = __ldg(slots + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (within == 0) record_error(err, PA_DEVERR_SLOT_);
+            continue;
+        }
+        const int64_t dst = slot * row_chunks + within;
+        const uint4 kv = __ldg(key + i);
+        const uint4 vv = __ldg(value + i);
+        k_cache[dst] = kv;
+        v_cache[dst] = vv;
+    }
+}
+
+cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_tables, int max_blocks,
+                                const int32_t* seq_lens, const int32_t* cu_q_lens, int num_seqs,
+                                int num_tokens, int num_blocks, unsigned int* err, cudaStream_t s) {
+    (void)num_tokens;
+    if (num_seqs == 0) return cudaSuccess;
+    const int threads = 128;
+    const int blocks = (num_seqs * 32 + threads - 1) / threads;
+    slot_mapping_kernel<<<blocks, threads, 0, s>>>(slots, block_tables, max_blocks, seq_lens, cu_q_lens,
+                                                   num_seqs, num_blocks, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kv_write(const void* key, const void* value, void* k_cache, void* v_cache,
+                            const int64_t* slots, int num_tokens, int num_blocks, int num_kv_heads,
+                            int head_dim, unsigned int* err, cudaStream_t s) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * (head_dim / 8);
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    const int64_t cap = 152LL * 16;  // a few waves of the GPU; the loop strides the rest
+    if (blocks > cap) blocks = cap;
+    const int64_t num_slots = static_cast<int64_t>(num_blocks) * 16;
+    if (head_dim == 128)
+        kv_write_kernel<128><<<static_cast<int>(blocks), threads, 0, s>>>(
+            static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
+            static_cast<uint4*>(v_cache), slots, num_tokens, num_kv_heads, num_slots, err);
+    else
+        kv_write_kernel<64><<<static_cast<int>(blocks), threads, 0, s>>>(
+            static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
+            static_cast<uint4*>(v_cache), slots, num_tokens, num_kv_heads, num_slots, err);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,69 @@
+// Internal (non-ABI) declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+// Device error word bits (mirrors the PA_DEVERR_* values of the public header).
+#define PA_DEVERR_BLOCK_ID_ 1u
+#define PA_DEVERR_SLOT_ 2u
+#define PA_DEVERR_SEQ_LEN_ 4u
+#define PA_DEVERR_TIMEOUT_ 8u
+
+namespace pa {
+
+struct DecodeParams {
+    void* out;                    // [rows, Hq, D]
+    const void* q;                // [rows, Hq, D]
+    const int32_t* block_tables;  // [B, max_blocks]
+    const int32_t* seq_lens;      // [B]
+    const int32_t* cu_q_lens;     // [B+1] or nullptr (row b = sequence b)
+    float* ws_m;                  // [B, Hq, max_parts] running max (log2 units)
+    float* ws_l;                  // [B, Hq, max_parts] running sum
+    float* ws_acc;                // [B, Hq, max_parts, D] unnormalised accumulator
+    unsigned int* err;            // device error word
+    int num_seqs;
+    int max_blocks;
+    int max_seq_len;
+    int num_blocks;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;                    // num_q_heads / num_kv_heads
+    int partition_tokens;         // multiple of 16
+    int max_parts;                // ceil(max_seq_len / partition_tokens)
+    float scale_log2;             // scale * log2(e)
+};
+
+struct PrefillParams {
+    void* out;                    // [T, Hq, D]
+    const void* q;                // [T, Hq, D]
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    const int32_t* cu_q_lens;     // [B+1]
+    unsigned int* err;
+    int num_seqs;
+    int max_blocks;
+    int max_seq_len;
+    int num_blocks;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;
+    int q_per_tile;               // queries per CTA tile (rows = q_per_tile * group <= 64)
+    float scale_log2;
+};
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_tables, int max_blocks,
+                                const int32_t* seq_lens, const int32_t* cu_q_lens, int num_seqs,
+                                int num_tokens, int num_blocks, unsigned int* err, cudaStream_t s);
+cudaError_t launch_kv_write(const void* key, const void* value, void* k_cache, void* v_cache,
+                            const int64_t* slots, int num_tokens, int num_blocks, int num_kv_heads,
+                            int head_dim, unsigned int* err, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          int head_dim, int dtype, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           int head_dim, int dtype, int max_q_len, cudaStream_t s);
+
+}  // namespace pa

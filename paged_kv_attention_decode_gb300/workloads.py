@@ -125,9 +125,10 @@ def _blocks_for(n: np.ndarray, bs: int) -> np.ndarray:
     return (-(-n.astype(np.int64) // bs)).astype(np.int64)
 
 
-def _fill_normal(t: torch.Tensor, gen: torch.Generator, chunk_rows: int = 1 << 16) -> None:
-    """Fill ``t`` (any float dtype) with N(0,1) drawn in fp32, chunked over dim 0."""
+def _fill_normal(t: torch.Tensor, gen: torch.Generator, chunk_elems: int = 1 << 26) -> None:
+    """Fill ``t`` (any float dtype) with N(0,1) drawn in fp32, in chunks of dim-0 rows."""
     flat = t.view(t.shape[0], -1)
+    chunk_rows = max(1, chunk_elems // max(1, flat.shape[1]))
     for r0 in range(0, flat.shape[0], chunk_rows):
         r1 = min(flat.shape[0], r0 + chunk_rows)
         tmp = torch.randn((r1 - r0, flat.shape[1]), generator=gen, device=t.device, dtype=torch.float32)

@@ -1,0 +1,117 @@
+"""Host-side checks of the C ABI (no GPU needed: nothing here launches work).
+
+The library must load on a machine without a GPU, export every function the
+header declares, and reject bad arguments on the host before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_attention_decode_gb300 as pa
+from paged_kv_attention_decode_gb300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_binding.library_path()):
+        from paged_kv_attention_decode_gb300 import build_lib
+        build_lib.build()
+    return _binding.load_library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_path(lib):
+    names = header_functions()
+    for want in ("pa_slot_mapping", "pa_paged_kv_write", "pa_paged_attention_decode",
+                 "pa_paged_attention_prefill", "pa_decode_workspace_bytes", "pa_get_device_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(_binding.library_path())
+    missing = [n for n in header_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_strings(lib):
+    assert lib.pa_version() >= 100
+    assert lib.pa_status_string(0) == b"PA_OK"
+    assert lib.pa_status_string(3) == b"PA_ERR_WORKSPACE_TOO_SMALL"
+    assert lib.pa_status_string(99) == b"PA_ERR_UNKNOWN"
+
+
+def _align(x):
+    return (x + 255) // 256 * 256
+
+
+def test_workspace_sizes(lib):
+    assert pa.decode_workspace_bytes(64, 32, 128, 512, 512) == 0       # one partition: no scratch
+    n = 64 * 32 * 8
+    assert pa.decode_workspace_bytes(64, 32, 128, 4096, 512) == 2 * _align(n * 4) + _align(n * 128 * 4)
+    n = 8 * 64 * 256
+    assert pa.decode_workspace_bytes(8, 64, 128, 131072, 0) == 2 * _align(n * 4) + _align(n * 128 * 4)
+    assert pa.prefill_workspace_bytes(8, 64, 128, 131072) == pa.decode_workspace_bytes(8, 64, 128, 131072, 0)
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced on rejected calls
+
+
+def _decode(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, maxb=4, sl=FAKE, B=2, maxlen=64, nb=8,
+             scale=0.1, hq=4, hkv=2, d=128, bs=16, part=0, ws=None, wsb=0, dt=0)
+    a.update(kw)
+    return lib.pa_paged_attention_decode(a["out"], a["q"], a["k"], a["v"], a["bt"], a["maxb"], a["sl"],
+                                         a["B"], a["maxlen"], a["nb"], a["scale"], a["hq"], a["hkv"],
+                                         a["d"], a["bs"], a["part"], a["ws"], a["wsb"], a["dt"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dt=7), 2), (dict(d=96), 2), (dict(bs=32), 2), (dict(hq=5, hkv=2), 1),
+    (dict(hq=32, hkv=2), 2), (dict(part=17), 1), (dict(part=-16), 1), (dict(q=None), 1),
+    (dict(out=FAKE + 2), 1), (dict(B=-1), 1), (dict(nb=0), 1), (dict(scale=float("nan")), 1),
+    (dict(maxlen=4096, part=512), 3), (dict(maxlen=4096, ws=FAKE, wsb=10), 3),
+    (dict(B=0), 0),
+])
+def test_decode_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _decode(lib, **kw) == status
+
+
+def test_write_and_slot_mapping_reject_bad_arguments(lib):
+    w = lib.pa_paged_kv_write
+    assert w(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 96, 16, 0, None) == 2
+    assert w(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 128, 8, 0, None) == 2
+    assert w(FAKE, FAKE, FAKE, FAKE, None, 4, 8, 2, 128, 16, 0, None) == 1
+    assert w(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 8, 2, 128, 16, 0, None) == 0
+    s = lib.pa_slot_mapping
+    assert s(FAKE, FAKE, 4, FAKE, None, 3, 5, 8, 16, None) == 1     # decode form needs T == B
+    assert s(FAKE, FAKE, 4, FAKE, None, 3, 3, 8, 32, None) == 2
+    assert s(FAKE, FAKE, 4, FAKE, None, 0, 0, 8, 16, None) == 0
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    p = lib.pa_paged_attention_prefill
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 10, 8, 64, 8, 0.1, 8, 2, 128, 16, None, 0, 1, None]
+    bad = list(args)
+    bad[7] = None        # cu_q_lens
+    assert p(*bad) == 1
+    bad = list(args)
+    bad[14], bad[15] = 9, 3   # group 3 is fine, 9 % 3 == 0, but check head_dim
+    bad[16] = 80
+    assert p(*bad) == 2
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(_binding.PagedAttnError):
+        _binding.load_library()

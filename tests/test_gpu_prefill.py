@@ -1,0 +1,58 @@
+"""GPU parity of chunked-prefill (causal, varlen, on cached prefixes) and of
+the mixed prefill + decode step against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_attention_decode_gb300 as pa
+from paged_kv_attention_decode_gb300 import workloads as W
+from tests._gpu_util import TOL, gpu_step, max_err, oracle_rows, snapshot
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+# (q_len, cached prefix) per sequence: chunks shorter and longer than a tile,
+# ragged block and tile tails, empty and long prefixes, decode rows mixed in.
+CASES = [(2, 0), (17, 0), (64, 0), (65, 3), (100, 200), (1, 50), (130, 1000), (33, 15), (1, 1), (300, 17)]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,dtype", [
+    (8, 2, 128, "bf16"), (4, 4, 64, "f16"), (32, 8, 128, "bf16"), (8, 1, 64, "bf16"), (6, 2, 128, "f16"),
+    (16, 2, 128, "f16"),
+])
+def test_prefill_parity(Hq, Hkv, D, dtype):
+    q_lens = [c[0] for c in CASES]
+    seq_lens = [c[0] + c[1] for c in CASES]
+    w = W.build_workload(name="pre", seq_lens=seq_lens, q_lens=q_lens, num_q_heads=Hq, num_kv_heads=Hkv,
+                         head_dim=D, dtype=dtype, seed=Hq + 17 * D, device=DEV, poison=True, pool_slack=0.2)
+    seqs = np.arange(w.batch)
+    snap = snapshot(w, seqs)
+    _, out = gpu_step(w, prefill=True)
+    rows, ref = oracle_rows(w, seqs, snap)
+    err = max_err(out[torch.from_numpy(rows).to(DEV)], ref)
+    assert err <= TOL[dtype], err
+    assert pa.device_error() == 0
+
+
+def test_mixed_step_small():
+    w = W.make("mixed", device=DEV, poison=True, n_prefill=3, chunk=150, n_decode=40, prefix_hi=700,
+               dec_lo=1, dec_hi=900)
+    seqs = np.arange(w.batch)
+    snap = snapshot(w, seqs)
+    _, out = gpu_step(w)
+    rows, ref = oracle_rows(w, seqs, snap)
+    err = max_err(out[torch.from_numpy(rows).to(DEV)], ref)
+    assert err <= TOL["bf16"], err
+    assert pa.device_error() == 0
+
+
+def test_pure_prefill_without_prefix_matches_decode_of_last_row():
+    w = W.build_workload(name="pp", seq_lens=[77, 200], q_lens=[77, 200], num_q_heads=8, num_kv_heads=8,
+                         head_dim=128, dtype="f16", seed=21, device=DEV)
+    _, out = gpu_step(w, prefill=True)
+    last = torch.tensor([76, 276], device=DEV)
+    bt = torch.from_numpy(w.block_tables).to(DEV)
+    sl = torch.from_numpy(w.seq_lens).to(DEV)
+    dec = pa.paged_attention_decode(w.q[last].contiguous(), w.k_cache, w.v_cache, bt, sl, w.scale, 200)
+    torch.cuda.synchronize()
+    assert float((out[last].float() - dec.float()).abs().max()) <= 2e-3
