@@ -134,40 +134,41 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def cpu_baseline(w, seconds: float = 10.0, seq_budget: int = 64) -> dict:
+def cpu_baseline(w, seconds: float = 10.0) -> dict:
     """Time the fp64 oracle (as it stands) on the host cores over whole
     sequences of the same workload: slot mapping, KV write and decode
-    attention of each sampled sequence."""
+    attention of each sampled sequence, cycling through the batch until about
+    `seconds` of CPU time have been spent."""
     import oracle
     import torch
 
-    rng = np.random.default_rng(7)
-    order = rng.permutation(w.batch)
-    done = 0
-    t_total = 0.0
-    i = 0
-    while (t_total < seconds and done < seq_budget) or done == 0:
-        b = int(order[i % w.batch])
-        i += 1
+    def u16(t):
+        return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+    snaps = []
+    for b in np.random.default_rng(7).permutation(w.batch)[: min(w.batch, 64)]:
+        b = int(b)
         nb = -(-int(w.seq_lens[b]) // 16)
         idx = torch.from_numpy(w.block_tables[b, :nb].astype(np.int64)).to(w.k_cache.device)
-        kc = w.k_cache.index_select(0, idx).cpu().view(torch.int16).numpy().view(np.uint16)
-        vc = w.v_cache.index_select(0, idx).cpu().view(torch.int16).numpy().view(np.uint16)
+        snaps.append((b, nb, u16(w.k_cache.index_select(0, idx)), u16(w.v_cache.index_select(0, idx)),
+                      u16(w.q[b:b + 1]), u16(w.key[b:b + 1]), u16(w.value[b:b + 1])))
+    done = tokens = 0
+    t_total = 0.0
+    while t_total < seconds or done == 0:
+        b, nb, kc, vc, q, key, val = snaps[done % len(snaps)]
         tables = np.arange(nb, dtype=np.int32)[None, :]
         sl = w.seq_lens[b:b + 1]
-        q = w.q[b:b + 1].cpu().view(torch.int16).numpy().view(np.uint16)
-        key = w.key[b:b + 1].cpu().view(torch.int16).numpy().view(np.uint16)
-        val = w.value[b:b + 1].cpu().view(torch.int16).numpy().view(np.uint16)
         t0 = time.perf_counter()
         slots = oracle.slot_mapping(tables, sl, np.ones(1, np.int32), 16, nb)
         oracle.kv_write(key, val, kc, vc, slots)
         oracle.paged_attention_decode(q, kc, vc, tables, sl, w.scale, w.dtype)
         t_total += time.perf_counter() - t0
         done += 1
+        tokens += int(sl[0])
     return {"value": done / t_total, "unit": UNIT, "cores": oracle.num_threads(0), "kind": "oracle",
-            "sample": f"{done} whole sequences of the workload (all {w.num_q_heads} heads, mean ctx "
-                      f"{int(w.seq_lens.mean())}), slot mapping + KV write + decode attention, fp64, "
-                      f"{t_total:.1f} s of CPU time"}
+            "sample": f"{done} whole sequences drawn from the workload ({len(snaps)} distinct, all "
+                      f"{w.num_q_heads} heads, {tokens / done:.0f} context tokens on average): slot mapping "
+                      f"+ KV write + decode attention in fp64, {t_total:.1f} s of CPU time"}
 
 
 def run_reference(args):
@@ -181,7 +182,8 @@ def run_reference(args):
 
     import torch
 
-    w = W.make(args.workload, device="cpu")
+    kw = {"batch": args.batch} if args.batch else {}
+    w = W.make(args.workload, device="cpu", **kw)
     bt = w.block_tables
 
     def u16(t):
@@ -238,7 +240,8 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     pa.load_library()
 
-    w = W.make(args.workload, device=dev)
+    kw = {"batch": args.batch} if args.batch else {}
+    w = W.make(args.workload, device=dev, **kw)
     B = w.batch
     bt = torch.from_numpy(w.block_tables).to(dev)
     sl = torch.from_numpy(w.seq_lens).to(dev)
@@ -377,6 +380,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="llama7b_decode")
     ap.add_argument("--partition", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -165,6 +165,40 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
                                void* stream);
 
 /*
+ * Decode attention for callers that cannot allocate device memory.
+ *
+ * No counterpart in the pages: this is a deployment variant of
+ * pa_paged_attention_decode.  Some callers cannot call cudaMalloc when they
+ * run a step: an inference runtime that handed all remaining HBM to its own
+ * pool (the KV block pool usually takes everything left) and so has nothing
+ * to give a library, or a plugin inside a host framework whose interface
+ * forbids device allocation by extensions.  This entry point takes the same
+ * arguments as pa_paged_attention_decode minus the workspace and keeps the
+ * split-context partials in a fixed scratch array of PA_NOALLOC_SCRATCH_BYTES
+ * that the library holds on every GPU where it is loaded, until the process
+ * exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *  - Sizes whose partials need more than PA_NOALLOC_SCRATCH_BYTES
+ *    (pa_decode_workspace_bytes(...) > PA_NOALLOC_SCRATCH_BYTES) are rejected
+ *    with PA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *  - The first call on a device looks up that device's scratch address
+ *    (once per device, with the device current); make that first call before
+ *    any stream capture.
+ *  - Every call on a device shares the one scratch array and it keeps the
+ *    last call's contents.  Nothing in it needs to start at zero (each call
+ *    writes every partial before reading it), but calls whose work overlaps
+ *    on the GPU (two streams, two host threads) race on it: serialise them.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+int pa_paged_attention_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                                      int max_seq_len, int num_blocks, float scale,
+                                      int num_q_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int partition_size, int dtype, void* stream);
+
+/*
  * Read the device error word (PA_DEVERR_* bits) of the current device after
  * the work queued on `stream` has finished; `clear` != 0 resets it to 0.
  * This call synchronises the stream.

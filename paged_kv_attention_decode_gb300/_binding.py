@@ -39,6 +39,8 @@ _SIGNATURES = {
                                           _i32, _i32, _f32, _i32, _i32, _i32, _i32, _p, _sz,
                                           _i32, _p]),
     "pa_get_device_error": (_i32, [ctypes.POINTER(_i32), _i32, _p]),
+    "pa_paged_attention_decode_noalloc": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _f32,
+                                                 _i32, _i32, _i32, _i32, _i32, _i32, _p]),
 }
 
 
