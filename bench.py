@@ -48,15 +48,36 @@ def _dist():
 
 
 def _algorithmic_bytes(w) -> dict:
-    """Bytes the decode attention must move per launch: every live K/V row of
-    every sequence once, the queries, the outputs, the live table entries and
-    the lengths."""
+    """Bytes the attention launch must move: every live K/V row once per kv
+    head (a block shared by several sequences counts once: `kv_unique`; once
+    per sequence that reads it: `kv`), the query rows, the output rows, the
+    live table entries and the lengths."""
     n = w.seq_lens.astype(np.int64)
-    kv = int(n.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
-    q = w.batch * w.num_q_heads * w.head_dim * 2
+    row = w.num_kv_heads * w.head_dim * 2 * 2          # K and V bytes of one token
+    kv = int(n.sum()) * row
+    rows_per_block = {}
+    for b in range(w.batch):
+        nb = -(-int(n[b]) // 16)
+        for j in range(nb):
+            blk = int(w.block_tables[b, j])
+            rows_per_block[blk] = max(rows_per_block.get(blk, 0), min(16, int(n[b]) - 16 * j))
+    kv_unique = sum(rows_per_block.values()) * row
+    q = w.num_tokens * w.num_q_heads * w.head_dim * 2
     live_entries = int((-(-n // 16)).sum())
-    meta = live_entries * 4 + w.batch * 4
-    return {"kv": kv, "q": q, "out": q, "meta": meta, "total": kv + 2 * q + meta}
+    meta = live_entries * 4 + w.batch * 4 * (1 if w.is_decode else 2)
+    return {"kv": kv, "kv_unique": kv_unique, "q": q, "out": q, "meta": meta,
+            "total": kv_unique + 2 * q + meta, "total_logical": kv + 2 * q + meta}
+
+
+def _prefill_flops(w) -> float:
+    """Dense-contraction FLOPs of the chunked-prefill rows: for a chunk of C
+    new tokens on P cached ones, Hq * 4 * D * (C * P + C * (C + 1) / 2)."""
+    f = 0.0
+    for n, c in zip(w.seq_lens.astype(np.float64), w.q_lens.astype(np.float64)):
+        if c > 1:
+            p = n - c
+            f += w.num_q_heads * 4.0 * w.head_dim * (c * p + c * (c + 1) / 2)
+    return f
 
 
 def _source_hash() -> str:
@@ -171,6 +192,12 @@ def cpu_baseline(w, seconds: float = 10.0) -> dict:
                       f"+ KV write + decode attention in fp64, {t_total:.1f} s of CPU time"}
 
 
+def _workload_kw(args) -> dict:
+    if not args.batch:
+        return {}
+    return {"n_decode": args.batch} if args.workload == "mixed" else {"batch": args.batch}
+
+
 def run_reference(args):
     """--impl reference: the oracle on the host cores, one whole sequence per step."""
     import oracle
@@ -182,8 +209,10 @@ def run_reference(args):
 
     import torch
 
-    kw = {"batch": args.batch} if args.batch else {}
-    w = W.make(args.workload, device="cpu", **kw)
+    w = W.make(args.workload, device="cpu", **_workload_kw(args))
+    if not w.is_decode:
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm times decode workloads only"}))
+        return 0
     bt = w.block_tables
 
     def u16(t):
@@ -240,31 +269,43 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     pa.load_library()
 
-    kw = {"batch": args.batch} if args.batch else {}
-    w = W.make(args.workload, device=dev, **kw)
+    w = W.make(args.workload, device=dev, **_workload_kw(args))
     B = w.batch
+    T = w.num_tokens
+    decode = w.is_decode
     bt = torch.from_numpy(w.block_tables).to(dev)
     sl = torch.from_numpy(w.seq_lens).to(dev)
-    slots = torch.empty(B, dtype=torch.int64, device=dev)
+    cu = None if decode else torch.from_numpy(w.cu_q_lens).to(dev)
+    slots = torch.empty(T, dtype=torch.int64, device=dev)
     out = torch.empty_like(w.q)
-    nbytes = pa.decode_workspace_bytes(B, w.num_q_heads, w.head_dim, w.max_seq_len, args.partition)
+    if decode:
+        nbytes = pa.decode_workspace_bytes(B, w.num_q_heads, w.head_dim, w.max_seq_len, args.partition)
+    else:
+        nbytes = pa.prefill_workspace_bytes(B, w.num_q_heads, w.head_dim, w.max_seq_len)
     wsp = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
     max_len = w.max_seq_len
     stream = torch.cuda.current_stream()
 
     def step():
-        pa.slot_mapping(bt, sl, None, B, w.num_blocks, out=slots)
+        pa.slot_mapping(bt, sl, cu, T, w.num_blocks, out=slots)
         pa.paged_kv_write(w.key, w.value, w.k_cache, w.v_cache, slots)
 
-    def attend():
-        pa.paged_attention_decode(w.q, w.k_cache, w.v_cache, bt, sl, w.scale, max_len, out=out,
-                                  partition_size=args.partition, workspace=wsp)
+    def attend(q=None, btab=None, lens=None, cul=None):
+        q = w.q if q is None else q
+        btab = bt if btab is None else btab
+        lens = sl if lens is None else lens
+        if decode:
+            pa.paged_attention_decode(q, w.k_cache, w.v_cache, btab, lens, w.scale, max_len, out=out,
+                                      partition_size=args.partition, workspace=wsp)
+        else:
+            pa.paged_attention_prefill(q, w.k_cache, w.v_cache, btab, lens, cu if cul is None else cul,
+                                       w.scale, w.max_q_len, max_len, out=out, workspace=wsp)
 
     for _ in range(args.warmup):
         step()
         attend()
     torch.cuda.synchronize()
-    launches_per_step = 3 + (1 if nbytes > 0 else 0)
+    launches_per_step = (3 if decode else 4) + (1 if nbytes > 0 else 0)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -292,7 +333,7 @@ def run_ours(args):
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t)
-    value = ws * B * args.steps / (total_ms / 1e3)
+    value = ws * T * args.steps / (total_ms / 1e3)
 
     # ---- end to end through the public API with host buffers -------------
     q_h = w.q.cpu().pin_memory()
@@ -307,16 +348,22 @@ def run_ours(args):
     d2h = out_h.numel() * out_h.element_size()
     e2e_steps = max(10, min(args.steps, 500))
 
+    cu_h = None if decode else torch.from_numpy(w.cu_q_lens).pin_memory()
+    cu_d = None if decode else torch.empty_like(cu)
+    if cu_h is not None:
+        h2d += cu_h.numel() * cu_h.element_size()
+
     def e2e_step():
         q_d.copy_(q_h, non_blocking=True)
         k_d.copy_(k_h, non_blocking=True)
         v_d.copy_(v_h, non_blocking=True)
         bt_d.copy_(bt_h, non_blocking=True)
         sl_d.copy_(sl_h, non_blocking=True)
-        pa.slot_mapping(bt_d, sl_d, None, B, w.num_blocks, out=slots)
+        if cu_d is not None:
+            cu_d.copy_(cu_h, non_blocking=True)
+        pa.slot_mapping(bt_d, sl_d, cu_d, T, w.num_blocks, out=slots)
         pa.paged_kv_write(k_d, v_d, w.k_cache, w.v_cache, slots)
-        pa.paged_attention_decode(q_d, w.k_cache, w.v_cache, bt_d, sl_d, w.scale, max_len, out=out,
-                                  partition_size=args.partition, workspace=wsp)
+        attend(q_d, bt_d, sl_d, cu_d)
         out_h.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -332,7 +379,7 @@ def run_ours(args):
         t = torch.tensor([e2e_s], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t)
-    e2e_value = ws * B * e2e_steps / e2e_s
+    e2e_value = ws * T * e2e_steps / e2e_s
 
     if rank != 0:
         if dist:
@@ -342,29 +389,36 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     ab = _algorithmic_bytes(w)
     achieved = ab["total"] / (attn_ms / 1e3) / 1e9
+    ctx = (f"U[512,4096] (mean {int(w.seq_lens.mean())})" if args.workload == "llama7b_decode"
+           else f"mean {int(w.seq_lens.mean())}, max {w.max_seq_len}")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": args.workload, "batch": B, "ctx": f"U[512,4096] (mean {int(w.seq_lens.mean())})"
-                   if args.workload == "llama7b_decode" else f"max {w.max_seq_len}",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16" if w.dtype == "f16" else "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch": B, "new_tokens_per_step": T, "ctx": ctx,
                    "heads": f"{w.num_q_heads}/{w.num_kv_heads}", "head_dim": w.head_dim, "block_size": 16,
-                   "partition": args.partition or 512, "pool_blocks": w.num_blocks,
+                   "partition": (args.partition or 512), "pool_blocks": w.num_blocks,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": f"inputs larger than L2: {ab['kv'] / 1e9:.2f} GB of KV read per step"},
+                   "l2": f"inputs larger than L2: {ab['kv_unique'] / 1e9:.2f} GB of KV read per step"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _traffic_per_launch(args.workload),
-                     "kernel": "decode attention (partition kernel + log-sum-exp reduce)",
+                     "kernel": ("decode attention (partition kernel + log-sum-exp reduce)" if decode else
+                                "attention call (decode rows: partition + reduce kernels; chunks: prefill kernel)"),
                      "peak_kind": f"{peak_kind} HBM copy", "frac_of_8TBs_spec": achieved / SPEC_HBM_GBS,
                      "algorithmic_bytes_per_launch": ab["total"], "ms_per_launch": attn_ms},
         "write_ms_per_step": write_ms,
-        "attention_tokens_per_s": B / (attn_ms / 1e3),
+        "attention_tokens_per_s": T / (attn_ms / 1e3),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
-    if ws == 1 and not args.no_cpu_baseline:
+    if ab["kv"] != ab["kv_unique"]:
+        line["roofline"]["logical_gbs"] = ab["total_logical"] / (attn_ms / 1e3) / 1e9
+    if not decode:
+        line["prefill_gflop_per_step"] = _prefill_flops(w) / 1e9
+    if ws == 1 and decode and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, seconds=args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if dist:

@@ -43,8 +43,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Tensor map over one pool [num_blocks * 16 token rows, Hkv, D] viewed as 4-D
-// (64-element row piece, D/64 pieces, head, token slot); one box = the 16 rows
-// of one (block, head), 128-byte swizzled.
+// (64-element row piece, D/64 pieces, head, token slot); one box = one 64-dim
+// half of the 16 rows of one (block, head), 128-byte swizzled.
 bool make_kv_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads, int head_dim, int dtype) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -52,7 +52,7 @@ bool make_kv_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_
                                 static_cast<cuuint64_t>(num_blocks) * 16};
     const cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(head_dim) * 2,
                                    static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
-    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(head_dim / 64), 1, 16};
+    const cuuint32_t box[4] = {64, 1, 1, 16};   // one 64-dim half of a (block, head) tile
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

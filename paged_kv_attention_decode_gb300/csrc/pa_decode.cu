@@ -13,8 +13,9 @@
 //  * grid (partition, kv head, sequence); a CTA handles the `group` query
 //    heads that share one kv head, so every K/V byte is read once.
 //  * each warp owns a private ring of STAGES shared-memory slots; its lane 0
-//    fetches whole (16-token block, kv head) tiles of K and V with one 4-D TMA
-//    each (128-byte swizzle), completing on a per-slot mbarrier.
+//    fetches whole (16-token block, kv head) tiles of K and V with 4-D TMA
+//    loads (one per 64-dim half, 128-byte swizzle), completing on a per-slot
+//    mbarrier.
 //  * MHA (group 1): fp32 FMA dot products, a 16-way transpose-reduction
 //    across the warp (16 shuffles per block), register-resident (m, l, acc).
 //  * GQA (group 2..8): the query group x K-block product is a dense
@@ -50,8 +51,12 @@ __device__ __forceinline__ void issue_tile(const WarpRing& ring, int slot, int p
                                           const CUtensorMap* kmap, const CUtensorMap* vmap) {
     uint8_t* dst = ring.base + slot * DecodeShape<D>::kStageBytes;
     mbar_arrive_expect_tx(&ring.bars[slot], DecodeShape<D>::kStageBytes);
-    tma_load_4d(dst, kmap, &ring.bars[slot], 0, 0, kv_head, phys * 16);
-    tma_load_4d(dst + DecodeShape<D>::kTileBytes, vmap, &ring.bars[slot], 0, 0, kv_head, phys * 16);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+        tma_load_4d(dst + h * TileGeom<D>::kHalfBytes, kmap, &ring.bars[slot], 0, h, kv_head, phys * 16);
+        tma_load_4d(dst + DecodeShape<D>::kTileBytes + h * TileGeom<D>::kHalfBytes, vmap, &ring.bars[slot], 0, h,
+                    kv_head, phys * 16);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -229,9 +234,12 @@ struct MmaState {
         if (nvalid < 16) {
             // rows past the sequence end may hold anything (even NaN): p = 0
             // there, but 0 * NaN would poison the product, so clear them.
-            uint4* z = reinterpret_cast<uint4*>(vt + nvalid * D * 2);
-            const int nchunks = (16 - nvalid) * D * 2 / 16;
-            for (int i = lane; i < nchunks; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+            const int nchunks = (16 - nvalid) * 8;   // 16-byte chunks per half
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {
+                uint4* z = reinterpret_cast<uint4*>(vt + h * TileGeom<D>::kHalfBytes + nvalid * 128);
+                for (int i = lane; i < nchunks; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+            }
             __syncwarp();
         }
         {
@@ -466,9 +474,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     }
 }
 
-// Merge the partitions of each (sequence, q head): out = sum_p acc_p 2^(m_p - M) / sum_p l_p 2^(m_p - M).
+// Merge the partitions of each (sequence, q head):
+// out = sum_p acc_p 2^(m_p - M) / sum_p l_p 2^(m_p - M), M = max_p m_p.
+// The per-partition weights are formed once in shared memory; each thread then
+// streams one head dimension of every partition's accumulator.
+constexpr int kReduceMaxParts = 1024;   // partitions staged in shared memory per pass
+
 template <typename T, int D>
 __global__ void __launch_bounds__(D) decode_reduce_kernel(const DecodeParams p) {
+    __shared__ float sc[kReduceMaxParts];
+    __shared__ float red[D / 32];
     const int hq = blockIdx.x;
     const int b = blockIdx.y;
     const int d = threadIdx.x;
@@ -487,14 +502,46 @@ __global__ void __launch_bounds__(D) decode_reduce_kernel(const DecodeParams p) 
     const float* wm = p.ws_m + base;
     const float* wl = p.ws_l + base;
     const float* wa = p.ws_acc + base * D;
+
+    // M = max_p m_p (block reduction)
     float M = -INFINITY;
-    for (int i = 0; i < nparts; ++i) M = fmaxf(M, wm[i]);
+    for (int i = d; i < nparts; i += D) M = fmaxf(M, wm[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    if ((d & 31) == 0) red[d >> 5] = M;
+    __syncthreads();
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
+    __syncthreads();
+
     float L = 0.f, A = 0.f;
     if (M != -INFINITY) {
-        for (int i = 0; i < nparts; ++i) {
-            const float sc = fast_exp2(wm[i] - M);
-            L = fmaf(wl[i], sc, L);
-            A = fmaf(wa[static_cast<int64_t>(i) * D + d], sc, A);
+        for (int p0 = 0; p0 < nparts; p0 += kReduceMaxParts) {
+            const int np = min(kReduceMaxParts, nparts - p0);
+            float lpart = 0.f;
+            for (int i = d; i < np; i += D) {
+                const float s = fast_exp2(wm[p0 + i] - M);
+                sc[i] = s;
+                lpart = fmaf(wl[p0 + i], s, lpart);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) lpart += __shfl_xor_sync(kFull, lpart, off);
+            if ((d & 31) == 0) red[d >> 5] = lpart;
+            __syncthreads();
+#pragma unroll
+            for (int w = 0; w < D / 32; ++w) L += red[w];
+            const float* a = wa + static_cast<int64_t>(p0) * D + d;
+            int i = 0;
+            for (; i + 8 <= np; i += 8) {
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] = a[static_cast<int64_t>(i + u) * D];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) A = fmaf(x[u], sc[i + u], A);
+            }
+            for (; i < np; ++i) A = fmaf(a[static_cast<int64_t>(i) * D], sc[i], A);
+            __syncthreads();
         }
     }
     const float v = L > 0.f ? A / L : 0.f;

@@ -114,16 +114,28 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 // ---------------------------------------------------------------------------
 // K/V tile addressing.
 //
-// One TMA box is the 16 token rows of one (physical block, kv head), each row
-// head_dim 16-bit values.  The tensor map splits a row into D/64 pieces of
-// 128 bytes and applies the 128-byte swizzle, so a tile is (16 * D/64) rows of
-// 128 bytes where the 16-byte chunk c of 128-byte row r sits at chunk c ^ (r & 7).
+// A tile is the 16 token rows of one (physical block, kv head), head_dim
+// 16-bit values each.  It is fetched as D/64 TMA boxes, one per 64-dim half of
+// the row, so shared memory holds [half][16 tokens][128 bytes]; the tensor map
+// applies the 128-byte swizzle: 16-byte chunk c of the 128-byte row r sits at
+// chunk c ^ (r & 7).  Consecutive tokens of one half are consecutive rows, so
+// eight ldmatrix row addresses (eight tokens, one chunk) hit eight different
+// bank groups.  Rows of a multi-block stage continue across tiles (a tile is a
+// whole number of 1 KiB swizzle atoms), so token t of a stage is tile t / 16.
 // ---------------------------------------------------------------------------
 template <int D>
+struct TileGeom {
+    static constexpr int kHalfBytes = 16 * 128;           // one 64-dim half of a tile
+    static constexpr int kTileBytes = (D / 64) * kHalfBytes;
+};
+
+template <int D>
 __device__ __forceinline__ uint32_t tile_off(int tok, int dim) {
-    const int r = tok * (D / 64) + (dim >> 6);
+    const int tile = tok >> 4;
+    const int r = tok & 15;
     const int c = (dim & 63) >> 3;
-    return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4) + ((dim & 7) << 1));
+    return static_cast<uint32_t>(tile * TileGeom<D>::kTileBytes + (dim >> 6) * TileGeom<D>::kHalfBytes + r * 128 +
+                                 ((c ^ (r & 7)) << 4) + ((dim & 7) << 1));
 }
 
 // ---------------------------------------------------------------------------

@@ -11,7 +11,8 @@
 // GB300 design: one CTA per (query tile, kv head, sequence).  Its 64 rows are
 // (query, q head) pairs of one kv-head group, so a K/V tile is loaded once for
 // all the group's heads.  A producer warp gathers 64-token K/V tiles (four
-// 16-token blocks, one 4-D TMA each, 128-byte swizzle) into a two-stage ring;
+// 16-token blocks, 4-D TMA loads per 64-dim half, 128-byte swizzle) into a
+// two-stage ring;
 // four consumer warps run Q K^T and P V on the tensor cores (mma.sync
 // m16n8k16, fp32 accumulate) with an online softmax per row.  Only tiles on
 // the causal diagonal are masked.
@@ -132,9 +133,13 @@ __global__ void __launch_bounds__(kPreThreads, 2)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     if (phys[j] >= 0) {
-                        tma_load_4d(st + j * Shape::kBlockTile, &kmap, &full_bar[s], 0, 0, g, phys[j] * 16);
-                        tma_load_4d(st + Shape::kHalf + j * Shape::kBlockTile, &vmap, &full_bar[s], 0, 0, g,
-                                    phys[j] * 16);
+#pragma unroll
+                        for (int h = 0; h < D / 64; ++h) {
+                            tma_load_4d(st + j * Shape::kBlockTile + h * TileGeom<D>::kHalfBytes, &kmap,
+                                        &full_bar[s], 0, h, g, phys[j] * 16);
+                            tma_load_4d(st + Shape::kHalf + j * Shape::kBlockTile + h * TileGeom<D>::kHalfBytes,
+                                        &vmap, &full_bar[s], 0, h, g, phys[j] * 16);
+                        }
                     }
                 }
             }
