@@ -47,6 +47,21 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """Largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
+
+
+def replica_throughput(world_size: int, units_per_step: int, steps: int, slowest_ms: float) -> float:
+    """Units processed by all replicas per second, timed by the slowest rank."""
+    return world_size * units_per_step * steps / (slowest_ms / 1e3)
+
+
 def _algorithmic_bytes(w) -> dict:
     """Bytes the attention launch must move: every live K/V row once per kv
     head (a block shared by several sequences counts once: `kv_unique`; once
@@ -329,11 +344,8 @@ def run_ours(args):
     total_ms = ev[0][0].elapsed_time(ev[-1][2])
     attn_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / args.steps
     write_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in ev) / args.steps
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t)
-    value = ws * T * args.steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(total_ms, dist, dev)
+    value = replica_throughput(ws, T, args.steps, total_ms)
 
     # ---- end to end through the public API with host buffers -------------
     q_h = w.q.cpu().pin_memory()
@@ -375,11 +387,8 @@ def run_ours(args):
     for _ in range(e2e_steps):
         e2e_step()
     e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t)
-    e2e_value = ws * T * e2e_steps / e2e_s
+    e2e_s = max_over_ranks(e2e_s, dist, dev)
+    e2e_value = replica_throughput(ws, T, e2e_steps, e2e_s * 1e3)
 
     if rank != 0:
         if dist:
