@@ -140,7 +140,9 @@ int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, con
                               int head_dim, int block_size, int partition_size, void* workspace,
                               size_t workspace_bytes, int dtype, void* stream);
 
-/* Workspace for pa_paged_attention_prefill (the decode rows' partials). */
+/* Workspace for pa_paged_attention_prefill: the chunk tile work list
+ * (num_seqs + 1 int32) followed by the decode rows' split-context partials.
+ * Nonzero whenever num_seqs > 0. */
 size_t pa_prefill_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len);
 
 /*

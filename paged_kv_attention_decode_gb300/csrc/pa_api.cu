@@ -60,6 +60,26 @@ bool make_kv_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_
     return r == CUDA_SUCCESS;
 }
 
+// Tensor map over the query rows [T, Hq, D] viewed as 4-D (64-element row
+// piece, D/64 pieces, q head, token); one box = one 64-dim half of the `group`
+// heads of `q_per_tile` consecutive tokens, i.e. 128 rows of 128 bytes whose
+// row index is token * group + head.
+bool make_q_map(CUtensorMap* map, const void* q, int num_tokens, int num_q_heads, int head_dim, int group,
+                int q_per_tile, int dtype) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(head_dim / 64), static_cast<cuuint64_t>(num_q_heads),
+                                static_cast<cuuint64_t>(num_tokens)};
+    const cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(head_dim) * 2,
+                                   static_cast<cuuint64_t>(num_q_heads) * head_dim * 2};
+    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(q_per_tile)};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                    const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
@@ -218,8 +238,12 @@ int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, con
                        workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream));
 }
 
+// Prefill workspace: [tile work list: num_seqs + 1 int32, 256-aligned][decode-row partials].
+static size_t plan_bytes(int num_seqs) { return align256(static_cast<size_t>(num_seqs + 1) * sizeof(int32_t)); }
+
 size_t pa_prefill_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len) {
-    return pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len, 0);
+    if (num_seqs <= 0) return 0;
+    return plan_bytes(num_seqs) + pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len, 0);
 }
 
 int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -238,10 +262,15 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
     if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_q_lens) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t pb = plan_bytes(num_seqs);
+    if (!workspace || workspace_bytes < pa_prefill_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len))
+        return PA_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned256(workspace)) return PA_ERR_INVALID_ARG;
+    int32_t* plan = static_cast<int32_t*>(workspace);
     // decode rows (q_len == 1) through the decode kernel
     rc = decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens, num_seqs,
-                     max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, 0, workspace,
-                     workspace_bytes, dtype, s);
+                     max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, 0,
+                     static_cast<uint8_t*>(workspace) + pb, workspace_bytes - pb, dtype, s);
     if (rc) return rc;
     if (max_q_len <= 1) return PA_OK;
     unsigned int* err = error_word();
@@ -263,9 +292,20 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
     p.num_q_heads = num_q_heads;
     p.num_kv_heads = num_kv_heads;
     p.group = num_q_heads / num_kv_heads;
-    p.q_per_tile = 64 / p.group;
     p.scale_log2 = scale_log2(scale);
-    cudaError_t e = pa::launch_prefill(p, kmap, vmap, head_dim, dtype, max_q_len, s);
+    cudaError_t e;
+    if (p.group == 1 || p.group == 2 || p.group == 4 || p.group == 8) {
+        // 128-row tiles on the tcgen05 tensor cores
+        p.q_per_tile = 128 / p.group;
+        CUtensorMap qmap;
+        if (!make_q_map(&qmap, q, num_tokens, num_q_heads, head_dim, p.group, p.q_per_tile, dtype))
+            return PA_ERR_CUDA;
+        e = pa::launch_prefill_tc(p, plan, kmap, vmap, qmap, head_dim, dtype, max_q_len, num_tokens, s);
+    } else {
+        // other groupings: 64-row mma.sync tiles
+        p.q_per_tile = 64 / p.group;
+        e = pa::launch_prefill(p, kmap, vmap, head_dim, dtype, max_q_len, s);
+    }
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -65,5 +65,10 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& kmap, const 
                           int head_dim, int dtype, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            int head_dim, int dtype, int max_q_len, cudaStream_t s);
+// tcgen05 prefill: groups of 1, 2, 4 or 8 q heads per kv head; q_per_tile = 128 / group.
+// `plan` is device scratch of num_seqs + 1 int32 (the tile work list).
+cudaError_t launch_prefill_tc(const PrefillParams& p, int32_t* plan, const CUtensorMap& kmap,
+                              const CUtensorMap& vmap, const CUtensorMap& qmap, int head_dim, int dtype,
+                              int max_q_len, int num_tokens, cudaStream_t s);
 
 }  // namespace pa

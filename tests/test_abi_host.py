@@ -60,7 +60,9 @@ def test_workspace_sizes(lib):
     assert pa.decode_workspace_bytes(64, 32, 128, 4096, 512) == 2 * _align(n * 4) + _align(n * 128 * 4)
     n = 8 * 64 * 256
     assert pa.decode_workspace_bytes(8, 64, 128, 131072, 0) == 2 * _align(n * 4) + _align(n * 128 * 4)
-    assert pa.prefill_workspace_bytes(8, 64, 128, 131072) == pa.decode_workspace_bytes(8, 64, 128, 131072, 0)
+    assert pa.prefill_workspace_bytes(8, 64, 128, 131072) == _align(9 * 4) + pa.decode_workspace_bytes(8, 64, 128, 131072, 0)
+    assert pa.prefill_workspace_bytes(2052, 32, 128, 300) == _align(2053 * 4)
+    assert pa.prefill_workspace_bytes(0, 32, 128, 300) == 0
 
 
 FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced on rejected calls

@@ -56,3 +56,26 @@ def test_pure_prefill_without_prefix_matches_decode_of_last_row():
     dec = pa.paged_attention_decode(w.q[last].contiguous(), w.k_cache, w.v_cache, bt, sl, w.scale, 200)
     torch.cuda.synchronize()
     assert float((out[last].float() - dec.float()).abs().max()) <= 2e-3
+
+
+def test_long_chunks_many_tiles_per_cta():
+    # more (tile, kv head) work items than resident CTAs, long key ranges:
+    # every persistent CTA runs several items back to back
+    w = W.build_workload(name="long_chunks", seq_lens=[1536 + 4000, 1536 + 3100, 1536 + 2500, 1536, 300],
+                         q_lens=[1536, 1536, 1536, 1536, 1], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                         dtype="bf16", seed=31, device=DEV, poison=True)
+    seqs = np.arange(w.batch)
+    snap = snapshot(w, seqs)
+    _, out = gpu_step(w, prefill=True)
+    assert pa.device_error() == 0
+    assert torch.isfinite(out.float()).all()
+
+    def pick(b, ql):
+        if ql == 1:
+            return [0]
+        return sorted(set([0, 31, 32, 127, 128, ql // 2, ql - 33, ql - 1] +
+                          np.random.default_rng(b).choice(ql, 8, replace=False).tolist()))
+
+    rows, ref = oracle_rows(w, seqs, snap, q_rows_per_seq=pick)
+    err = max_err(out[torch.from_numpy(rows).to(DEV)], ref)
+    assert err <= TOL["bf16"], err
