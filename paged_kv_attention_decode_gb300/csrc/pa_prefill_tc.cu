@@ -109,8 +109,10 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
 // Persistent: each CTA walks work items w = blockIdx.x, blockIdx.x + gridDim.x, ...
 // over (tile, kv head) pairs of the plan; within a sequence the tiles nearest
 // the end (the longest key ranges) come first.
+// Two CTAs share an SM: ten warps, so one SM sub-partition runs three of them
+// and its 16K registers allow at most 168 per thread.
 template <typename T, int D, int ST>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __maxnreg__(168)
     prefill_tc_kernel(const PrefillParams p, const int32_t* __restrict__ plan,
                       const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const __grid_constant__ CUtensorMap qmap) {
