@@ -108,10 +108,11 @@ int pa_paged_kv_write(const void* key, const void* value, void* k_cache, void* v
                       int num_kv_heads, int head_dim, int block_size, int dtype, void* stream);
 
 /*
- * Workspace for pa_paged_attention_decode: the split-context partials of
- * num_seqs sequences no longer than max_seq_len, cut into partitions of
- * partition_size tokens (0 = PA_DEFAULT_PARTITION).  Returns 0 when no
- * sequence needs more than one partition.
+ * Workspace for pa_paged_attention_decode: the kernel's work list (one entry
+ * per sequence partition) and the split-context partials of num_seqs
+ * sequences no longer than max_seq_len, cut into partitions of
+ * partition_size tokens (0 = PA_DEFAULT_PARTITION).  Nonzero whenever
+ * num_seqs > 0.
  */
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len,
                                  int partition_size);
@@ -130,7 +131,7 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, in
  *   partition_size tokens per partition, a positive multiple of block_size,
  *                 or 0 for PA_DEFAULT_PARTITION.
  *   workspace     device scratch of at least pa_decode_workspace_bytes(...)
- *                 bytes, 256-byte aligned; may be NULL when that is 0.
+ *                 bytes, 256-byte aligned.
  * A sequence with seq_len == 0 gets an all-zero output row.
  */
 int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, const void* v_cache,

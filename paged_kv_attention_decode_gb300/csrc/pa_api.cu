@@ -107,13 +107,25 @@ size_t partials_bytes(int num_seqs, int num_q_heads, int head_dim, int parts) {
     return 2 * align256(n * sizeof(float)) + align256(n * head_dim * sizeof(float));
 }
 
-void carve_partials(pa::DecodeParams& p, void* ws, int head_dim) {
-    const size_t n = static_cast<size_t>(p.num_seqs) * p.num_q_heads * p.max_parts;
+// Decode workspace: [unit count (256 B)][unit list: num_seqs * parts int32][partials when parts > 1]
+size_t decode_ws_bytes(int num_seqs, int num_q_heads, int head_dim, int parts) {
+    size_t b = 256 + align256(static_cast<size_t>(num_seqs) * parts * sizeof(int32_t));
+    if (parts > 1) b += partials_bytes(num_seqs, num_q_heads, head_dim, parts);
+    return b;
+}
+
+void carve_workspace(pa::DecodeParams& p, void* ws) {
     uint8_t* base = static_cast<uint8_t*>(ws);
-    p.ws_m = reinterpret_cast<float*>(base);
-    p.ws_l = reinterpret_cast<float*>(base + align256(n * sizeof(float)));
-    p.ws_acc = reinterpret_cast<float*>(base + 2 * align256(n * sizeof(float)));
-    (void)head_dim;
+    p.unit_count = reinterpret_cast<int32_t*>(base);
+    p.work_counter = reinterpret_cast<int32_t*>(base + 128);
+    p.units = reinterpret_cast<int32_t*>(base + 256);
+    base += 256 + align256(static_cast<size_t>(p.num_seqs) * p.max_parts * sizeof(int32_t));
+    if (p.max_parts > 1) {
+        const size_t n = static_cast<size_t>(p.num_seqs) * p.num_q_heads * p.max_parts;
+        p.ws_m = reinterpret_cast<float*>(base);
+        p.ws_l = reinterpret_cast<float*>(base + align256(n * sizeof(float)));
+        p.ws_acc = reinterpret_cast<float*>(base + 2 * align256(n * sizeof(float)));
+    }
 }
 
 float scale_log2(float scale) { return scale * 1.4426950408889634f; }
@@ -173,11 +185,9 @@ int pa_paged_kv_write(const void* key, const void* value, void* k_cache, void* v
 
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len,
                                  int partition_size) {
-    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len <= 0 || partition_size < 0) return 0;
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len < 0 || partition_size < 0) return 0;
     const int part = partition_size ? partition_size : PA_DEFAULT_PARTITION;
-    const int parts = parts_for(max_seq_len, part);
-    if (parts <= 1) return 0;
-    return partials_bytes(num_seqs, num_q_heads, head_dim, parts);
+    return decode_ws_bytes(num_seqs, num_q_heads, head_dim, parts_for(max_seq_len, part));
 }
 
 static int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -187,11 +197,10 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
                        size_t workspace_bytes, int dtype, cudaStream_t stream) {
     const int part = partition_size ? partition_size : PA_DEFAULT_PARTITION;
     const int parts = parts_for(max_seq_len, part);
-    const size_t need = parts > 1 ? partials_bytes(num_seqs, num_q_heads, head_dim, parts) : 0;
-    if (need) {
-        if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
-        if (!aligned256(workspace)) return PA_ERR_INVALID_ARG;
-    }
+    if (parts > 65535) return PA_ERR_INVALID_ARG;   // partition index is a 16-bit field of the work list
+    const size_t need = decode_ws_bytes(num_seqs, num_q_heads, head_dim, parts);
+    if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned256(workspace)) return PA_ERR_INVALID_ARG;
     unsigned int* err = error_word();
     if (!err) return PA_ERR_CUDA;
     CUtensorMap kmap, vmap;
@@ -211,11 +220,12 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
     p.num_blocks = num_blocks;
     p.num_q_heads = num_q_heads;
     p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
     p.group = num_q_heads / num_kv_heads;
     p.partition_tokens = part;
     p.max_parts = parts;
     p.scale_log2 = scale_log2(scale);
-    if (need) carve_partials(p, workspace, head_dim);
+    carve_workspace(p, workspace);
     cudaError_t e = pa::launch_decode(p, kmap, vmap, head_dim, dtype, stream);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -16,6 +16,7 @@ __global__ void __launch_bounds__(128) slot_mapping_kernel(int64_t* __restrict__
                                                            int max_blocks, const int32_t* __restrict__ seq_lens,
                                                            const int32_t* __restrict__ cu_q_lens, int num_seqs,
                                                            int num_blocks, unsigned int* err) {
+    pdl_trigger();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= num_seqs) return;
@@ -54,6 +55,7 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__
                                                        uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                                                        const int64_t* __restrict__ slots, int num_tokens,
                                                        int num_kv_heads, int64_t num_slots, unsigned int* err) {
+    pdl_trigger();  // a following kernel that only reads inputs may overlap this one
     constexpr int CPR = D / 8;  // 16-byte chunks per (token, head) row
     const int64_t row_chunks = static_cast<int64_t>(num_kv_heads) * CPR;
     const int64_t total = static_cast<int64_t>(num_tokens) * row_chunks;

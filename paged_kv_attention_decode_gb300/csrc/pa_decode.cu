@@ -10,18 +10,23 @@
 // workspace and a second kernel merges them by log-sum-exp.
 //
 // GB300 design:
-//  * grid (partition, kv head, sequence); a CTA handles the `group` query
-//    heads that share one kv head, so every K/V byte is read once.
+//  * a one-CTA plan kernel lists the (sequence, partition) units; the decode
+//    kernel is persistent and gives each work item (unit, kv head) to one
+//    warp, which handles the `group` query heads that share the kv head, so
+//    every K/V byte is read once and no CTA is launched without work.
 //  * each warp owns a private ring of STAGES shared-memory slots; its lane 0
 //    fetches whole (16-token block, kv head) tiles of K and V with 4-D TMA
 //    loads (one per 64-dim half, 128-byte swizzle), completing on a per-slot
-//    mbarrier.
+//    mbarrier, and keeps fetching ahead across the warp's items.
 //  * MHA (group 1): fp32 FMA dot products, a 16-way transpose-reduction
 //    across the warp (16 shuffles per block), register-resident (m, l, acc).
 //  * GQA (group 2..8): the query group x K-block product is a dense
 //    contraction: S^T[16 tokens x 8 heads] = K Q^T and O^T += V^T P^T with
 //    mma.sync m16n8k16 (fp32 accumulate); M = 16 tokens matches the block.
-//  * warps of a CTA merge their states through shared memory at the end.
+//  * a warp writes its item's output row, or the partition's (m, l, acc)
+//    for the log-sum-exp reduction kernel.
+#include <algorithm>
+
 #include "pa_device.cuh"
 
 namespace pa {
@@ -256,221 +261,373 @@ struct MmaState {
 };
 
 // ---------------------------------------------------------------------------
+// work list: one unit per (sequence, partition) of every decode row
+// ---------------------------------------------------------------------------
+// units[k] = (b << 16) | partition; *unit_count = total.
+// A sequence of length 0 (or one rejected by the bounds checks) gets no unit:
+// its zero output row is written here.  Rows with q_len != 1 in a mixed batch
+// belong to the prefill kernel and get none.  Also resets the work counter.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* carry, int& chunk_total) {
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int t = warp_tot[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(kFull, t, off);
+            if (lane >= off) t += y;
+        }
+        warp_tot[lane] = t;
+    }
+    __syncthreads();
+    const int excl = *carry + (warp > 0 ? warp_tot[warp - 1] : 0) + incl - v;
+    chunk_total = warp_tot[31];
+    __syncthreads();
+    if (tid == 0) *carry += chunk_total;
+    __syncthreads();
+    return excl;
+}
+
+// Units are listed longest first: every sequence's full partitions, then the
+// shorter last partitions, so the items claimed at the end of a launch are
+// the small ones.
+__global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p) {
+    __shared__ int warp_tot[32];
+    __shared__ int carry;
+    const int tid = threadIdx.x;
+    // the decode kernel may launch now; it waits for this grid to complete
+    // before it reads the list
+    pdl_trigger();
+    const int P = p.partition_tokens;
+    auto seq_len_of = [&](int b, bool record) -> int {
+        if (p.cu_q_lens && p.cu_q_lens[b + 1] - p.cu_q_lens[b] != 1) return -1;  // not a decode row
+        int n = p.seq_lens[b];
+        if (n < 0 || n > p.max_seq_len || n > p.max_blocks * 16) {
+            if (record) record_error(p.err, PA_DEVERR_SEQ_LEN_);
+            n = 0;
+        }
+        return n;
+    };
+    int chunk_total = 0;
+    // pass 1: full partitions (and the zero rows of empty sequences)
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < p.num_seqs; base += 1024) {
+        const int b = base + tid;
+        int v = 0;
+        if (b < p.num_seqs) {
+            const int n = seq_len_of(b, true);
+            if (n > 0) {
+                v = n / P;
+            } else if (n == 0) {
+                // an empty (or rejected) sequence gets the zero row here
+                const int qrow = p.cu_q_lens ? p.cu_q_lens[b] : b;
+                uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                                    static_cast<int64_t>(qrow) * p.num_q_heads * p.head_dim);
+                for (int i = 0; i < p.num_q_heads * p.head_dim / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        const int start = block_exclusive_scan(v, warp_tot, &carry, chunk_total);
+        for (int i = 0; i < v; ++i)
+            p.units[start + i] = static_cast<int32_t>((static_cast<uint32_t>(b) << 16) | static_cast<uint32_t>(i));
+    }
+    // pass 2: the partial last partitions
+    for (int base = 0; base < p.num_seqs; base += 1024) {
+        const int b = base + tid;
+        int v = 0, last = 0;
+        if (b < p.num_seqs) {
+            const int n = seq_len_of(b, false);
+            if (n > 0 && n % P) {
+                v = 1;
+                last = n / P;
+            }
+        }
+        const int start = block_exclusive_scan(v, warp_tot, &carry, chunk_total);
+        if (v) p.units[start] = static_cast<int32_t>((static_cast<uint32_t>(b) << 16) | static_cast<uint32_t>(last));
+    }
+    if (tid == 0) {
+        *p.unit_count = carry;
+        *p.work_counter = 0;
+    }
+    // Only the lengths and tables (inputs) were read above, so this grid may
+    // have overlapped the previous kernel of the stream (the KV write).  It
+    // completes only after that kernel, so the decode kernel's wait on this
+    // grid also covers the write.
+    pdl_wait();
+}
+
+// ---------------------------------------------------------------------------
 // the decode kernel
 // ---------------------------------------------------------------------------
+// Persistent, warp-granular: work item w = (unit w / Hkv, kv head w % Hkv) is
+// one partition of one sequence for one kv head, handled start to finish by a
+// single warp.  Warps claim items from a global counter as they go (dynamic
+// balance).  Each warp streams the 16-token blocks of its items, in order,
+// through its own ring of shared-memory slots: lane 0 keeps the TMA fetches
+// STAGES blocks ahead of the block being computed, claiming the next item as
+// soon as the fetches reach the end of the current one, so the warp's HBM
+// pipeline never drains between items.  Warps never wait for one another.
 template <typename T, int D, bool kMma>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap) {
     using Shape = DecodeShape<D>;
+    constexpr int kQueue = 8;  // claimed items not yet computed (<= STAGES + 1 in use)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bars[kDecodeWarps * kDecodeStages];
-    __shared__ int any_timeout;
+    __shared__ int claimed[kDecodeWarps][kQueue];
 
-    const int part = blockIdx.x;
-    const int g = blockIdx.y;
-    const int b = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = p.group;
-
-    int qrow = b;
-    if (p.cu_q_lens) {
-        const int r0 = p.cu_q_lens[b];
-        if (p.cu_q_lens[b + 1] - r0 != 1) return;  // not a decode row
-        qrow = r0;
-    }
-    int n = p.seq_lens[b];
-    if (n < 0 || n > p.max_seq_len || n > p.max_blocks * 16) {
-        if (part == 0 && g == 0 && threadIdx.x == 0) record_error(p.err, PA_DEVERR_SEQ_LEN_);
-        n = 0;  // defined result: a zero row
-    }
+    const int H = p.num_kv_heads;
     const int P = p.partition_tokens;
-    const int nparts = n > 0 ? (n + P - 1) / P : 1;
-    if (part >= nparts) return;
-    const int tok0 = part * P;
-    const int tok1 = min(n, tok0 + P);
-    const int blk0 = tok0 >> 4;
-    const int nblk = n > 0 ? ((tok1 + 15) >> 4) - blk0 : 0;
-    const int32_t* bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks + blk0;
 
-    // 1024-byte aligned slot area (the 128-byte swizzle pattern repeats every 1 KiB)
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kDecodeWarps * kDecodeStages; ++i) mbar_init(&bars[i], 1);
-        any_timeout = 0;
+    WarpRing ring{smem + warp * Shape::kWarpBytes, bars + warp * kDecodeStages};
+    if (lane == 0) {
+        for (int s = 0; s < kDecodeStages; ++s) mbar_init(&ring.bars[s], 1);
         fence_barrier_init();
     }
-    __syncthreads();
+    __syncwarp();
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+    pdl_wait();  // the work list (and, through it, the KV write) is complete
+    const int total = *p.unit_count * H;
+    if (total == 0) return;
+    int* queue = claimed[warp];
 
-    WarpRing ring{smem + warp * Shape::kWarpBytes, bars + warp * kDecodeStages};
-    const int64_t q_base = (static_cast<int64_t>(qrow) * p.num_q_heads + g * G) * D;
-    const T* q = static_cast<const T*>(p.q) + q_base;
+    struct Item {
+        int b, g, part, n, tok1, blk0, nblk;
+        const int32_t* bt;
+    };
+    auto load_item = [&](int w, Item& it) {
+        const uint32_t unit = static_cast<uint32_t>(p.units[w / H]);
+        it.g = w % H;
+        it.b = static_cast<int>(unit >> 16);
+        it.part = static_cast<int>(unit & 0xffffu);
+        int n = p.seq_lens[it.b];
+        if (n < 0 || n > p.max_seq_len || n > p.max_blocks * 16) n = 0;
+        it.n = n;
+        const int tok0 = it.part * P;
+        it.tok1 = min(n, tok0 + P);
+        it.blk0 = tok0 >> 4;
+        it.nblk = n > 0 ? ((it.tok1 + 15) >> 4) - it.blk0 : 0;
+        it.bt = p.block_tables + static_cast<int64_t>(it.b) * p.max_blocks + it.blk0;
+    };
 
-    // prologue: fill the ring
-    uint32_t inflight = 0;
+    // ---- fetch cursor: claims items, loads their blocks ahead ----------------
+    uint32_t q_tail = 0, q_head = 0;  // queue of claimed item ids (uniform across lanes)
+    Item fi;
+    int fblk = 0;
+    bool fvalid = false;
+    // this lane's query words of the most recently claimed item, loaded at
+    // claim time so that they have arrived when the item's compute starts
+    constexpr int kQWords = kMma ? 2 * (D / 16) : D / 64;
+    uint32_t qpre[kQWords];
+    int qpre_item = -1;
+    auto load_q = [&](const Item& it, uint32_t (&dst)[kQWords]) {
+        const int qrow = p.cu_q_lens ? p.cu_q_lens[it.b] : it.b;
+        const uint16_t* qq = static_cast<const uint16_t*>(p.q) +
+                             (static_cast<int64_t>(qrow) * p.num_q_heads + it.g * G) * D;
+        if constexpr (!kMma) {
 #pragma unroll
-    for (int s = 0; s < kDecodeStages; ++s) {
-        const int i = warp + s * kDecodeWarps;
-        if (i < nblk) {
-            const int phys = bt[i];
-            if (phys >= 0 && phys < p.num_blocks) {
-                inflight |= 1u << s;
-                if (lane == 0) issue_tile<D>(ring, s, phys, g, &kmap, &vmap);
-            } else if (lane == 0) {
-                record_error(p.err, PA_DEVERR_BLOCK_ID_);
+            for (int j = 0; j < kQWords; ++j)
+                dst[j] = *reinterpret_cast<const uint32_t*>(qq + lane * AluState<T, D>::DPL + 2 * j);
+        } else {
+            const int hh = lane >> 2;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int d = kk * 16 + 2 * (lane & 3);
+                dst[2 * kk] = hh < G ? *reinterpret_cast<const uint32_t*>(qq + hh * D + d) : 0u;
+                dst[2 * kk + 1] = hh < G ? *reinterpret_cast<const uint32_t*>(qq + hh * D + d + 8) : 0u;
             }
         }
-    }
-
-    AluState<T, D> alu;
-    MmaState<T, D> mma;
-    if constexpr (!kMma) {
-        const uint16_t* qq = reinterpret_cast<const uint16_t*>(q);
-#pragma unroll
-        for (int j = 0; j < AluState<T, D>::DPL; j += 2) {
-            const uint32_t raw = *reinterpret_cast<const uint32_t*>(qq + lane * AluState<T, D>::DPL + j);
-            const float2 f = Elem<T>::to_float2(raw);
-            alu.q[j] = f.x * p.scale_log2;
-            alu.q[j + 1] = f.y * p.scale_log2;
-            alu.acc[j] = 0.f;
-            alu.acc[j + 1] = 0.f;
+    };
+    auto claim_next = [&]() {
+        int w = 0;
+        if (lane == 0) w = atomicAdd(p.work_counter, 1);
+        w = __shfl_sync(kFull, w, 0);
+        if (w >= total) {
+            fvalid = false;
+            return;
         }
-        alu.m = -INFINITY;
-        alu.l = 0.f;
-    } else {
-        const int hh = lane >> 2;
-        const uint16_t* qq = reinterpret_cast<const uint16_t*>(q);
-#pragma unroll
-        for (int kk = 0; kk < MmaState<T, D>::KS; ++kk) {
-            const int d = kk * 16 + 2 * (lane & 3);
-            mma.qb[kk][0] = hh < G ? *reinterpret_cast<const uint32_t*>(qq + hh * D + d) : 0u;
-            mma.qb[kk][1] = hh < G ? *reinterpret_cast<const uint32_t*>(qq + hh * D + d + 8) : 0u;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) mma.o[kk][e] = 0.f;
+        if (lane == 0) queue[q_tail % kQueue] = w;
+        ++q_tail;
+        load_item(w, fi);
+        load_q(fi, qpre);
+        qpre_item = w;
+        fblk = 0;
+        fvalid = fi.nblk > 0;  // every listed unit has at least one block
+    };
+    uint32_t kf = 0;  // blocks issued so far
+    auto issue_next = [&]() {
+        if (!fvalid) return;
+        const int slot = static_cast<int>(kf % kDecodeStages);
+        const int phys = fi.bt[fblk];
+        if (lane == 0) {
+            if (phys >= 0 && phys < p.num_blocks) {
+                issue_tile<D>(ring, slot, phys, fi.g, &kmap, &vmap);
+            } else {
+                record_error(p.err, PA_DEVERR_BLOCK_ID_);
+                mbar_arrive(&ring.bars[slot]);  // complete the phase without data
+            }
         }
-        mma.m[0] = mma.m[1] = -INFINITY;
-        mma.l[0] = mma.l[1] = 0.f;
-    }
+        ++kf;
+        if (++fblk >= fi.nblk) claim_next();
+    };
+    claim_next();
+#pragma unroll
+    for (int s = 0; s < kDecodeStages; ++s) issue_next();
 
-    uint32_t phases = 0;
-    bool timed_out = false;
-    for (int it = 0;; ++it) {
-        const int i = warp + it * kDecodeWarps;
-        if (i >= nblk) break;
-        const int s = it % kDecodeStages;
-        if (inflight & (1u << s)) {
-            const bool got = mbar_wait(&ring.bars[s], (phases >> s) & 1u);
+    // ---- compute: the claimed items in order, their blocks in order ---------
+    uint32_t kc = 0;  // blocks consumed so far
+    bool failed = false;
+    while (q_head != q_tail) {
+        __syncwarp();
+        const int w = queue[q_head % kQueue];
+        ++q_head;
+        Item it;
+        load_item(w, it);
+        const int qrow = p.cu_q_lens ? p.cu_q_lens[it.b] : it.b;
+        const int nparts = it.n > 0 ? (it.n + P - 1) / P : 1;
+        uint32_t qw[kQWords];
+        if (qpre_item == w) {
+#pragma unroll
+            for (int j = 0; j < kQWords; ++j) qw[j] = qpre[j];
+        } else {
+            load_q(it, qw);  // the fetch cursor has moved past this item already
+        }
+
+        AluState<T, D> alu;
+        MmaState<T, D> mma;
+        if constexpr (!kMma) {
+#pragma unroll
+            for (int j = 0; j < kQWords; ++j) {
+                const float2 f = Elem<T>::to_float2(qw[j]);
+                alu.q[2 * j] = f.x * p.scale_log2;
+                alu.q[2 * j + 1] = f.y * p.scale_log2;
+                alu.acc[2 * j] = 0.f;
+                alu.acc[2 * j + 1] = 0.f;
+            }
+            alu.m = -INFINITY;
+            alu.l = 0.f;
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < MmaState<T, D>::KS; ++kk) {
+                mma.qb[kk][0] = qw[2 * kk];
+                mma.qb[kk][1] = qw[2 * kk + 1];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mma.o[kk][e] = 0.f;
+            }
+            mma.m[0] = mma.m[1] = -INFINITY;
+            mma.l[0] = mma.l[1] = 0.f;
+        }
+
+        for (int blk = 0; blk < it.nblk; ++blk, ++kc) {
+            const int slot = static_cast<int>(kc % kDecodeStages);
+            const bool got = mbar_wait(&ring.bars[slot], (kc / kDecodeStages) & 1u);
             if (__any_sync(kFull, !got)) {
-                timed_out = true;
+                failed = true;
                 break;
             }
-            phases ^= 1u << s;
-            inflight &= ~(1u << s);
-            uint8_t* kt = ring.base + s * Shape::kStageBytes;
-            uint8_t* vt = kt + Shape::kTileBytes;
-            const int nvalid = min(16, tok1 - (blk0 + i) * 16);
-            if constexpr (!kMma)
-                alu.step(kt, vt, nvalid, lane);
-            else
-                mma.step(kt, vt, nvalid, lane, p.scale_log2);
-        }
-        // refill this slot with the warp's block STAGES iterations ahead
-        const int i2 = i + kDecodeStages * kDecodeWarps;
-        if (i2 < nblk) {
-            const int phys = bt[i2];
+            const int phys = it.bt[blk];
+            if (phys >= 0 && phys < p.num_blocks) {
+                uint8_t* kt = ring.base + slot * Shape::kStageBytes;
+                uint8_t* vt = kt + Shape::kTileBytes;
+                const int nvalid = min(16, it.tok1 - (it.blk0 + blk) * 16);
+                if constexpr (!kMma)
+                    alu.step(kt, vt, nvalid, lane);
+                else
+                    mma.step(kt, vt, nvalid, lane, p.scale_log2);
+            }
+            // the slot is free again: refill it with the block STAGES ahead
             fence_proxy_async_smem();
             __syncwarp();
-            if (phys >= 0 && phys < p.num_blocks) {
-                inflight |= 1u << s;
-                if (lane == 0) issue_tile<D>(ring, s, phys, g, &kmap, &vmap);
-            } else if (lane == 0) {
-                record_error(p.err, PA_DEVERR_BLOCK_ID_);
-            }
+            issue_next();
         }
-    }
-    if (timed_out) {
-        if (lane == 0) {
-            record_error(p.err, PA_DEVERR_TIMEOUT_);
-            atomicOr(&any_timeout, 1);
-        }
-        // let copies still in flight land before the CTA's memory is reused
-        for (int s = 0; s < kDecodeStages; ++s)
-            if (inflight & (1u << s)) (void)mbar_wait(&ring.bars[s], (phases >> s) & 1u);
-    }
+        if (failed) break;
 
-    // ---- merge the warps' (m, l, acc) -------------------------------------
-    __syncthreads();
-    float* red_m = reinterpret_cast<float*>(smem);                   // [NW][8]
-    float* red_l = red_m + kDecodeWarps * 8;                         // [NW][8]
-    float* red_acc = red_l + kDecodeWarps * 8;                       // [NW][8][D]
-    if constexpr (!kMma) {
-        float lsum = alu.l;
+        // ---- finalise this item: the output row, or the partition's partials
+        if constexpr (!kMma) {
+            constexpr int DPL = AluState<T, D>::DPL;
+            float lsum = alu.l;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
-        if (lane == 0) {
-            red_m[warp * 8] = alu.m;
-            red_l[warp * 8] = lsum;
-        }
+            for (int off = 1; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
+            const int hq = it.g;
+            if (nparts == 1) {
+                const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                uint16_t* o = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(qrow) * p.num_q_heads + hq) * D +
+                              lane * DPL;
+                if constexpr (DPL == 4) {
+                    uint2 v;
+                    v.x = Elem<T>::pack(alu.acc[0] * inv, alu.acc[1] * inv);
+                    v.y = Elem<T>::pack(alu.acc[2] * inv, alu.acc[3] * inv);
+                    *reinterpret_cast<uint2*>(o) = v;
+                } else {
+                    *reinterpret_cast<uint32_t*>(o) = Elem<T>::pack(alu.acc[0] * inv, alu.acc[1] * inv);
+                }
+            } else {
+                const int64_t pi = (static_cast<int64_t>(it.b) * p.num_q_heads + hq) * p.max_parts + it.part;
+                if (lane == 0) {
+                    p.ws_m[pi] = alu.m;
+                    p.ws_l[pi] = lsum;
+                }
 #pragma unroll
-        for (int j = 0; j < AluState<T, D>::DPL; ++j) red_acc[(warp * 8) * D + lane * AluState<T, D>::DPL + j] = alu.acc[j];
-    } else {
-        float l0 = mma.l[0], l1 = mma.l[1];
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(kFull, l0, off);
-            l1 += __shfl_xor_sync(kFull, l1, off);
-        }
-        const int h0 = 2 * (lane & 3);
-        if (lane < 4) {
-            red_m[warp * 8 + h0] = mma.m[0];
-            red_m[warp * 8 + h0 + 1] = mma.m[1];
-            red_l[warp * 8 + h0] = l0;
-            red_l[warp * 8 + h0 + 1] = l1;
-        }
-        const int dr = lane >> 2;
-#pragma unroll
-        for (int mt = 0; mt < MmaState<T, D>::KS; ++mt) {
-            red_acc[(warp * 8 + h0) * D + mt * 16 + dr] = mma.o[mt][0];
-            red_acc[(warp * 8 + h0 + 1) * D + mt * 16 + dr] = mma.o[mt][1];
-            red_acc[(warp * 8 + h0) * D + mt * 16 + dr + 8] = mma.o[mt][2];
-            red_acc[(warp * 8 + h0 + 1) * D + mt * 16 + dr + 8] = mma.o[mt][3];
-        }
-    }
-    __syncthreads();
-    if (any_timeout) return;
-
-    const int heads = kMma ? G : 1;
-    for (int idx = threadIdx.x; idx < heads * D; idx += kDecodeWarps * 32) {
-        const int h = idx / D;
-        const int d = idx - h * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, red_m[w * 8 + h]);
-        float L = 0.f, A = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kDecodeWarps; ++w) {
-                const float sc = fast_exp2(red_m[w * 8 + h] - M);
-                L = fmaf(red_l[w * 8 + h], sc, L);
-                A = fmaf(red_acc[(w * 8 + h) * D + d], sc, A);
+                for (int j = 0; j < DPL; ++j) p.ws_acc[pi * D + lane * DPL + j] = alu.acc[j];
             }
-        }
-        const int hq = g * G + h;
-        if (nparts == 1) {
-            const float v = L > 0.f ? A / L : 0.f;
-            reinterpret_cast<uint16_t*>(p.out)[(static_cast<int64_t>(qrow) * p.num_q_heads + hq) * D + d] =
-                Elem<T>::from_float(v);
         } else {
-            const int64_t pi = (static_cast<int64_t>(b) * p.num_q_heads + hq) * p.max_parts + part;
-            if (d == 0) {
-                p.ws_m[pi] = M;
-                p.ws_l[pi] = L;
+            float l0 = mma.l[0], l1 = mma.l[1];
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                l0 += __shfl_xor_sync(kFull, l0, off);
+                l1 += __shfl_xor_sync(kFull, l1, off);
             }
-            p.ws_acc[pi * D + d] = A;
+            const int dr = lane >> 2;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int h = 2 * (lane & 3) + e;
+                if (h >= G) continue;
+                const int hq = it.g * G + h;
+                const float lh = e ? l1 : l0;
+                if (nparts == 1) {
+                    const float inv = lh > 0.f ? 1.f / lh : 0.f;
+                    uint16_t* o = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(qrow) * p.num_q_heads + hq) * D;
+#pragma unroll
+                    for (int mt = 0; mt < MmaState<T, D>::KS; ++mt) {
+                        o[mt * 16 + dr] = Elem<T>::from_float(mma.o[mt][e] * inv);
+                        o[mt * 16 + dr + 8] = Elem<T>::from_float(mma.o[mt][2 + e] * inv);
+                    }
+                } else {
+                    const int64_t pi = (static_cast<int64_t>(it.b) * p.num_q_heads + hq) * p.max_parts + it.part;
+                    if (dr == 0) {
+                        p.ws_m[pi] = mma.m[e];
+                        p.ws_l[pi] = lh;
+                    }
+                    float* a = p.ws_acc + pi * D;
+#pragma unroll
+                    for (int mt = 0; mt < MmaState<T, D>::KS; ++mt) {
+                        a[mt * 16 + dr] = mma.o[mt][e];
+                        a[mt * 16 + dr + 8] = mma.o[mt][2 + e];
+                    }
+                }
+            }
         }
+    }
+    if (failed) {
+        if (lane == 0) record_error(p.err, PA_DEVERR_TIMEOUT_);
+        // let copies still in flight land before the CTA's memory is reused
+        for (uint32_t k = kc; k < kf; ++k) (void)mbar_wait(&ring.bars[k % kDecodeStages], (k / kDecodeStages) & 1u);
     }
 }
 
@@ -549,6 +706,18 @@ __global__ void __launch_bounds__(D) decode_reduce_kernel(const DecodeParams p) 
         Elem<T>::from_float(v);
 }
 
+int sm_count() {
+    static int count[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!count[dev]) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 148;
+        count[dev] = c;
+    }
+    return count[dev];
+}
+
 template <typename T, int D, bool kMma>
 cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t s) {
@@ -556,9 +725,13 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, cons
     auto kern = decode_kernel<T, D, kMma>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.max_parts, p.num_kv_heads, p.num_seqs);
-    kern<<<grid, kDecodeWarps * 32, smem, s>>>(p, kmap, vmap);
-    e = cudaGetLastError();
+    e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, s, p);
+    if (e != cudaSuccess) return e;
+    // persistent: two CTAs per SM, fewer when there cannot be that many items
+    const long long max_items = static_cast<long long>(p.num_seqs) * p.max_parts * p.num_kv_heads;
+    const long long want = (max_items + kDecodeWarps - 1) / kDecodeWarps;
+    const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(want, 2LL * sm_count())));
+    e = launch_pdl(kern, dim3(grid), dim3(kDecodeWarps * 32), smem, s, p, kmap, vmap);
     if (e != cudaSuccess) return e;
     if (p.max_parts > 1) {
         dim3 rgrid(p.num_q_heads, p.num_seqs);

@@ -259,6 +259,15 @@ __host__ __device__ constexpr uint32_t mma_idesc_f16(int M, int N, bool bf16, bo
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Block until the preceding kernel in the stream has completed and its
+// memory is visible (a no-op for kernels launched without the attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel in the stream (launched with the attribute) to start.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void record_error(unsigned int* err, unsigned int bits) {
     if (err) atomicOr(err, bits);
 }

@@ -14,6 +14,25 @@
 
 namespace pa {
 
+// Launch `kern` with programmatic stream serialization: it may start before
+// the preceding kernel of the stream has finished; it must call pdl_wait()
+// before touching anything that kernel produces.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 struct DecodeParams {
     void* out;                    // [rows, Hq, D]
     const void* q;                // [rows, Hq, D]
@@ -23,6 +42,9 @@ struct DecodeParams {
     float* ws_m;                  // [B, Hq, max_parts] running max (log2 units)
     float* ws_l;                  // [B, Hq, max_parts] running sum
     float* ws_acc;                // [B, Hq, max_parts, D] unnormalised accumulator
+    int32_t* units;               // [B * max_parts] (sequence << 16 | partition) work list
+    int32_t* unit_count;          // number of entries in `units`
+    int32_t* work_counter;        // next work item to claim (reset by the plan kernel)
     unsigned int* err;            // device error word
     int num_seqs;
     int max_blocks;
@@ -30,6 +52,7 @@ struct DecodeParams {
     int num_blocks;
     int num_q_heads;
     int num_kv_heads;
+    int head_dim;
     int group;                    // num_q_heads / num_kv_heads
     int partition_tokens;         // multiple of 16
     int max_parts;                // ceil(max_seq_len / partition_tokens)

@@ -55,14 +55,18 @@ def _align(x):
 
 
 def test_workspace_sizes(lib):
-    assert pa.decode_workspace_bytes(64, 32, 128, 512, 512) == 0       # one partition: no scratch
+    # [unit count: 256 B][work list: B x partitions int32][partials when partitions > 1]
+    assert pa.decode_workspace_bytes(64, 32, 128, 512, 512) == 256 + _align(64 * 4)
     n = 64 * 32 * 8
-    assert pa.decode_workspace_bytes(64, 32, 128, 4096, 512) == 2 * _align(n * 4) + _align(n * 128 * 4)
+    assert pa.decode_workspace_bytes(64, 32, 128, 4096, 512) == (256 + _align(64 * 8 * 4) + 2 * _align(n * 4)
+                                                                 + _align(n * 128 * 4))
     n = 8 * 64 * 256
-    assert pa.decode_workspace_bytes(8, 64, 128, 131072, 0) == 2 * _align(n * 4) + _align(n * 128 * 4)
+    assert pa.decode_workspace_bytes(8, 64, 128, 131072, 0) == (256 + _align(8 * 256 * 4) + 2 * _align(n * 4)
+                                                                + _align(n * 128 * 4))
     assert pa.prefill_workspace_bytes(8, 64, 128, 131072) == _align(9 * 4) + pa.decode_workspace_bytes(8, 64, 128, 131072, 0)
-    assert pa.prefill_workspace_bytes(2052, 32, 128, 300) == _align(2053 * 4)
+    assert pa.prefill_workspace_bytes(2052, 32, 128, 300) == _align(2053 * 4) + 256 + _align(2052 * 4)
     assert pa.prefill_workspace_bytes(0, 32, 128, 300) == 0
+    assert pa.decode_workspace_bytes(0, 32, 128, 300, 0) == 0
 
 
 FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced on rejected calls
@@ -81,7 +85,8 @@ def _decode(lib, **kw):
     (dict(dt=7), 2), (dict(d=96), 2), (dict(bs=32), 2), (dict(hq=5, hkv=2), 1),
     (dict(hq=32, hkv=2), 2), (dict(part=17), 1), (dict(part=-16), 1), (dict(q=None), 1),
     (dict(out=FAKE + 2), 1), (dict(B=-1), 1), (dict(nb=0), 1), (dict(scale=float("nan")), 1),
-    (dict(maxlen=4096, part=512), 3), (dict(maxlen=4096, ws=FAKE, wsb=10), 3),
+    (dict(maxlen=4096, part=512), 3), (dict(maxlen=4096, ws=FAKE, wsb=10), 3), (dict(maxlen=16), 3),
+    (dict(maxlen=1 << 24, part=16), 1),
     (dict(B=0), 0),
 ])
 def test_decode_rejects_bad_arguments_on_host(lib, kw, status):
