@@ -1,0 +1,74 @@
+"""A decode step captured once in a CUDA graph and replayed, as a serving
+engine does ("vLLM-Ascend 原理", section 4 "图模式": capture a decode step,
+then replay it with new contents written into fixed-address inputs; block
+tables are inputs whose contents change every step).  The library's calls
+only enqueue work on the caller's stream, so the whole step (slot mapping,
+KV write, work-list, decode, reduce) is capturable; max_seq_len is the
+capture-time bound and the batch size is fixed (a bucket)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_decode_gb300 as pa
+from paged_kv_attention_decode_gb300 import workloads as W
+from tests._gpu_util import TOL, bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _step_inputs(seed, lens, nb, Hq=8, Hkv=2, D=128):
+    return W.build_workload(name=f"g{seed}", seq_lens=lens, q_lens=1, num_q_heads=Hq, num_kv_heads=Hkv,
+                            head_dim=D, dtype="bf16", seed=seed, num_blocks=nb, device=DEV)
+
+
+def test_captured_decode_step_replays_with_new_inputs():
+    max_len, nb = 2048, 2000
+    w0 = _step_inputs(1, [100, 2048, 700, 33], nb)
+    # fixed-address buffers
+    q, key, value = w0.q.clone(), w0.key.clone(), w0.value.clone()
+    kc, vc = w0.k_cache.clone(), w0.v_cache.clone()
+    bt = torch.zeros(4, max_len // 16, dtype=torch.int32, device=DEV)
+    sl = torch.zeros(4, dtype=torch.int32, device=DEV)
+    slots = torch.empty(4, dtype=torch.int64, device=DEV)
+    out = torch.empty_like(q)
+    ws = torch.empty(pa.decode_workspace_bytes(4, 8, 128, max_len, 0), dtype=torch.uint8, device=DEV)
+
+    def load(w):
+        q.copy_(w.q); key.copy_(w.key); value.copy_(w.value)
+        bt.zero_(); bt[:, : w.block_tables.shape[1]].copy_(torch.from_numpy(w.block_tables))
+        sl.copy_(torch.from_numpy(w.seq_lens))
+
+    def step():
+        pa.slot_mapping(bt, sl, None, 4, nb, out=slots)
+        pa.paged_kv_write(key, value, kc, vc, slots)
+        pa.paged_attention_decode(q, kc, vc, bt, sl, w0.scale, max_len, out=out, workspace=ws)
+
+    load(w0)
+    step()                      # first call on the device does its one-time set-up
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+
+    for seed, lens in ((2, [1, 1500, 2047, 16]), (3, [512, 513, 2, 900])):
+        w = _step_inputs(seed, lens, nb)
+        kc.copy_(w.k_cache); vc.copy_(w.v_cache)
+        load(w)
+        graph.replay()
+        torch.cuda.synchronize()
+        replayed = out.clone()
+        # eager on the same inputs (the cache already holds this step's tokens)
+        kc.copy_(w.k_cache); vc.copy_(w.v_cache)
+        step()
+        torch.cuda.synchronize()
+        assert torch.equal(replayed.view(torch.int16), out.view(torch.int16))
+        # and the oracle
+        okc, ovc = bits(w.k_cache), bits(w.v_cache)
+        oracle.kv_write(bits(w.key), bits(w.value), okc, ovc,
+                        oracle.slot_mapping(w.block_tables, w.seq_lens, w.q_lens, 16, nb))
+        ref = oracle.paged_attention_decode(bits(w.q), okc, ovc, w.block_tables, w.seq_lens, w.scale, "bf16")
+        err = float(np.max(np.abs(replayed.double().cpu().numpy() - ref)))
+        assert err <= TOL["bf16"], err
+    assert pa.device_error() == 0
