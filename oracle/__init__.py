@@ -43,9 +43,17 @@ def _load():
             _p, _p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32,
             ctypes.c_double, _i32, _p, _i64, _i32]
         lib.oracle_num_threads.argtypes = [_i32]
+        lib.oracle_decode_e4m3.argtypes = [_p, _p, _i64]
+        lib.oracle_encode_e4m3.argtypes = [_p, _p, _i64]
+        lib.oracle_kv_write_fp8.argtypes = [_p, _p, _p, _p, _p, _i64, _i32, _i32, _i32, _i32, _i32,
+                                            ctypes.c_float, ctypes.c_float]
+        lib.oracle_paged_attention_decode_fp8.argtypes = [
+            _p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32,
+            ctypes.c_double, _i32, ctypes.c_double, ctypes.c_double, _p, _i64, _i32]
         for f in ("oracle_decode_values", "oracle_slot_mapping", "oracle_kv_write",
                   "oracle_paged_attention_decode", "oracle_paged_attention_prefill",
-                  "oracle_num_threads"):
+                  "oracle_num_threads", "oracle_decode_e4m3", "oracle_encode_e4m3",
+                  "oracle_kv_write_fp8", "oracle_paged_attention_decode_fp8"):
             getattr(lib, f).restype = _i32
         _lib = lib
     return _lib
@@ -140,5 +148,63 @@ def paged_attention_prefill(q_bits, k_cache_bits, v_cache_bits, block_tables, se
     _check(_load().oracle_paged_attention_prefill(
         _ptr(out), _ptr(q_bits), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(sl), _ptr(ql),
         sl.size, NB, Hq, Hkv, D, bs, float(scale), _DT[dtype], _ptr(sel),
+        0 if sel is None else sel.size, threads))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) KV cache
+# ---------------------------------------------------------------------------
+
+def decode_e4m3(codes) -> np.ndarray:
+    """E4M3 (FN) codes -> fp64 values."""
+    codes = _c(codes, np.uint8)
+    out = np.empty(codes.shape, dtype=np.float64)
+    _check(_load().oracle_decode_e4m3(_ptr(codes), _ptr(out), codes.size))
+    return out
+
+
+def encode_e4m3(values) -> np.ndarray:
+    """fp32 values -> nearest E4M3 codes (ties to even, saturating at +-448)."""
+    values = _c(values, np.float32)
+    out = np.empty(values.shape, dtype=np.uint8)
+    _check(_load().oracle_encode_e4m3(_ptr(values), _ptr(out), values.size))
+    return out
+
+
+def kv_write_fp8(key_bits, value_bits, k_cache_codes, v_cache_codes, slots, src_dtype: str,
+                 k_scale: float, v_scale: float) -> None:
+    """In place: cache[slot] = e4m3(float(x) * float32(1 / scale)) for every slot >= 0."""
+    key_bits = _c(key_bits, np.uint16)
+    value_bits = _c(value_bits, np.uint16)
+    slots = _c(slots, np.int64)
+    assert k_cache_codes.dtype == np.uint8 and k_cache_codes.flags.c_contiguous
+    assert v_cache_codes.dtype == np.uint8 and v_cache_codes.flags.c_contiguous
+    NB, bs, H, D = k_cache_codes.shape
+    k_inv = float(np.float32(1.0) / np.float32(k_scale))
+    v_inv = float(np.float32(1.0) / np.float32(v_scale))
+    _check(_load().oracle_kv_write_fp8(_ptr(key_bits), _ptr(value_bits), _ptr(k_cache_codes),
+                                       _ptr(v_cache_codes), _ptr(slots), slots.size, NB, H, D, bs,
+                                       _DT[src_dtype], k_inv, v_inv))
+
+
+def paged_attention_decode_fp8(q_bits, k_cache_codes, v_cache_codes, block_tables, seq_lens, scale: float,
+                               q_dtype: str, k_scale: float, v_scale: float, select=None,
+                               threads: int = 0) -> np.ndarray:
+    """fp64 decode attention over an E4M3 cache (values = code * scale)."""
+    q_bits = _c(q_bits, np.uint16)
+    B, Hq, D = q_bits.shape
+    NB, bs, Hkv, D2 = k_cache_codes.shape
+    assert D2 == D
+    kc = _c(k_cache_codes, np.uint8)
+    vc = _c(v_cache_codes, np.uint8)
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    sel = None if select is None else _c(select, np.int64)
+    n = B if sel is None else sel.size
+    out = np.empty((n, Hq, D), dtype=np.float64)
+    _check(_load().oracle_paged_attention_decode_fp8(
+        _ptr(out), _ptr(q_bits), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(sl), B, NB, Hq, Hkv, D, bs,
+        float(scale), _DT[q_dtype], float(k_scale), float(v_scale), _ptr(sel),
         0 if sel is None else sel.size, threads))
     return out

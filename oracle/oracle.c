@@ -78,6 +78,45 @@ static double decode_bf16(uint16_t h) {
     return sign ? -v : v;
 }
 
+/* OCP 8-bit floating point E4M3, "FN" variant: 1 sign bit, 4 exponent bits
+ * (bias 7), 3 fraction bits.  Exponent 0: subnormal f * 2^-9.  The patterns
+ * S.1111.111 are NaN; there is no infinity; the largest finite value is 448. */
+static double decode_e4m3(uint8_t c) {
+    int sign = c >> 7;
+    int e = (c >> 3) & 0xf;
+    int f = c & 0x7;
+    double v;
+    if (e == 15 && f == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -9);
+    else
+        v = ldexp((double)(8 | f), e - 10);   /* (8+f) * 2^(e-7-3) */
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 code to x: round to nearest, ties to the even code (even
+ * fraction), saturating to +-448 beyond the finite range; NaN -> NaN.  Found by
+ * comparing x with every non-negative finite code (plain and slow). */
+static uint8_t encode_e4m3(float xf) {
+    double x = (double)xf;
+    if (x != x) return 0x7f;
+    int neg = signbit(x) ? 1 : 0;
+    double a = fabs(x);
+    if (a >= 448.0) return (uint8_t)((neg << 7) | 0x7e);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c < 0x7f; ++c) {           /* 0x7f is NaN */
+        double d = fabs(decode_e4m3((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best_d = d;
+            best = c;
+        }
+    }
+    return (uint8_t)((neg << 7) | best);
+}
+
+static double g_tab_e4m3[256];
 static double g_tab_f16[65536];
 static double g_tab_bf16[65536];
 static pthread_once_t g_once = PTHREAD_ONCE_INIT;
@@ -87,6 +126,12 @@ static void build_tables(void) {
         g_tab_f16[i] = decode_f16((uint16_t)i);
         g_tab_bf16[i] = decode_bf16((uint16_t)i);
     }
+    for (int i = 0; i < 256; ++i) g_tab_e4m3[i] = decode_e4m3((uint8_t)i);
+}
+
+static const double* table_e4m3(void) {
+    pthread_once(&g_once, build_tables);
+    return g_tab_e4m3;
 }
 
 static const double* table_for(int dtype) {
@@ -155,11 +200,57 @@ int oracle_kv_write(const uint16_t* key, const uint16_t* value, uint16_t* k_cach
     return OR_OK;
 }
 
+/* E4M3 codes -> fp64 values; fp32 values -> E4M3 codes (rules above). */
+int oracle_decode_e4m3(const uint8_t* in, double* out, int64_t n) {
+    const double* tab = table_e4m3();
+    for (int64_t i = 0; i < n; ++i) out[i] = tab[in[i]];
+    return OR_OK;
+}
+
+int oracle_encode_e4m3(const float* in, uint8_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = encode_e4m3(in[i]);
+    return OR_OK;
+}
+
+/* Quantising cache write ("vLLM-Ascend 原理", section 4 "量化": the k and v of
+ * a decode step are quantised as they are written into the cache).  Each new
+ * element is decoded from its fp16/bf16 pattern, multiplied in fp32 by the
+ * fp32 reciprocal scale, and stored as its E4M3 code:
+ *   cache[slot / bs][slot % bs][h][d] = e4m3(float(x) * inv_scale). */
+int oracle_kv_write_fp8(const uint16_t* key, const uint16_t* value, uint8_t* k_cache, uint8_t* v_cache,
+                        const int64_t* slots, int64_t T, int num_blocks, int num_kv_heads, int head_dim,
+                        int block_size, int src_dtype, float k_inv_scale, float v_inv_scale) {
+    if (src_dtype != OR_F16 && src_dtype != OR_BF16) return OR_ERR_ARG;
+    const double* tab = table_for(src_dtype);
+    int64_t num_slots = (int64_t)num_blocks * block_size;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t slot = slots[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) return OR_ERR_SLOT;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            for (int d = 0; d < head_dim; ++d) {
+                int64_t dst = (slot * num_kv_heads + h) * head_dim + d;
+                int64_t src = (t * num_kv_heads + h) * head_dim + d;
+                float kx = (float)tab[key[src]];     /* exact: fp16/bf16 values are floats */
+                float vx = (float)tab[value[src]];
+                volatile float kq = kx * k_inv_scale; /* one fp32 rounding, no contraction */
+                volatile float vq = vx * v_inv_scale;
+                k_cache[dst] = encode_e4m3(kq);
+                v_cache[dst] = encode_e4m3(vq);
+            }
+        }
+    }
+    return OR_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 
 typedef struct {
     /* problem */
     const uint16_t *q, *k_cache, *v_cache;
+    const uint8_t *k8, *v8;                     /* E4M3 cache (k_cache/v_cache unused) */
+    double k_scale, v_scale;                    /* dequantisation scales of the E4M3 cache */
+    const double* tab8;
     const int32_t *block_tables, *seq_lens;
     const int64_t *row_seq, *row_pos, *row_qrow; /* per computed row: seq, position, q row */
     int64_t n_rows;
@@ -191,9 +282,15 @@ static int attend_one(const job_t* J, int64_t r, int h, double* s, double* qd, d
         if (lb >= J->max_blocks) return OR_ERR_TABLE;
         int64_t phys = J->block_tables[b * J->max_blocks + lb];
         if (phys < 0 || phys >= J->num_blocks) return OR_ERR_TABLE;
-        const uint16_t* kp = J->k_cache + ((phys * bs + off) * J->Hkv + g) * D;
+        const int64_t koff = ((phys * bs + off) * J->Hkv + g) * D;
         double dot = 0.0;
-        for (int d = 0; d < D; ++d) dot += qd[d] * J->tab[kp[d]];
+        if (J->k8) {
+            const uint8_t* kp = J->k8 + koff;
+            for (int d = 0; d < D; ++d) dot += qd[d] * (J->tab8[kp[d]] * J->k_scale);
+        } else {
+            const uint16_t* kp = J->k_cache + koff;
+            for (int d = 0; d < D; ++d) dot += qd[d] * J->tab[kp[d]];
+        }
         s[t] = J->scale * dot;
         if (s[t] > M) M = s[t];
     }
@@ -202,10 +299,16 @@ static int attend_one(const job_t* J, int64_t r, int h, double* s, double* qd, d
     for (int64_t t = 0; t < n; ++t) {
         int64_t lb = t / bs, off = t % bs;
         int64_t phys = J->block_tables[b * J->max_blocks + lb];
-        const uint16_t* vp = J->v_cache + ((phys * bs + off) * J->Hkv + g) * D;
+        const int64_t voff = ((phys * bs + off) * J->Hkv + g) * D;
         double w = exp(s[t] - M);
         L += w;
-        for (int d = 0; d < D; ++d) acc[d] += w * J->tab[vp[d]];
+        if (J->v8) {
+            const uint8_t* vp = J->v8 + voff;
+            for (int d = 0; d < D; ++d) acc[d] += w * (J->tab8[vp[d]] * J->v_scale);
+        } else {
+            const uint16_t* vp = J->v_cache + voff;
+            for (int d = 0; d < D; ++d) acc[d] += w * J->tab[vp[d]];
+        }
     }
     for (int d = 0; d < D; ++d) o[d] = acc[d] / L;
     return OR_OK;
@@ -342,6 +445,43 @@ int oracle_paged_attention_prefill(double* out, const uint16_t* q, const uint16_
     J.tab = table_for(dtype); J.out = out; J.max_len = max_len;
     rc = run_rows(&J, num_threads);
     free(rs); free(seq_of);
+    return rc;
+}
+
+/* Decode attention over an E4M3 cache: k_t = e4m3(code) * k_scale and
+ * v_t = e4m3(code) * v_scale ("vLLM-Ascend 原理", section 4 "量化": blocks
+ * are dequantised after being read through the block table), then the same
+ * two-pass softmax as oracle_paged_attention_decode, in fp64. */
+int oracle_paged_attention_decode_fp8(double* out, const uint16_t* q, const uint8_t* k_cache,
+                                      const uint8_t* v_cache, const int32_t* block_tables, int max_blocks,
+                                      const int32_t* seq_lens, int B, int num_blocks, int Hq, int Hkv, int D,
+                                      int block_size, double scale, int q_dtype, double k_scale, double v_scale,
+                                      const int64_t* sel, int64_t n_sel, int num_threads) {
+    int rc = check_common(B, Hq, Hkv, D, block_size, q_dtype);
+    if (rc) return rc;
+    int64_t n = sel ? n_sel : B;
+    int64_t* rs = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1) * 3);
+    if (!rs) return OR_ERR_NOMEM;
+    int64_t *row_seq = rs, *row_pos = rs + n, *row_q = rs + 2 * n;
+    int max_len = 1;
+    for (int64_t r = 0; r < n; ++r) {
+        int64_t b = sel ? sel[r] : r;
+        if (b < 0 || b >= B) { free(rs); return OR_ERR_ARG; }
+        row_seq[r] = b;
+        row_pos[r] = (int64_t)seq_lens[b] - 1;
+        row_q[r] = b;
+        if (seq_lens[b] > max_len) max_len = seq_lens[b];
+    }
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k8 = k_cache; J.v8 = v_cache; J.k_scale = k_scale; J.v_scale = v_scale;
+    J.tab8 = table_e4m3(); J.block_tables = block_tables;
+    J.seq_lens = seq_lens; J.row_seq = row_seq; J.row_pos = row_pos; J.row_qrow = row_q;
+    J.n_rows = n; J.max_blocks = max_blocks; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
+    J.block_size = block_size; J.num_blocks = num_blocks; J.scale = scale;
+    J.tab = table_for(q_dtype); J.out = out; J.max_len = max_len;
+    rc = run_rows(&J, num_threads);
+    free(rs);
     return rc;
 }
 

@@ -1,0 +1,102 @@
+"""Pins for the oracle's FP8 (E4M3) KV-cache functions.
+
+The pages name the quantised cache ("vLLM-Ascend 原理", section 4 "量化": k and
+v quantised to FP8/INT8 as they are written, dequantised after the block-table
+read); they fix no format details, so the oracle follows the OCP E4M3 ("FN")
+format, round to nearest even with saturation at +-448, and one fp32 scale per
+cache.  Pinned against torch's float8_e4m3fn conversions (a library routine
+the oracle does not call), closed forms, and SDPA on the dequantised values.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from paged_kv_attention_decode_gb300 import workloads as W
+from tests._util import bits
+
+F8 = torch.float8_e4m3fn
+
+
+def test_decode_every_code_matches_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.decode_e4m3(codes)
+    ref = torch.from_numpy(codes).view(F8).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7e] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_encode_matches_torch_rounding_including_ties():
+    finite = np.arange(0, 0x7f, dtype=np.uint8)
+    vals = oracle.decode_e4m3(finite)
+    mids = (vals[:-1] + vals[1:]) / 2                     # exact ties
+    rng = np.random.default_rng(0)
+    x = np.concatenate([vals, mids, mids + 1e-7, mids - 1e-7, rng.normal(0, 40, 20000),
+                        rng.uniform(-448, 448, 20000), rng.normal(0, 0.01, 5000)]).astype(np.float32)
+    x = np.concatenate([x, -x])
+    x = x[np.abs(x) < 448]
+    got = oracle.encode_e4m3(x)
+    ref = torch.from_numpy(x).to(F8).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_encode_saturates_and_keeps_nan():
+    x = np.array([448.0, 449.0, 1e6, np.inf, -448.0, -5000.0, -np.inf, np.nan], dtype=np.float32)
+    got = oracle.encode_e4m3(x)
+    assert list(got[:4]) == [0x7e] * 4 and list(got[4:7]) == [0xfe] * 3 and got[7] == 0x7f
+
+
+@pytest.mark.parametrize("src", ["f16", "bf16"])
+def test_fp8_write_matches_torch_quantisation(src):
+    rng = np.random.default_rng(3)
+    NB, bs, H, D, T = 6, 16, 2, 128, 30
+    g = torch.Generator().manual_seed(4)
+    key = (torch.randn(T, H, D, generator=g) * 3).to(W.torch_dtype(src))
+    val = (torch.randn(T, H, D, generator=g) * 200).to(W.torch_dtype(src))
+    kc = rng.integers(0, 256, size=(NB, bs, H, D), dtype=np.uint8)
+    vc = kc.copy()
+    slots = rng.permutation(NB * bs)[:T].astype(np.int64)
+    slots[::5] = -1
+    k_scale, v_scale = 1 / 16, 0.37
+    kref, vref = kc.copy(), vc.copy()
+    keep = slots >= 0
+
+    def quant(x, scale):
+        inv = np.float32(1) / np.float32(scale)
+        y = (x.to(torch.float32) * torch.tensor(inv)).clamp(-448, 448)
+        return y.to(F8).view(torch.uint8).numpy()
+
+    kref.reshape(NB * bs, H, D)[slots[keep]] = quant(key, k_scale)[keep]
+    vref.reshape(NB * bs, H, D)[slots[keep]] = quant(val, v_scale)[keep]
+    oracle.kv_write_fp8(bits(key), bits(val), kc, vc, slots, src, k_scale, v_scale)
+    assert np.array_equal(kc, kref) and np.array_equal(vc, vref)
+
+
+def test_fp8_decode_equals_sdpa_on_dequantised_values():
+    Hq, Hkv, D = 8, 2, 128
+    lens = np.array([1, 17, 100, 300], dtype=np.int32)
+    w = W.build_workload(name="f8", seq_lens=lens, q_lens=1, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                         dtype="bf16", seed=9, pool_slack=0.5, materialize=False)
+    g = torch.Generator().manual_seed(10)
+    q = torch.randn(len(lens), Hq, D, generator=g).to(torch.bfloat16)
+    Kc = [(torch.randn(int(n), Hkv, D, generator=g) * 8).to(F8) for n in lens]
+    Vc = [(torch.randn(int(n), Hkv, D, generator=g) * 8).to(F8) for n in lens]
+    kpool = np.zeros((w.num_blocks, 16, Hkv, D), np.uint8)
+    vpool = np.zeros_like(kpool)
+    slots = oracle.slot_mapping(w.block_tables, lens, lens, 16, w.num_blocks)
+    kpool.reshape(-1, Hkv, D)[slots] = torch.cat(Kc).view(torch.uint8).numpy()
+    vpool.reshape(-1, Hkv, D)[slots] = torch.cat(Vc).view(torch.uint8).numpy()
+    k_scale, v_scale, scale = 1 / 8, 1 / 4, 1 / math.sqrt(D)
+    out = oracle.paged_attention_decode_fp8(bits(q), kpool, vpool, w.block_tables, lens, scale, "bf16",
+                                            k_scale, v_scale)
+    for b in range(len(lens)):
+        k = (Kc[b].to(torch.float64) * k_scale).transpose(0, 1).repeat_interleave(Hq // Hkv, 0)
+        v = (Vc[b].to(torch.float64) * v_scale).transpose(0, 1).repeat_interleave(Hq // Hkv, 0)
+        ref = F.scaled_dot_product_attention(q[b].to(torch.float64)[:, None][None], k[None], v[None],
+                                             scale=scale)[0, :, 0]
+        np.testing.assert_allclose(out[b], ref.numpy(), rtol=1e-11, atol=1e-12)
