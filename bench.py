@@ -68,7 +68,7 @@ def _algorithmic_bytes(w) -> dict:
     per sequence that reads it: `kv`), the query rows, the output rows, the
     live table entries and the lengths."""
     n = w.seq_lens.astype(np.int64)
-    row = w.num_kv_heads * w.head_dim * 2 * 2          # K and V bytes of one token
+    row = w.num_kv_heads * w.head_dim * 2 * w.cache_elem_bytes   # K and V bytes of one token
     kv = int(n.sum()) * row
     rows_per_block = {}
     for b in range(w.batch):
@@ -288,6 +288,8 @@ def run_ours(args):
     B = w.batch
     T = w.num_tokens
     decode = w.is_decode
+    fp8 = w.meta.get("cache_dtype") == "fp8"
+    kv_scale = w.meta.get("kv_scale", 1.0)
     bt = torch.from_numpy(w.block_tables).to(dev)
     sl = torch.from_numpy(w.seq_lens).to(dev)
     cu = None if decode else torch.from_numpy(w.cu_q_lens).to(dev)
@@ -303,13 +305,19 @@ def run_ours(args):
 
     def step():
         pa.slot_mapping(bt, sl, cu, T, w.num_blocks, out=slots)
-        pa.paged_kv_write(w.key, w.value, w.k_cache, w.v_cache, slots)
+        if fp8:
+            pa.paged_kv_write_fp8(w.key, w.value, w.k_cache, w.v_cache, slots, kv_scale, kv_scale)
+        else:
+            pa.paged_kv_write(w.key, w.value, w.k_cache, w.v_cache, slots)
 
     def attend(q=None, btab=None, lens=None, cul=None):
         q = w.q if q is None else q
         btab = bt if btab is None else btab
         lens = sl if lens is None else lens
-        if decode:
+        if fp8:
+            pa.paged_attention_decode_fp8(q, w.k_cache, w.v_cache, btab, lens, w.scale, kv_scale, kv_scale,
+                                          max_len, out=out, partition_size=args.partition, workspace=wsp)
+        elif decode:
             pa.paged_attention_decode(q, w.k_cache, w.v_cache, btab, lens, w.scale, max_len, out=out,
                                       partition_size=args.partition, workspace=wsp)
         else:
@@ -374,7 +382,10 @@ def run_ours(args):
         if cu_d is not None:
             cu_d.copy_(cu_h, non_blocking=True)
         pa.slot_mapping(bt_d, sl_d, cu_d, T, w.num_blocks, out=slots)
-        pa.paged_kv_write(k_d, v_d, w.k_cache, w.v_cache, slots)
+        if fp8:
+            pa.paged_kv_write_fp8(k_d, v_d, w.k_cache, w.v_cache, slots, kv_scale, kv_scale)
+        else:
+            pa.paged_kv_write(k_d, v_d, w.k_cache, w.v_cache, slots)
         attend(q_d, bt_d, sl_d, cu_d)
         out_h.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
@@ -403,7 +414,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16" if w.dtype == "f16" else "bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": ("e4m3 cache, " if fp8 else "") + ("f16" if w.dtype == "f16" else "bf16"),
         "data": "synthetic",
         "config": {"workload": args.workload, "batch": B, "new_tokens_per_step": T, "ctx": ctx,
                    "heads": f"{w.num_q_heads}/{w.num_kv_heads}", "head_dim": w.head_dim, "block_size": 16,
@@ -427,7 +439,7 @@ def run_ours(args):
         line["roofline"]["logical_gbs"] = ab["total_logical"] / (attn_ms / 1e3) / 1e9
     if not decode:
         line["prefill_gflop_per_step"] = _prefill_flops(w) / 1e9
-    if ws == 1 and decode and not args.no_cpu_baseline:
+    if ws == 1 and decode and not fp8 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, seconds=args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if dist:

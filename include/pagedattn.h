@@ -168,6 +168,35 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
                                void* stream);
 
 /*
+ * FP8 (E4M3) KV cache ("vLLM-Ascend 原理", section 4 "量化": k and v are
+ * quantised to 8 bits as they are written and dequantised after they are read
+ * through the block table; the cache takes half the HBM and half the bytes
+ * per decode step).  Codes are OCP E4M3 ("FN"), one byte per element, same
+ * [num_blocks, block_size, num_kv_heads, head_dim] layout; one fp32 scale per
+ * pool: value = code * scale.  head_dim must be 128.
+ *
+ * pa_paged_kv_write_fp8 stores code = e4m3(float(x) * (1.0f / scale)) for each
+ * new element x (fp16/bf16 `src_dtype`): one fp32 multiply, round to nearest
+ * even, saturating at +-448, NaN kept.  Other arguments as pa_paged_kv_write.
+ */
+int pa_paged_kv_write_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
+                          const int64_t* slot_mapping, int num_tokens, int num_blocks, int num_kv_heads,
+                          int head_dim, int block_size, int src_dtype, float k_scale, float v_scale,
+                          void* stream);
+
+/*
+ * Decode attention over an FP8 cache: as pa_paged_attention_decode with
+ * k_t = code * k_scale and v_t = code * v_scale; q and out keep `dtype`
+ * (fp16/bf16); the workspace is sized by pa_decode_workspace_bytes.
+ */
+int pa_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* seq_lens, int num_seqs, int max_seq_len, int num_blocks,
+                                  float scale, float k_scale, float v_scale, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int block_size, int partition_size,
+                                  void* workspace, size_t workspace_bytes, int dtype, void* stream);
+
+/*
  * Decode attention for callers that cannot allocate device memory.
  *
  * No counterpart in the pages: this is a deployment variant of

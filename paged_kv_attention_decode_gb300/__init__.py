@@ -11,8 +11,10 @@ from ._binding import (  # noqa: F401
     library_path,
     load_library,
     paged_attention_decode,
+    paged_attention_decode_fp8,
     paged_attention_prefill,
     paged_kv_write,
+    paged_kv_write_fp8,
     prefill_workspace_bytes,
     slot_mapping,
     device_error,

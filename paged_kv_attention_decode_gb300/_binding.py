@@ -41,6 +41,9 @@ _SIGNATURES = {
     "pa_get_device_error": (_i32, [ctypes.POINTER(_i32), _i32, _p]),
     "pa_paged_attention_decode_noalloc": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _f32,
                                                  _i32, _i32, _i32, _i32, _i32, _i32, _p]),
+    "pa_paged_kv_write_fp8": (_i32, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _p]),
+    "pa_paged_attention_decode_fp8": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _f32, _f32, _f32,
+                                             _i32, _i32, _i32, _i32, _i32, _p, _sz, _i32, _p]),
 }
 
 
@@ -215,3 +218,54 @@ def device_error(clear: bool = True, stream=None) -> int:
     _check(load_library().pa_get_device_error(ctypes.byref(code), int(clear), _stream(stream)),
            "pa_get_device_error")
     return code.value
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) cache
+# --------------------------------------------------------------------------
+
+def _u8(t: torch.Tensor) -> torch.Tensor:
+    _need(t.element_size() == 1, "FP8 caches hold one byte per element")
+    return t
+
+
+def paged_kv_write_fp8(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                       slot_mapping: torch.Tensor, k_scale: float, v_scale: float, stream=None) -> None:
+    """In place: E4M3 codes of key/value * (1 / scale) into the FP8 pools (slot < 0: skipped)."""
+    _cuda(key, value, k_cache, v_cache, slot_mapping)
+    _u8(k_cache), _u8(v_cache)
+    _need(slot_mapping.dtype == torch.int64, "slot_mapping must be int64")
+    NB, bs, H, D = k_cache.shape
+    T = key.shape[0]
+    _need(tuple(key.shape) == (T, H, D) and value.shape == key.shape and v_cache.shape == k_cache.shape,
+          "key/value/cache shapes")
+    rc = load_library().pa_paged_kv_write_fp8(key.data_ptr(), value.data_ptr(), k_cache.data_ptr(),
+                                              v_cache.data_ptr(), slot_mapping.data_ptr(), T, NB, H, D, bs,
+                                              _dt(key), float(k_scale), float(v_scale), _stream(stream))
+    _check(rc, "pa_paged_kv_write_fp8")
+
+
+def paged_attention_decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float, k_scale: float,
+                               v_scale: float, max_seq_len: int | None = None, out: torch.Tensor | None = None,
+                               partition_size: int = 0, workspace: torch.Tensor | None = None,
+                               stream=None) -> torch.Tensor:
+    """Decode attention over FP8 (E4M3) pools: q [B, Hq, 128] -> out [B, Hq, 128]."""
+    _cuda(q, k_cache, v_cache, block_tables, seq_lens, out, workspace)
+    _u8(k_cache), _u8(v_cache)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    _need(D2 == D and v_cache.shape == k_cache.shape, "cache shape")
+    if max_seq_len is None:
+        max_seq_len = int(seq_lens.max().item()) if B else 0
+    if out is None:
+        out = torch.empty_like(q)
+    nbytes = decode_workspace_bytes(B, Hq, D, max_seq_len, partition_size)
+    workspace = _workspace(nbytes, q.device, workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().pa_paged_attention_decode_fp8(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        block_tables.shape[1], seq_lens.data_ptr(), B, max_seq_len, NB, float(scale), float(k_scale),
+        float(v_scale), Hq, Hkv, D, bs, partition_size, _ptr(workspace), ws_bytes, _dt(q), _stream(stream))
+    _check(rc, "pa_paged_attention_decode_fp8")
+    return out

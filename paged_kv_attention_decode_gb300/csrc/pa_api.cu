@@ -80,6 +80,21 @@ bool make_q_map(CUtensorMap* map, const void* q, int num_tokens, int num_q_heads
     return r == CUDA_SUCCESS;
 }
 
+// Tensor map over an FP8 pool [num_blocks * 16 token rows, Hkv, 128 codes]:
+// one box = the 16 rows of one (block, head), 128 bytes each, 128-byte swizzled.
+bool make_kv_map_fp8(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(num_blocks) * 16};
+    const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(num_kv_heads) * 128};
+    const cuuint32_t box[3] = {128, 1, 16};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
@@ -194,7 +209,8 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
                        const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
                        const int32_t* cu_q_lens, int num_seqs, int max_seq_len, int num_blocks, float scale,
                        int num_q_heads, int num_kv_heads, int head_dim, int partition_size, void* workspace,
-                       size_t workspace_bytes, int dtype, cudaStream_t stream) {
+                       size_t workspace_bytes, int dtype, cudaStream_t stream, bool fp8 = false,
+                       float k_scale = 1.f, float v_scale = 1.f) {
     const int part = partition_size ? partition_size : PA_DEFAULT_PARTITION;
     const int parts = parts_for(max_seq_len, part);
     if (parts > 65535) return PA_ERR_INVALID_ARG;   // partition index is a 16-bit field of the work list
@@ -204,9 +220,11 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
     unsigned int* err = error_word();
     if (!err) return PA_ERR_CUDA;
     CUtensorMap kmap, vmap;
-    if (!make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) ||
-        !make_kv_map(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype))
-        return PA_ERR_CUDA;
+    const bool maps_ok = fp8 ? make_kv_map_fp8(&kmap, k_cache, num_blocks, num_kv_heads) &&
+                                   make_kv_map_fp8(&vmap, v_cache, num_blocks, num_kv_heads)
+                             : make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) &&
+                                   make_kv_map(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype);
+    if (!maps_ok) return PA_ERR_CUDA;
     pa::DecodeParams p{};
     p.out = out;
     p.q = q;
@@ -224,9 +242,11 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
     p.group = num_q_heads / num_kv_heads;
     p.partition_tokens = part;
     p.max_parts = parts;
-    p.scale_log2 = scale_log2(scale);
+    p.scale_log2 = scale_log2(scale) * k_scale;
+    p.v_scale = v_scale;
     carve_workspace(p, workspace);
-    cudaError_t e = pa::launch_decode(p, kmap, vmap, head_dim, dtype, stream);
+    cudaError_t e = fp8 ? pa::launch_decode_fp8(p, kmap, vmap, dtype, stream)
+                        : pa::launch_decode(p, kmap, vmap, head_dim, dtype, stream);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -250,6 +270,50 @@ int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, con
 
 // Prefill workspace: [tile work list: num_seqs + 1 int32, 256-aligned][decode-row partials].
 static size_t plan_bytes(int num_seqs) { return align256(static_cast<size_t>(num_seqs + 1) * sizeof(int32_t)); }
+
+int pa_paged_kv_write_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
+                          const int64_t* slot_mapping, int num_tokens, int num_blocks, int num_kv_heads,
+                          int head_dim, int block_size, int src_dtype, float k_scale, float v_scale, void* stream) {
+    if (src_dtype != PA_F16 && src_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (block_size != PA_BLOCK_SIZE || head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0 || num_blocks > kMaxPoolBlocks)
+        return PA_ERR_INVALID_ARG;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    unsigned int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    const float k_inv = 1.0f / k_scale;   // one fp32 division, as the quantiser's definition states
+    const float v_inv = 1.0f / v_scale;
+    cudaError_t e = pa::launch_kv_write_fp8(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks,
+                                            num_kv_heads, src_dtype, k_inv, v_inv, err,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                  int num_seqs, int max_seq_len, int num_blocks, float scale, float k_scale,
+                                  float v_scale, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int partition_size, void* workspace, size_t workspace_bytes, int dtype,
+                                  void* stream) {
+    int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size, dtype, num_blocks);
+    if (rc) return rc;
+    if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || num_seqs > kMaxGrid || max_seq_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (partition_size < 0 || partition_size % PA_BLOCK_SIZE) return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale)) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+    return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
+                       max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, partition_size,
+                       workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream), true, k_scale,
+                       v_scale);
+}
 
 size_t pa_prefill_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len) {
     if (num_seqs <= 0) return 0;

@@ -77,6 +77,79 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__
     }
 }
 
+// Quantising write into an FP8 (E4M3) cache ("vLLM-Ascend 原理", section 4
+// "量化": k and v are quantised as they are written).  Each thread turns 16
+// source values (fp16/bf16) into 16 codes: code = e4m3(float(x) * inv_scale),
+// one fp32 multiply, round to nearest even, saturating at +-448.
+template <typename T>
+__global__ void __launch_bounds__(256) kv_write_fp8_kernel(const uint4* __restrict__ key,
+                                                           const uint4* __restrict__ value,
+                                                           uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                                           const int64_t* __restrict__ slots, int num_tokens,
+                                                           int num_kv_heads, int64_t num_slots, float k_inv,
+                                                           float v_inv, unsigned int* err) {
+    pdl_trigger();
+    constexpr int D = 128;
+    constexpr int CPR = D / 16;  // 16-code chunks per (token, head) row
+    const int64_t row_chunks = static_cast<int64_t>(num_kv_heads) * CPR;
+    const int64_t total = static_cast<int64_t>(num_tokens) * row_chunks;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / row_chunks;
+        const int64_t within = i - t * row_chunks;
+        const int64_t slot = __ldg(slots + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (within == 0) record_error(err, PA_DEVERR_SLOT_);
+            continue;
+        }
+        uint4 out[2];
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint4* src = kv ? value : key;
+            const float inv = kv ? v_inv : k_inv;
+            const uint4 a = __ldg(src + 2 * i);
+            const uint4 b = __ldg(src + 2 * i + 1);
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            uint32_t codes[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 x0 = Elem<T>::to_float2(w[2 * j]);
+                const float2 x1 = Elem<T>::to_float2(w[2 * j + 1]);
+                const uint16_t lo = f32x2_to_e4m3x2(__fmul_rn(x0.x, inv), __fmul_rn(x0.y, inv));
+                const uint16_t hi = f32x2_to_e4m3x2(__fmul_rn(x1.x, inv), __fmul_rn(x1.y, inv));
+                codes[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+            }
+            out[kv] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        }
+        const int64_t dst = slot * row_chunks + within;
+        k_cache[dst] = out[0];
+        v_cache[dst] = out[1];
+    }
+}
+
+cudaError_t launch_kv_write_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
+                                const int64_t* slots, int num_tokens, int num_blocks, int num_kv_heads,
+                                int src_dtype, float k_inv_scale, float v_inv_scale, unsigned int* err,
+                                cudaStream_t s) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * 8;
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    if (blocks > 152LL * 16) blocks = 152LL * 16;
+    const int64_t num_slots = static_cast<int64_t>(num_blocks) * 16;
+    auto args = [&](auto kern) {
+        kern<<<static_cast<int>(blocks), threads, 0, s>>>(
+            static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
+            static_cast<uint4*>(v_cache), slots, num_tokens, num_kv_heads, num_slots, k_inv_scale, v_inv_scale, err);
+    };
+    if (src_dtype == 0)
+        args(kv_write_fp8_kernel<__half>);
+    else
+        args(kv_write_fp8_kernel<__nv_bfloat16>);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_tables, int max_blocks,
                                 const int32_t* seq_lens, const int32_t* cu_q_lens, int num_seqs,
                                 int num_tokens, int num_blocks, unsigned int* err, cudaStream_t s) {

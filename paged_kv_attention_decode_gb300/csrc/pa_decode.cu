@@ -26,6 +26,7 @@
 //  * a warp writes its item's output row, or the partition's (m, l, acc)
 //    for the log-sum-exp reduction kernel.
 #include <algorithm>
+#include <type_traits>
 
 #include "pa_device.cuh"
 
@@ -34,14 +35,19 @@ namespace pa {
 namespace {
 
 constexpr int kDecodeWarps = 4;
-constexpr int kDecodeStages = 3;
 constexpr unsigned kFull = 0xffffffffu;
 
-template <int D>
+// Per-warp shared memory: a ring of kStages (K tile, V tile) slots, plus, for
+// the FP8 GQA path, one K and one V tile converted to 16-bit for the MMA.
+// FP8 tiles are half the bytes, so the FP8 rings are deeper: the same bytes
+// stay in flight per warp.
+template <int D, bool kFp8, bool kMma>
 struct DecodeShape {
-    static constexpr int kTileBytes = 16 * D * 2;         // one (block, kv head) tile
-    static constexpr int kStageBytes = 2 * kTileBytes;    // K tile + V tile
-    static constexpr int kWarpBytes = kDecodeStages * kStageBytes;
+    static constexpr int kTileBytes = 16 * D * (kFp8 ? 1 : 2);  // one (block, kv head) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;          // K tile + V tile
+    static constexpr int kStages = kFp8 ? (kMma ? 4 : 6) : 3;
+    static constexpr int kConvBytes = (kFp8 && kMma) ? 2 * 16 * D * 2 : 0;
+    static constexpr int kWarpBytes = kStages * kStageBytes + kConvBytes;
     static constexpr int kSmemBytes = kDecodeWarps * kWarpBytes + 1024;  // + alignment slack
 };
 
@@ -51,16 +57,53 @@ struct WarpRing {
     uint64_t* bars;     // STAGES mbarriers
 };
 
-template <int D>
+template <int D, bool kFp8, bool kMma>
 __device__ __forceinline__ void issue_tile(const WarpRing& ring, int slot, int phys, int kv_head,
                                           const CUtensorMap* kmap, const CUtensorMap* vmap) {
-    uint8_t* dst = ring.base + slot * DecodeShape<D>::kStageBytes;
-    mbar_arrive_expect_tx(&ring.bars[slot], DecodeShape<D>::kStageBytes);
+    using Shape = DecodeShape<D, kFp8, kMma>;
+    uint8_t* dst = ring.base + slot * Shape::kStageBytes;
+    mbar_arrive_expect_tx(&ring.bars[slot], Shape::kStageBytes);
+    if constexpr (kFp8) {
+        tma_load_3d(dst, kmap, &ring.bars[slot], 0, kv_head, phys * 16);
+        tma_load_3d(dst + Shape::kTileBytes, vmap, &ring.bars[slot], 0, kv_head, phys * 16);
+    } else {
 #pragma unroll
-    for (int h = 0; h < D / 64; ++h) {
-        tma_load_4d(dst + h * TileGeom<D>::kHalfBytes, kmap, &ring.bars[slot], 0, h, kv_head, phys * 16);
-        tma_load_4d(dst + DecodeShape<D>::kTileBytes + h * TileGeom<D>::kHalfBytes, vmap, &ring.bars[slot], 0, h,
-                    kv_head, phys * 16);
+        for (int h = 0; h < D / 64; ++h) {
+            tma_load_4d(dst + h * TileGeom<D>::kHalfBytes, kmap, &ring.bars[slot], 0, h, kv_head, phys * 16);
+            tma_load_4d(dst + Shape::kTileBytes + h * TileGeom<D>::kHalfBytes, vmap, &ring.bars[slot], 0, h,
+                        kv_head, phys * 16);
+        }
+    }
+}
+
+// FP8 tile (16 rows x 128 codes) -> 16-bit tile in the swizzled layout the
+// MMA step reads (exact: every E4M3 value is an fp16 and a bf16 value).
+template <typename T>
+__device__ __forceinline__ void convert_fp8_tile(const uint8_t* src, uint8_t* dst, int lane) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int ci = lane + 32 * k;  // 128 chunks of 16 codes
+        const int row = ci >> 3;
+        const int c = ci & 7;
+        const uint4 raw = *reinterpret_cast<const uint4*>(src + fp8_off(row, c * 16));
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t h01 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] & 0xffffu));
+            const uint32_t h23 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] >> 16));
+            if constexpr (std::is_same<T, __half>::value) {
+                o[2 * j] = h01;
+                o[2 * j + 1] = h23;
+            } else {
+                const float2 a = Elem<__half>::to_float2(h01);
+                const float2 b = Elem<__half>::to_float2(h23);
+                o[2 * j] = Elem<T>::pack(a.x, a.y);
+                o[2 * j + 1] = Elem<T>::pack(b.x, b.y);
+            }
+        }
+        *reinterpret_cast<uint4*>(dst + tile_off<128>(row, c * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(dst + tile_off<128>(row, c * 16 + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
     }
 }
 
@@ -68,7 +111,7 @@ __device__ __forceinline__ void issue_tile(const WarpRing& ring, int slot, int p
 // MHA block step: fp32 dot products on the ALU.
 // Lane l owns head dims [l*DPL, (l+1)*DPL).
 // ---------------------------------------------------------------------------
-template <typename T, int D>
+template <typename T, int D, bool kFp8 = false>
 struct AluState {
     static constexpr int DPL = D / 32;
     float q[DPL];
@@ -77,7 +120,13 @@ struct AluState {
     float l;  // this lane's share (even lanes only)
 
     __device__ __forceinline__ void load_dims(const uint8_t* tile, int tok, int lane, float* x) const {
-        if constexpr (DPL == 4) {
+        if constexpr (kFp8) {
+            // four E4M3 codes (head_dim 128, one 128-byte row per token)
+            const uint32_t raw = *reinterpret_cast<const uint32_t*>(tile + fp8_off(tok, lane * 4));
+            const float2 a = Elem<__half>::to_float2(e4m3x2_to_f16x2(static_cast<uint16_t>(raw & 0xffffu)));
+            const float2 b = Elem<__half>::to_float2(e4m3x2_to_f16x2(static_cast<uint16_t>(raw >> 16)));
+            x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+        } else if constexpr (DPL == 4) {
             const uint2 raw = *reinterpret_cast<const uint2*>(tile + tile_off<D>(tok, lane * 4));
             const float2 a = Elem<T>::to_float2(raw.x), b = Elem<T>::to_float2(raw.y);
             x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
@@ -376,11 +425,12 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
 // STAGES blocks ahead of the block being computed, claiming the next item as
 // soon as the fetches reach the end of the current one, so the warp's HBM
 // pipeline never drains between items.  Warps never wait for one another.
-template <typename T, int D, bool kMma>
+template <typename T, int D, bool kMma, bool kFp8>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap) {
-    using Shape = DecodeShape<D>;
+    using Shape = DecodeShape<D, kFp8, kMma>;
+    constexpr int kDecodeStages = Shape::kStages;
     constexpr int kQueue = 8;  // claimed items not yet computed (<= STAGES + 1 in use)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bars[kDecodeWarps * kDecodeStages];
@@ -477,7 +527,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         const int phys = fi.bt[fblk];
         if (lane == 0) {
             if (phys >= 0 && phys < p.num_blocks) {
-                issue_tile<D>(ring, slot, phys, fi.g, &kmap, &vmap);
+                issue_tile<D, kFp8, kMma>(ring, slot, phys, fi.g, &kmap, &vmap);
             } else {
                 record_error(p.err, PA_DEVERR_BLOCK_ID_);
                 mbar_arrive(&ring.bars[slot]);  // complete the phase without data
@@ -509,7 +559,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
             load_q(it, qw);  // the fetch cursor has moved past this item already
         }
 
-        AluState<T, D> alu;
+        AluState<T, D, kFp8> alu;
         MmaState<T, D> mma;
         if constexpr (!kMma) {
 #pragma unroll
@@ -546,10 +596,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
                 uint8_t* kt = ring.base + slot * Shape::kStageBytes;
                 uint8_t* vt = kt + Shape::kTileBytes;
                 const int nvalid = min(16, it.tok1 - (it.blk0 + blk) * 16);
-                if constexpr (!kMma)
+                if constexpr (!kMma) {
                     alu.step(kt, vt, nvalid, lane);
-                else
+                } else if constexpr (kFp8) {
+                    uint8_t* ck = ring.base + kDecodeStages * Shape::kStageBytes;
+                    uint8_t* cv = ck + 16 * D * 2;
+                    convert_fp8_tile<T>(kt, ck, lane);
+                    convert_fp8_tile<T>(vt, cv, lane);
+                    __syncwarp();
+                    mma.step(ck, cv, nvalid, lane, p.scale_log2);
+                    __syncwarp();  // the next block's conversion overwrites ck / cv
+                } else {
                     mma.step(kt, vt, nvalid, lane, p.scale_log2);
+                }
             }
             // the slot is free again: refill it with the block STAGES ahead
             fence_proxy_async_smem();
@@ -561,6 +620,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         // ---- finalise this item: the output row, or the partition's partials
         if constexpr (!kMma) {
             constexpr int DPL = AluState<T, D>::DPL;
+#pragma unroll
+            for (int j = 0; j < DPL; ++j) alu.acc[j] *= p.v_scale;
             float lsum = alu.l;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
@@ -587,6 +648,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
                 for (int j = 0; j < DPL; ++j) p.ws_acc[pi * D + lane * DPL + j] = alu.acc[j];
             }
         } else {
+#pragma unroll
+            for (int mt = 0; mt < MmaState<T, D>::KS; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mma.o[mt][e] *= p.v_scale;
             float l0 = mma.l[0], l1 = mma.l[1];
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
@@ -718,11 +783,11 @@ int sm_count() {
     return count[dev];
 }
 
-template <typename T, int D, bool kMma>
+template <typename T, int D, bool kMma, bool kFp8 = false>
 cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t s) {
-    constexpr int smem = DecodeShape<D>::kSmemBytes;
-    auto kern = decode_kernel<T, D, kMma>;
+    constexpr int smem = DecodeShape<D, kFp8, kMma>::kSmemBytes;
+    auto kern = decode_kernel<T, D, kMma, kFp8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, s, p);
@@ -742,6 +807,17 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, cons
 }
 
 }  // namespace
+
+cudaError_t launch_decode_fp8(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                              int dtype, cudaStream_t s) {
+    if (p.num_seqs == 0) return cudaSuccess;
+    const bool mma = p.group > 1;
+    if (dtype == 0)
+        return mma ? launch_decode_t<__half, 128, true, true>(p, kmap, vmap, s)
+                   : launch_decode_t<__half, 128, false, true>(p, kmap, vmap, s);
+    return mma ? launch_decode_t<__nv_bfloat16, 128, true, true>(p, kmap, vmap, s)
+               : launch_decode_t<__nv_bfloat16, 128, false, true>(p, kmap, vmap, s);
+}
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           int head_dim, int dtype, cudaStream_t s) {

@@ -107,6 +107,16 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// 3-D tiled TMA load into shared memory, completing on `bar` (tx bytes).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -136,6 +146,27 @@ __device__ __forceinline__ uint32_t tile_off(int tok, int dim) {
     const int c = (dim & 63) >> 3;
     return static_cast<uint32_t>(tile * TileGeom<D>::kTileBytes + (dim >> 6) * TileGeom<D>::kHalfBytes + r * 128 +
                                  ((c ^ (r & 7)) << 4) + ((dim & 7) << 1));
+}
+
+// FP8 (E4M3) tiles: one token row of 128 codes (head_dim 128) per 128-byte
+// swizzle row, fetched with a single 3-D TMA per tile.
+__device__ __forceinline__ uint32_t fp8_off(int tok, int byte) {
+    return static_cast<uint32_t>(tok * 128 + ((((byte >> 4) ^ (tok & 7))) << 4) + (byte & 15));
+}
+
+// Two E4M3 codes (low byte first) -> two fp16 values (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
+    return r;
+}
+
+// Two fp32 values -> two E4M3 codes, round to nearest even, saturating to the
+// finite range; `lo` goes to the low byte.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 // ---------------------------------------------------------------------------

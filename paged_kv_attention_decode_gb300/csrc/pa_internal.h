@@ -56,7 +56,8 @@ struct DecodeParams {
     int group;                    // num_q_heads / num_kv_heads
     int partition_tokens;         // multiple of 16
     int max_parts;                // ceil(max_seq_len / partition_tokens)
-    float scale_log2;             // scale * log2(e)
+    float scale_log2;             // scale * log2(e) (times the K dequantisation scale for FP8)
+    float v_scale;                // V dequantisation scale (1 for 16-bit caches)
 };
 
 struct PrefillParams {
@@ -86,6 +87,13 @@ cudaError_t launch_kv_write(const void* key, const void* value, void* k_cache, v
                             int head_dim, unsigned int* err, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           int head_dim, int dtype, cudaStream_t s);
+// FP8 (E4M3) cache, head_dim 128; q/out of `dtype`.
+cudaError_t launch_decode_fp8(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                              int dtype, cudaStream_t s);
+cudaError_t launch_kv_write_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
+                                const int64_t* slots, int num_tokens, int num_blocks, int num_kv_heads,
+                                int src_dtype, float k_inv_scale, float v_inv_scale, unsigned int* err,
+                                cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            int head_dim, int dtype, int max_q_len, cudaStream_t s);
 // tcgen05 prefill: groups of 1, 2, 4 or 8 q heads per kv head; q_per_tile = 128 / group.

@@ -110,9 +110,14 @@ class Workload:
     def is_decode(self) -> bool:
         return bool(np.all(self.q_lens == 1))
 
+    @property
+    def cache_elem_bytes(self) -> int:
+        return 1 if self.meta.get("cache_dtype") == "fp8" else 2
+
     def kv_bytes_logical(self) -> int:
         """K+V bytes that attention reads if every sequence's blocks are distinct."""
-        return int(self.seq_lens.astype(np.int64).sum()) * 2 * self.num_kv_heads * self.head_dim * 2
+        return (int(self.seq_lens.astype(np.int64).sum()) * 2 * self.num_kv_heads * self.head_dim
+                * self.cache_elem_bytes)
 
     def used_blocks(self) -> np.ndarray:
         """Sorted distinct physical block ids referenced by the live part of the tables."""
@@ -125,13 +130,15 @@ def _blocks_for(n: np.ndarray, bs: int) -> np.ndarray:
     return (-(-n.astype(np.int64) // bs)).astype(np.int64)
 
 
-def _fill_normal(t: torch.Tensor, gen: torch.Generator, chunk_elems: int = 1 << 26) -> None:
-    """Fill ``t`` (any float dtype) with N(0,1) drawn in fp32, in chunks of dim-0 rows."""
+def _fill_normal(t: torch.Tensor, gen: torch.Generator, chunk_elems: int = 1 << 26, scale: float = 1.0) -> None:
+    """Fill ``t`` (any float dtype) with N(0, scale^2) drawn in fp32, in chunks of dim-0 rows."""
     flat = t.view(t.shape[0], -1)
     chunk_rows = max(1, chunk_elems // max(1, flat.shape[1]))
     for r0 in range(0, flat.shape[0], chunk_rows):
         r1 = min(flat.shape[0], r0 + chunk_rows)
         tmp = torch.randn((r1 - r0, flat.shape[1]), generator=gen, device=t.device, dtype=torch.float32)
+        if scale != 1.0:
+            tmp.mul_(scale)
         flat[r0:r1].copy_(tmp)
 
 
@@ -155,6 +162,8 @@ def build_workload(
     scale: float | None = None,
     block_size: int = BLOCK_SIZE,
     materialize: bool = True,
+    cache_dtype: str = "same",
+    kv_scale: float = 1.0 / 16,
 ) -> Workload:
     """Build a seeded workload.
 
@@ -173,6 +182,11 @@ def build_workload(
     (ids outside the pool, including negative ones).
 
     materialize: False builds the integer tables only (tensors are None).
+
+    cache_dtype: "same" (the pools hold ``dtype``) or "fp8": the pools hold
+    E4M3 codes (uint8) of N(0, 1) / kv_scale values drawn in fp32 and
+    converted by torch, so that code * kv_scale is about N(0, 1); the new
+    key/value rows stay in ``dtype`` (they are quantised by the write).
     """
     rng = np.random.Generator(np.random.PCG64(seed))
     seq_lens = np.asarray(seq_lens, dtype=np.int32).reshape(-1)
@@ -244,11 +258,19 @@ def build_workload(
     q = torch.empty((T, num_q_heads, head_dim), dtype=tdt, device=dev)
     key = torch.empty((T, num_kv_heads, head_dim), dtype=tdt, device=dev)
     value = torch.empty((T, num_kv_heads, head_dim), dtype=tdt, device=dev)
-    k_cache = torch.empty((num_blocks, bs, num_kv_heads, head_dim), dtype=tdt, device=dev)
-    v_cache = torch.empty((num_blocks, bs, num_kv_heads, head_dim), dtype=tdt, device=dev)
-    for t in (q, key, value, k_cache, v_cache):
+    fp8 = cache_dtype == "fp8"
+    cdt = torch.float8_e4m3fn if fp8 else tdt
+    k_cache = torch.empty((num_blocks, bs, num_kv_heads, head_dim), dtype=cdt, device=dev)
+    v_cache = torch.empty((num_blocks, bs, num_kv_heads, head_dim), dtype=cdt, device=dev)
+    for t in (q, key, value):
         if t.numel():
             _fill_normal(t, gen)
+    for t in (k_cache, v_cache):
+        if t.numel():
+            _fill_normal(t, gen, scale=1.0 / kv_scale if fp8 else 1.0)
+    if fp8:
+        k_cache = k_cache.view(torch.uint8)
+        v_cache = v_cache.view(torch.uint8)
 
     if poison:
         live = np.zeros((num_blocks, bs), dtype=bool)
@@ -259,9 +281,12 @@ def build_workload(
                 n_ok = max(0, min(bs, first_new - lo))
                 live[tables[b, j], :n_ok] = True
         dead = torch.from_numpy(~live).to(dev)
-        nan = torch.tensor(float("nan"), dtype=tdt, device=dev)
+        nan = torch.tensor(0x7F if fp8 else float("nan"), dtype=k_cache.dtype, device=dev)
         k_cache.masked_fill_(dead[:, :, None, None], nan)
         v_cache.masked_fill_(dead[:, :, None, None], nan)
+    if fp8:
+        meta["kv_scale"] = float(kv_scale)
+        meta["cache_dtype"] = "fp8"
 
     return Workload(
         name=name, dtype=dtype, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
@@ -275,7 +300,8 @@ def build_workload(
 # the named workloads
 # ---------------------------------------------------------------------------
 
-CONFIG_NAMES = ("tiny", "llama7b_decode", "gqa_prefix", "long_context", "mixed", "llama7b_ctx4096")
+CONFIG_NAMES = ("tiny", "llama7b_decode", "gqa_prefix", "long_context", "mixed", "llama7b_ctx4096",
+                "llama7b_decode_fp8")
 
 
 def _seed(idx: int) -> int:
@@ -380,6 +406,16 @@ def config_mixed(device="cpu", n_prefill=4, chunk=1536, n_decode=2048,
                           device=device, **kw)
 
 
+def config_llama7b_decode_fp8(device="cpu", batch=64, lo=512, hi=4096, **kw) -> Workload:
+    """The LLaMA-2-7B-shaped decode workload with an FP8 (E4M3) cache."""
+    seed = _seed(1)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lens = rng.integers(lo, hi + 1, size=batch).astype(np.int32)
+    return build_workload(name="llama7b_decode_fp8", seq_lens=lens, q_lens=1, num_q_heads=32,
+                          num_kv_heads=32, head_dim=128, dtype="f16", seed=seed + 1000,
+                          device=device, cache_dtype="fp8", **kw)
+
+
 CONFIGS = {
     "tiny": config_tiny,
     "llama7b_decode": config_llama7b_decode,
@@ -387,6 +423,7 @@ CONFIGS = {
     "long_context": config_long_context,
     "mixed": config_mixed,
     "llama7b_ctx4096": config_llama7b_ctx4096,
+    "llama7b_decode_fp8": config_llama7b_decode_fp8,
 }
 
 
