@@ -39,13 +39,14 @@ constexpr unsigned kFull = 0xffffffffu;
 
 // Per-warp shared memory: a ring of kStages (K tile, V tile) slots, plus, for
 // the FP8 GQA path, one K and one V tile converted to 16-bit for the MMA.
-// FP8 tiles are half the bytes, so the FP8 rings are deeper: the same bytes
-// stay in flight per warp.
+// A warp handles one block at a time, so it moves bytes at (tile bytes) /
+// (block latency); FP8 tiles are half the bytes, so the FP8 MHA kernel keeps
+// small rings and runs more CTAs (warps) per SM instead.
 template <int D, bool kFp8, bool kMma>
 struct DecodeShape {
     static constexpr int kTileBytes = 16 * D * (kFp8 ? 1 : 2);  // one (block, kv head) tile
     static constexpr int kStageBytes = 2 * kTileBytes;          // K tile + V tile
-    static constexpr int kStages = kFp8 ? (kMma ? 4 : 6) : 3;
+    static constexpr int kStages = kFp8 ? (kMma ? 4 : 2) : 3;
     static constexpr int kConvBytes = (kFp8 && kMma) ? 2 * 16 * D * 2 : 0;
     static constexpr int kWarpBytes = kStages * kStageBytes + kConvBytes;
     static constexpr int kSmemBytes = kDecodeWarps * kWarpBytes + 1024;  // + alignment slack
@@ -792,10 +793,13 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, cons
     if (e != cudaSuccess) return e;
     e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, s, p);
     if (e != cudaSuccess) return e;
-    // persistent: two CTAs per SM, fewer when there cannot be that many items
+    // persistent: as many CTAs as fit on every SM (shared memory bound), fewer
+    // when there cannot be that many items
+    constexpr int kCtasPerSm = (228 * 1024) / (smem + 2048);
     const long long max_items = static_cast<long long>(p.num_seqs) * p.max_parts * p.num_kv_heads;
     const long long want = (max_items + kDecodeWarps - 1) / kDecodeWarps;
-    const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(want, 2LL * sm_count())));
+    const int grid = static_cast<int>(
+        std::max<long long>(1, std::min<long long>(want, static_cast<long long>(kCtasPerSm) * sm_count())));
     e = launch_pdl(kern, dim3(grid), dim3(kDecodeWarps * 32), smem, s, p, kmap, vmap);
     if (e != cudaSuccess) return e;
     if (p.max_parts > 1) {
