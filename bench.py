@@ -424,7 +424,8 @@ def run_ours(args):
                    "l2": f"inputs larger than L2: {ab['kv_unique'] / 1e9:.2f} GB of KV read per step"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _traffic_per_launch(args.workload),
-                     "kernel": ("decode attention (partition kernel + log-sum-exp reduce)" if decode else
+                     "kernel": ("decode attention call (work-list plan + persistent decode kernel + log-sum-exp "
+                                "reduce)" if decode else
                                 "attention call (decode rows: partition + reduce kernels; chunks: prefill kernel)"),
                      "peak_kind": f"{peak_kind} HBM copy", "frac_of_8TBs_spec": achieved / SPEC_HBM_GBS,
                      "algorithmic_bytes_per_launch": ab["total"], "ms_per_launch": attn_ms},
