@@ -55,6 +55,9 @@ extern "C" {
 #define PA_BLOCK_SIZE 16
 #define PA_DEFAULT_PARTITION 512
 #define PA_MAX_GROUP 8
+/* Chunks of at most this many queries (decode rows, speculative-verify rows)
+ * run in the decode kernel inside pa_paged_attention_prefill. */
+#define PA_VERIFY_MAX_Q 8
 
 typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
 
@@ -141,23 +144,35 @@ int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, con
                               int head_dim, int block_size, int partition_size, void* workspace,
                               size_t workspace_bytes, int dtype, void* stream);
 
-/* Workspace for pa_paged_attention_prefill: the chunk tile work list
- * (num_seqs + 1 int32) followed by the decode rows' split-context partials.
- * Nonzero whenever num_seqs > 0. */
-size_t pa_prefill_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len);
+/* Workspace for pa_paged_attention_prefill over num_seqs sequences and
+ * num_tokens query rows: the chunk tile work list (num_seqs + 1 int32), the
+ * decode kernel's work list, and the split-context partials of up to
+ * min(num_tokens, PA_VERIFY_MAX_Q * num_seqs) query rows of decode and verify
+ * chunks (partitions of PA_DEFAULT_PARTITION tokens).  Nonzero whenever
+ * num_seqs > 0; 0 for a negative argument. */
+size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_q_heads, int head_dim,
+                                  int max_seq_len);
 
 /*
  * Causal attention of query chunks appended onto a cached prefix, as in
  * chunked prefill ("vLLM-Ascend 原理", section 2.3 "因果自注意力": the query
  * at position i sees positions 0..i; section 2.4: a later chunk reads the KV
  * that earlier chunks wrote).  Query row cu_q_lens[b] + i of sequence b sits
- * at position seq_lens[b] - q_len_b + i.  Sequences with q_len == 1 are
- * decodes and run through the decode kernel; longer chunks run through the
- * tensor-core prefill kernel.  The new tokens' k/v must already be in the
- * cache (pa_paged_kv_write first).
+ * at position seq_lens[b] - q_len_b + i.  Sequences with 1 <= q_len <=
+ * PA_VERIFY_MAX_Q run through the decode kernel: single-query decodes, and the
+ * speculative-decoding verify step, where the k draft tokens and the last
+ * accepted one form a mini-prefill of q_len = k + 1 queries ("vLLM-Ascend
+ * 原理", section 4 "推测解码").  Longer chunks run through the tensor-core
+ * prefill kernel.  The new tokens' k/v must already be in the cache
+ * (pa_paged_kv_write first).  Rolling back rejected drafts needs no call:
+ * lowering seq_lens[b] hides every position at or past it, and the next
+ * write overwrites those slots.
  *   out, q        [num_tokens, num_q_heads, head_dim]; num_tokens = cu_q_lens[num_seqs]
- *   max_q_len, max_seq_len  host-side upper bounds (grid sizing).
- *   workspace     >= pa_prefill_workspace_bytes(...) bytes, 256-byte aligned.
+ *   max_q_len, max_seq_len  host-side upper bounds (grid sizing, routing).
+ *   workspace     >= pa_prefill_workspace_bytes(num_seqs, num_tokens, ...) bytes,
+ *                 256-byte aligned.
+ * A chunk longer than its seq_len, or a decode/verify chunk longer than
+ * max_q_len, sets PA_DEVERR_SEQ_LEN and gets zero rows.
  */
 int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* block_tables, int max_blocks_per_seq,

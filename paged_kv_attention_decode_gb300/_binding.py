@@ -34,7 +34,7 @@ _SIGNATURES = {
     "pa_decode_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "pa_paged_attention_decode": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _f32,
                                          _i32, _i32, _i32, _i32, _i32, _p, _sz, _i32, _p]),
-    "pa_prefill_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
+    "pa_prefill_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "pa_paged_attention_prefill": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32,
                                           _i32, _i32, _f32, _i32, _i32, _i32, _i32, _p, _sz,
                                           _i32, _p]),
@@ -149,8 +149,10 @@ def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_s
                                                         partition_size))
 
 
-def prefill_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_seq_len: int) -> int:
-    return int(load_library().pa_prefill_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len))
+def prefill_workspace_bytes(num_seqs: int, num_tokens: int, num_q_heads: int, head_dim: int,
+                            max_seq_len: int) -> int:
+    return int(load_library().pa_prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, head_dim,
+                                                         max_seq_len))
 
 
 def _workspace(nbytes: int, device, workspace):
@@ -192,7 +194,11 @@ def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
                             cu_q_lens: torch.Tensor, scale: float, max_q_len: int,
                             max_seq_len: int, out: torch.Tensor | None = None,
                             workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Causal varlen attention of new query rows over the paged cache."""
+    """Causal varlen attention of new query rows over the paged cache.
+
+    Chunks of at most PA_VERIFY_MAX_Q (8) queries -- decodes and speculative
+    verify steps -- run in the decode kernel, longer chunks in the prefill
+    kernels."""
     _cuda(q, k_cache, v_cache, block_tables, seq_lens, cu_q_lens, out, workspace)
     T, Hq, D = q.shape
     NB, bs, Hkv, D2 = k_cache.shape
@@ -201,7 +207,7 @@ def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     _need(cu_q_lens.shape[0] == B + 1 and cu_q_lens.dtype == torch.int32, "cu_q_lens")
     if out is None:
         out = torch.empty_like(q)
-    nbytes = prefill_workspace_bytes(B, Hq, D, max_seq_len)
+    nbytes = prefill_workspace_bytes(B, T, Hq, D, max_seq_len)
     workspace = _workspace(nbytes, q.device, workspace)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load_library().pa_paged_attention_prefill(

@@ -1,6 +1,7 @@
 // C ABI of libpagedattn.so: argument validation, tensor-map set-up, launches.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -122,25 +123,43 @@ size_t partials_bytes(int num_seqs, int num_q_heads, int head_dim, int parts) {
     return 2 * align256(n * sizeof(float)) + align256(n * head_dim * sizeof(float));
 }
 
-// Decode workspace: [unit count (256 B)][unit list: num_seqs * parts int32][partials when parts > 1]
-size_t decode_ws_bytes(int num_seqs, int num_q_heads, int head_dim, int parts) {
+// Decode workspace:
+//   [header 256 B: unit count @0, partials row count @64, work counter @128]
+//   [unit list: num_seqs * parts int32]
+//   when parts > 1: [row_base: num_seqs int32][rows: max_rows int32][partials of max_rows rows]
+size_t decode_ws_bytes(int num_seqs, int max_rows, int num_q_heads, int head_dim, int parts) {
     size_t b = 256 + align256(static_cast<size_t>(num_seqs) * parts * sizeof(int32_t));
-    if (parts > 1) b += partials_bytes(num_seqs, num_q_heads, head_dim, parts);
+    if (parts > 1)
+        b += align256(static_cast<size_t>(num_seqs) * sizeof(int32_t)) +
+             align256(static_cast<size_t>(max_rows) * sizeof(int32_t)) +
+             partials_bytes(max_rows, num_q_heads, head_dim, parts);
     return b;
 }
 
 void carve_workspace(pa::DecodeParams& p, void* ws) {
     uint8_t* base = static_cast<uint8_t*>(ws);
     p.unit_count = reinterpret_cast<int32_t*>(base);
+    p.row_count = reinterpret_cast<int32_t*>(base + 64);
     p.work_counter = reinterpret_cast<int32_t*>(base + 128);
     p.units = reinterpret_cast<int32_t*>(base + 256);
     base += 256 + align256(static_cast<size_t>(p.num_seqs) * p.max_parts * sizeof(int32_t));
     if (p.max_parts > 1) {
-        const size_t n = static_cast<size_t>(p.num_seqs) * p.num_q_heads * p.max_parts;
+        p.row_base = reinterpret_cast<int32_t*>(base);
+        base += align256(static_cast<size_t>(p.num_seqs) * sizeof(int32_t));
+        p.rows = reinterpret_cast<int32_t*>(base);
+        base += align256(static_cast<size_t>(p.max_rows) * sizeof(int32_t));
+        const size_t n = static_cast<size_t>(p.max_rows) * p.num_q_heads * p.max_parts;
         p.ws_m = reinterpret_cast<float*>(base);
         p.ws_l = reinterpret_cast<float*>(base + align256(n * sizeof(float)));
         p.ws_acc = reinterpret_cast<float*>(base + 2 * align256(n * sizeof(float)));
     }
+}
+
+// Query rows of a varlen call that can need split-context partials: only
+// chunks of at most PA_VERIFY_MAX_Q queries run in the decode kernel.
+int verify_rows_bound(int num_seqs, int num_tokens) {
+    const long long r = std::min<long long>(num_tokens, static_cast<long long>(num_seqs) * PA_VERIFY_MAX_Q);
+    return static_cast<int>(r);
 }
 
 float scale_log2(float scale) { return scale * 1.4426950408889634f; }
@@ -202,19 +221,19 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, in
                                  int partition_size) {
     if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len < 0 || partition_size < 0) return 0;
     const int part = partition_size ? partition_size : PA_DEFAULT_PARTITION;
-    return decode_ws_bytes(num_seqs, num_q_heads, head_dim, parts_for(max_seq_len, part));
+    return decode_ws_bytes(num_seqs, num_seqs, num_q_heads, head_dim, parts_for(max_seq_len, part));
 }
 
 static int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
                        const int32_t* cu_q_lens, int num_seqs, int max_seq_len, int num_blocks, float scale,
                        int num_q_heads, int num_kv_heads, int head_dim, int partition_size, void* workspace,
-                       size_t workspace_bytes, int dtype, cudaStream_t stream, bool fp8 = false,
-                       float k_scale = 1.f, float v_scale = 1.f) {
+                       size_t workspace_bytes, int dtype, cudaStream_t stream, int max_q, int max_rows,
+                       bool fp8 = false, float k_scale = 1.f, float v_scale = 1.f) {
     const int part = partition_size ? partition_size : PA_DEFAULT_PARTITION;
     const int parts = parts_for(max_seq_len, part);
     if (parts > 65535) return PA_ERR_INVALID_ARG;   // partition index is a 16-bit field of the work list
-    const size_t need = decode_ws_bytes(num_seqs, num_q_heads, head_dim, parts);
+    const size_t need = decode_ws_bytes(num_seqs, max_rows, num_q_heads, head_dim, parts);
     if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned256(workspace)) return PA_ERR_INVALID_ARG;
     unsigned int* err = error_word();
@@ -242,6 +261,11 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
     p.group = num_q_heads / num_kv_heads;
     p.partition_tokens = part;
     p.max_parts = parts;
+    p.max_q = max_q;
+    p.max_rows = max_rows;
+    // (query, head) columns per work item: 8, or 16 once a row can have more
+    const int cols = max_q * p.group;
+    p.col_chunks = cols > 8 ? (cols + 15) / 16 : 1;
     p.scale_log2 = scale_log2(scale) * k_scale;
     p.v_scale = v_scale;
     carve_workspace(p, workspace);
@@ -265,7 +289,7 @@ int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, con
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
     return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
                        max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, partition_size,
-                       workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream));
+                       workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream), 1, num_seqs);
 }
 
 // Prefill workspace: [tile work list: num_seqs + 1 int32, 256-aligned][decode-row partials].
@@ -311,13 +335,14 @@ int pa_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache,
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
     return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
                        max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, partition_size,
-                       workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream), true, k_scale,
-                       v_scale);
+                       workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream), 1, num_seqs, true,
+                       k_scale, v_scale);
 }
 
-size_t pa_prefill_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len) {
-    if (num_seqs <= 0) return 0;
-    return plan_bytes(num_seqs) + pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len, 0);
+size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_q_heads, int head_dim, int max_seq_len) {
+    if (num_seqs <= 0 || num_tokens < 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len < 0) return 0;
+    return plan_bytes(num_seqs) + decode_ws_bytes(num_seqs, verify_rows_bound(num_seqs, num_tokens), num_q_heads,
+                                                  head_dim, parts_for(max_seq_len, PA_DEFAULT_PARTITION));
 }
 
 int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -337,16 +362,20 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t pb = plan_bytes(num_seqs);
-    if (!workspace || workspace_bytes < pa_prefill_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len))
+    if (!workspace ||
+        workspace_bytes < pa_prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, head_dim, max_seq_len))
         return PA_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned256(workspace)) return PA_ERR_INVALID_ARG;
     int32_t* plan = static_cast<int32_t*>(workspace);
-    // decode rows (q_len == 1) through the decode kernel
+    // decode rows (q_len == 1) and speculative-verify rows (q_len <= PA_VERIFY_MAX_Q)
+    // through the decode kernel
+    const int max_q = std::max(1, std::min(max_q_len, PA_VERIFY_MAX_Q));
     rc = decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens, num_seqs,
                      max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, 0,
-                     static_cast<uint8_t*>(workspace) + pb, workspace_bytes - pb, dtype, s);
+                     static_cast<uint8_t*>(workspace) + pb, workspace_bytes - pb, dtype, s, max_q,
+                     verify_rows_bound(num_seqs, num_tokens));
     if (rc) return rc;
-    if (max_q_len <= 1) return PA_OK;
+    if (max_q_len <= PA_VERIFY_MAX_Q) return PA_OK;
     unsigned int* err = error_word();
     CUtensorMap kmap, vmap;
     if (!make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) ||

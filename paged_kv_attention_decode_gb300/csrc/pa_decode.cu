@@ -221,24 +221,37 @@ struct AluState {
 };
 
 // ---------------------------------------------------------------------------
-// GQA block step on the tensor cores (mma.sync m16n8k16, fp32 accumulate).
-// S^T = K Q^T: rows = 16 tokens of the block, cols = 8 (padded) query heads.
-// Lane l holds S^T rows l/4 and l/4+8, head columns 2*(l%4) and 2*(l%4)+1;
-// O^T (head_dim x heads) uses the same columns, so the per-head rescale needs
-// no data movement.
+// Query-group x K-block step on the tensor cores (mma.sync m16n8k16, fp32
+// accumulate).  The columns are (query, head) pairs that share one kv head:
+// the `group` heads of a decode row, or q_len x group pairs of a
+// speculative-verify row, in NT tiles of 8 columns.
+// S^T = K Q^T: rows = the 16 tokens of the block.  Lane l holds S^T rows l/4
+// and l/4+8 of columns 8*nt + 2*(l%4) + {0,1}; O^T (head_dim x columns) uses
+// the same columns, so the per-column rescale needs no data movement.  Column
+// j sees the tokens below lim[nt][e]: its query's causal limit, capped at the
+// partition end.
 // ---------------------------------------------------------------------------
-template <typename T, int D>
+template <typename T, int D, int NT>
 struct MmaState {
     static constexpr int KS = D / 16;
-    uint32_t qb[KS][2];   // Q^T as the B operand, per 16-dim k-step
-    float o[KS][4];       // O^T accumulator, per 16-dim m-tile
-    float m[2];
-    float l[2];
+    uint32_t qb[KS][NT][2];   // Q^T as the B operand, per 16-dim k-step and column tile
+    float o[KS][NT][4];       // O^T accumulator, per 16-dim m-tile and column tile
+    float m[NT][2];
+    float l[NT][2];
+    int lim[NT][2];           // first token the column may not see
 
-    __device__ __forceinline__ void step(uint8_t* kt, uint8_t* vt, int nvalid, int lane, float scale_log2) {
+    // `masked`: some column of this block has a limit inside it (else every
+    // token of the block is visible to every column).  Rows at or past
+    // `nvalid` lie beyond the partition end.
+    __device__ __forceinline__ void step(uint8_t* kt, uint8_t* vt, int base, int nvalid, bool masked, int lane,
+                                         float scale_log2) {
         const uint32_t ka = smem_addr(kt);
         const uint32_t va = smem_addr(vt);
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        float c[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c[nt][e] = 0.f;
         {
             const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
             const int dsub = ((lane >> 4) & 1) * 8;
@@ -246,49 +259,64 @@ struct MmaState {
             for (int kk = 0; kk < KS; ++kk) {
                 uint32_t a[4];
                 ldsm_x4(ka + tile_off<D>(tok, kk * 16 + dsub), a[0], a[1], a[2], a[3]);
-                Mma<T>::run(c, a, qb[kk][0], qb[kk][1]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) Mma<T>::run(c[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
             }
         }
         const int r0 = lane >> 2;
-        float s0 = r0 < nvalid ? c[0] * scale_log2 : -INFINITY;
-        float s1 = r0 < nvalid ? c[1] * scale_log2 : -INFINITY;
-        float s2 = r0 + 8 < nvalid ? c[2] * scale_log2 : -INFINITY;
-        float s3 = r0 + 8 < nvalid ? c[3] * scale_log2 : -INFINITY;
-        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+        uint32_t b0[NT], b1[NT];
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
-        }
-        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-        const float al0 = fast_exp2(m[0] - mn0), al1 = fast_exp2(m[1] - mn1);
-        m[0] = mn0;
-        m[1] = mn1;
-        const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
-        const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
-        l[0] = l[0] * al0 + p0 + p2;
-        l[1] = l[1] * al1 + p1 + p3;
+        for (int nt = 0; nt < NT; ++nt) {
+            float s[4];
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
+            for (int e = 0; e < 2; ++e) {
+                const bool v0 = !masked || base + r0 < lim[nt][e];
+                const bool v8 = !masked || base + r0 + 8 < lim[nt][e];
+                s[e] = v0 ? c[nt][e] * scale_log2 : -INFINITY;
+                s[2 + e] = v8 ? c[nt][2 + e] * scale_log2 : -INFINITY;
+            }
+            float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+            }
+            const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+            // a column that has seen no visible token yet keeps m = -inf; its
+            // weights are then exp2(-inf - 0) = 0, never exp2(-inf + inf)
+            const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+            const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = fast_exp2(m[nt][0] - mu0), al1 = fast_exp2(m[nt][1] - mu1);
+            m[nt][0] = mn0;
+            m[nt][1] = mn1;
+            const float p0 = fast_exp2(s[0] - mu0), p1 = fast_exp2(s[1] - mu1);
+            const float p2 = fast_exp2(s[2] - mu0), p3 = fast_exp2(s[3] - mu1);
+            l[nt][0] = l[nt][0] * al0 + p0 + p2;
+            l[nt][1] = l[nt][1] * al1 + p1 + p3;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                o[mt][nt][0] *= al0;
+                o[mt][nt][1] *= al1;
+                o[mt][nt][2] *= al0;
+                o[mt][nt][3] *= al1;
+            }
+            // P^T as the B operand: lane l needs P[token 2*(l%4)+e (+8)][column l/4].
+            const uint32_t lo = Elem<T>::pack(p0, p1);
+            const uint32_t hi = Elem<T>::pack(p2, p3);
+            const int src0 = ((lane & 3) << 3) + (lane >> 3);
+            const uint32_t x0 = __shfl_sync(kFull, lo, src0);
+            const uint32_t x1 = __shfl_sync(kFull, lo, src0 + 4);
+            const uint32_t y0 = __shfl_sync(kFull, hi, src0);
+            const uint32_t y1 = __shfl_sync(kFull, hi, src0 + 4);
+            const uint32_t sel = ((lane >> 2) & 1) ? 0x7632u : 0x5410u;
+            b0[nt] = __byte_perm(x0, x1, sel);
+            b1[nt] = __byte_perm(y0, y1, sel);
         }
-        // P^T as the B operand: lane l needs P[token 2*(l%4)+e (+8)][head l/4].
-        const uint32_t lo = Elem<T>::pack(p0, p1);
-        const uint32_t hi = Elem<T>::pack(p2, p3);
-        const int src0 = ((lane & 3) << 3) + (lane >> 3);
-        const uint32_t x0 = __shfl_sync(kFull, lo, src0);
-        const uint32_t x1 = __shfl_sync(kFull, lo, src0 + 4);
-        const uint32_t y0 = __shfl_sync(kFull, hi, src0);
-        const uint32_t y1 = __shfl_sync(kFull, hi, src0 + 4);
-        const uint32_t sel = ((lane >> 2) & 1) ? 0x7632u : 0x5410u;
-        const uint32_t b0 = __byte_perm(x0, x1, sel);
-        const uint32_t b1 = __byte_perm(y0, y1, sel);
         if (nvalid < 16) {
             // rows past the sequence end may hold anything (even NaN): p = 0
             // there, but 0 * NaN would poison the product, so clear them.
+            // (Rows before the end that a column may not see are cache data
+            // of the sequence: finite.)
             const int nchunks = (16 - nvalid) * 8;   // 16-byte chunks per half
 #pragma unroll
             for (int h = 0; h < D / 64; ++h) {
@@ -304,19 +332,23 @@ struct MmaState {
             for (int mt = 0; mt < KS; ++mt) {
                 uint32_t a[4];
                 ldsm_x4_t(va + tile_off<D>(tok, mt * 16 + dsub), a[0], a[1], a[2], a[3]);
-                Mma<T>::run(o[mt], a, b0, b1);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) Mma<T>::run(o[mt][nt], a, b0[nt], b1[nt]);
             }
         }
     }
 };
 
 // ---------------------------------------------------------------------------
-// work list: one unit per (sequence, partition) of every decode row
+// work list: one unit per (sequence, partition) of every decode or verify row
 // ---------------------------------------------------------------------------
-// units[k] = (b << 16) | partition; *unit_count = total.
+// units[k] = (b << 16) | partition; *unit_count = total.  A row here is a
+// sequence whose chunk has 1..max_q queries (one query without cu_q_lens).
 // A sequence of length 0 (or one rejected by the bounds checks) gets no unit:
-// its zero output row is written here.  Rows with q_len != 1 in a mixed batch
-// belong to the prefill kernel and get none.  Also resets the work counter.
+// its zero output rows are written here.  Longer chunks of a varlen batch
+// belong to the prefill kernels and get none.  Every query of a sequence that
+// is split into several partitions gets a partials row, listed in `rows` as
+// (b << 3) | query index from row_base[b] on.  Also resets the work counter.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* carry, int& chunk_total) {
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -352,61 +384,82 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* c
 // the small ones.
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p) {
     __shared__ int warp_tot[32];
-    __shared__ int carry;
+    __shared__ int carry_u;
+    __shared__ int carry_r;
     const int tid = threadIdx.x;
     // the decode kernel may launch now; it waits for this grid to complete
     // before it reads the list
     pdl_trigger();
     const int P = p.partition_tokens;
-    auto seq_len_of = [&](int b, bool record) -> int {
-        if (p.cu_q_lens && p.cu_q_lens[b + 1] - p.cu_q_lens[b] != 1) return -1;  // not a decode row
+    // (length, queries) of row b; queries = 0 when the row is not handled here
+    auto row_of = [&](int b, bool record, int& qlen) -> int {
+        qlen = 1;
+        if (p.cu_q_lens) {
+            qlen = p.cu_q_lens[b + 1] - p.cu_q_lens[b];
+            if (qlen < 1 || qlen > PA_VERIFY_MAX_Q_) {
+                qlen = 0;
+                return 0;
+            }
+        }
         int n = p.seq_lens[b];
-        if (n < 0 || n > p.max_seq_len || n > p.max_blocks * 16) {
+        const bool bad = n < 0 || n > p.max_seq_len || n > p.max_blocks * 16 || qlen > p.max_q ||
+                         (qlen > 1 && n < qlen);
+        if (bad) {
             if (record) record_error(p.err, PA_DEVERR_SEQ_LEN_);
             n = 0;
         }
         return n;
     };
     int chunk_total = 0;
-    // pass 1: full partitions (and the zero rows of empty sequences)
-    if (tid == 0) carry = 0;
+    // pass 1: full partitions, partials rows (and the zero rows of empty sequences)
+    if (tid == 0) {
+        carry_u = 0;
+        carry_r = 0;
+    }
     __syncthreads();
     for (int base = 0; base < p.num_seqs; base += 1024) {
         const int b = base + tid;
-        int v = 0;
+        int v = 0, vr = 0, qlen = 0;
         if (b < p.num_seqs) {
-            const int n = seq_len_of(b, true);
+            const int n = row_of(b, true, qlen);
             if (n > 0) {
                 v = n / P;
-            } else if (n == 0) {
-                // an empty (or rejected) sequence gets the zero row here
+                vr = n > P ? qlen : 0;
+            } else if (qlen > 0) {
+                // an empty (or rejected) sequence gets zero rows here
                 const int qrow = p.cu_q_lens ? p.cu_q_lens[b] : b;
                 uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
                                                     static_cast<int64_t>(qrow) * p.num_q_heads * p.head_dim);
-                for (int i = 0; i < p.num_q_heads * p.head_dim / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+                for (int i = 0; i < qlen * p.num_q_heads * p.head_dim / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
             }
         }
-        const int start = block_exclusive_scan(v, warp_tot, &carry, chunk_total);
+        const int start = block_exclusive_scan(v, warp_tot, &carry_u, chunk_total);
         for (int i = 0; i < v; ++i)
             p.units[start + i] = static_cast<int32_t>((static_cast<uint32_t>(b) << 16) | static_cast<uint32_t>(i));
+        const int rstart = block_exclusive_scan(vr, warp_tot, &carry_r, chunk_total);
+        if (vr) {
+            p.row_base[b] = rstart;
+            for (int i = 0; i < vr; ++i) p.rows[rstart + i] = static_cast<int32_t>((static_cast<uint32_t>(b) << 3) | i);
+        }
     }
     // pass 2: the partial last partitions
     for (int base = 0; base < p.num_seqs; base += 1024) {
         const int b = base + tid;
-        int v = 0, last = 0;
+        int v = 0, last = 0, qlen = 0;
         if (b < p.num_seqs) {
-            const int n = seq_len_of(b, false);
+            const int n = row_of(b, false, qlen);
             if (n > 0 && n % P) {
                 v = 1;
                 last = n / P;
             }
         }
-        const int start = block_exclusive_scan(v, warp_tot, &carry, chunk_total);
+        const int start = block_exclusive_scan(v, warp_tot, &carry_u, chunk_total);
         if (v) p.units[start] = static_cast<int32_t>((static_cast<uint32_t>(b) << 16) | static_cast<uint32_t>(last));
     }
     if (tid == 0) {
-        *p.unit_count = carry;
+        *p.unit_count = carry_u;
         *p.work_counter = 0;
+        if (p.row_count) *p.row_count = carry_r;
     }
     // Only the lengths and tables (inputs) were read above, so this grid may
     // have overlapped the previous kernel of the stream (the KV write).  It
@@ -418,21 +471,25 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
 // ---------------------------------------------------------------------------
 // the decode kernel
 // ---------------------------------------------------------------------------
-// Persistent, warp-granular: work item w = (unit w / Hkv, kv head w % Hkv) is
+// Persistent, warp-granular: work item w = (unit, kv head, column chunk) is
 // one partition of one sequence for one kv head, handled start to finish by a
-// single warp.  Warps claim items from a global counter as they go (dynamic
-// balance).  Each warp streams the 16-token blocks of its items, in order,
-// through its own ring of shared-memory slots: lane 0 keeps the TMA fetches
-// STAGES blocks ahead of the block being computed, claiming the next item as
-// soon as the fetches reach the end of the current one, so the warp's HBM
-// pipeline never drains between items.  Warps never wait for one another.
-template <typename T, int D, bool kMma, bool kFp8>
+// single warp, for up to 16 of the (query, head) pairs that read that kv head
+// (kMaxNT = 2; 8 when kMaxNT = 1).  Warps claim items from a global counter as
+// they go (dynamic balance).  Each warp streams the 16-token blocks of its
+// items, in order, through its own ring of shared-memory slots: lane 0 keeps
+// the TMA fetches STAGES blocks ahead of the block being computed, claiming
+// the next item as soon as the fetches reach the end of the current one, so
+// the warp's HBM pipeline never drains between items.  Warps never wait for
+// one another.
+template <typename T, int D, bool kMma, bool kFp8, int kMaxNT>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap) {
+    static_assert(kMma || kMaxNT == 1, "the FMA path handles one query per row");
     using Shape = DecodeShape<D, kFp8, kMma>;
     constexpr int kDecodeStages = Shape::kStages;
     constexpr int kQueue = 8;  // claimed items not yet computed (<= STAGES + 1 in use)
+    constexpr int kChunkCols = 8 * kMaxNT;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bars[kDecodeWarps * kDecodeStages];
     __shared__ int claimed[kDecodeWarps][kQueue];
@@ -441,6 +498,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     const int lane = threadIdx.x & 31;
     const int G = p.group;
     const int H = p.num_kv_heads;
+    const int C = p.col_chunks;
     const int P = p.partition_tokens;
 
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -454,27 +512,57 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
     pdl_wait();  // the work list (and, through it, the KV write) is complete
-    const int total = *p.unit_count * H;
+    const int total = *p.unit_count * H * C;
     if (total == 0) return;
     int* queue = claimed[warp];
 
     struct Item {
-        int b, g, part, n, tok1, blk0, nblk;
+        int b, g, part, n, qlen, qrow0, col0, ncols, tok1, lim_min, blk0, nblk;
         const int32_t* bt;
     };
     auto load_item = [&](int w, Item& it) {
-        const uint32_t unit = static_cast<uint32_t>(p.units[w / H]);
-        it.g = w % H;
+        const int ug = w / C;
+        const uint32_t unit = static_cast<uint32_t>(p.units[ug / H]);
+        it.g = ug % H;
         it.b = static_cast<int>(unit >> 16);
         it.part = static_cast<int>(unit & 0xffffu);
+        it.qlen = 1;
+        it.qrow0 = it.b;
+        if (p.cu_q_lens) {
+            it.qrow0 = p.cu_q_lens[it.b];
+            it.qlen = p.cu_q_lens[it.b + 1] - it.qrow0;
+        }
         int n = p.seq_lens[it.b];
-        if (n < 0 || n > p.max_seq_len || n > p.max_blocks * 16) n = 0;
+        if (n < it.qlen || n > p.max_seq_len || n > p.max_blocks * 16 || it.qlen < 1 || it.qlen > p.max_q) n = 0;
         it.n = n;
+        it.col0 = (w % C) * kChunkCols;
+        it.ncols = min(kChunkCols, it.qlen * G - it.col0);
         const int tok0 = it.part * P;
         it.tok1 = min(n, tok0 + P);
+        // query q (position n - qlen + q) sees the tokens below n - qlen + q + 1
+        it.lim_min = min(it.tok1, n - it.qlen + 1 + it.col0 / G);
         it.blk0 = tok0 >> 4;
-        it.nblk = n > 0 ? ((it.tok1 + 15) >> 4) - it.blk0 : 0;
+        it.nblk = (n > 0 && it.ncols > 0) ? ((it.tok1 + 15) >> 4) - it.blk0 : 0;
         it.bt = p.block_tables + static_cast<int64_t>(it.b) * p.max_blocks + it.blk0;
+    };
+    // this lane's Q^T words of column tiles 0..NT-1 of an item
+    auto load_q_mma = [&](const Item& it, uint32_t* dst, int nt_count) {
+        const uint16_t* qbase = static_cast<const uint16_t*>(p.q);
+        for (int nt = 0; nt < nt_count; ++nt) {
+            const int cl = nt * 8 + (lane >> 2);
+            const bool ok = cl < it.ncols;
+            const int c = it.col0 + cl;
+            const int qi = ok ? c / G : 0;
+            const int h = ok ? c - qi * G : 0;
+            const uint16_t* qq =
+                qbase + (static_cast<int64_t>(it.qrow0 + qi) * p.num_q_heads + it.g * G + h) * D;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int d = kk * 16 + 2 * (lane & 3);
+                dst[(kk * nt_count + nt) * 2] = ok ? *reinterpret_cast<const uint32_t*>(qq + d) : 0u;
+                dst[(kk * nt_count + nt) * 2 + 1] = ok ? *reinterpret_cast<const uint32_t*>(qq + d + 8) : 0u;
+            }
+        }
     };
 
     // ---- fetch cursor: claims items, loads their blocks ahead ----------------
@@ -484,42 +572,43 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     bool fvalid = false;
     // this lane's query words of the most recently claimed item, loaded at
     // claim time so that they have arrived when the item's compute starts
+    // (single-tile kernels only: a wider tile's words stay in memory)
+    constexpr bool kPrefetchQ = kMaxNT == 1;
     constexpr int kQWords = kMma ? 2 * (D / 16) : D / 64;
     uint32_t qpre[kQWords];
     int qpre_item = -1;
     auto load_q = [&](const Item& it, uint32_t (&dst)[kQWords]) {
-        const int qrow = p.cu_q_lens ? p.cu_q_lens[it.b] : it.b;
-        const uint16_t* qq = static_cast<const uint16_t*>(p.q) +
-                             (static_cast<int64_t>(qrow) * p.num_q_heads + it.g * G) * D;
         if constexpr (!kMma) {
+            const uint16_t* qq = static_cast<const uint16_t*>(p.q) +
+                                 (static_cast<int64_t>(it.qrow0) * p.num_q_heads + it.g) * D;
 #pragma unroll
             for (int j = 0; j < kQWords; ++j)
                 dst[j] = *reinterpret_cast<const uint32_t*>(qq + lane * AluState<T, D>::DPL + 2 * j);
         } else {
-            const int hh = lane >> 2;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const int d = kk * 16 + 2 * (lane & 3);
-                dst[2 * kk] = hh < G ? *reinterpret_cast<const uint32_t*>(qq + hh * D + d) : 0u;
-                dst[2 * kk + 1] = hh < G ? *reinterpret_cast<const uint32_t*>(qq + hh * D + d + 8) : 0u;
-            }
+            load_q_mma(it, dst, 1);
         }
     };
     auto claim_next = [&]() {
-        int w = 0;
-        if (lane == 0) w = atomicAdd(p.work_counter, 1);
-        w = __shfl_sync(kFull, w, 0);
-        if (w >= total) {
-            fvalid = false;
+        for (;;) {
+            int w = 0;
+            if (lane == 0) w = atomicAdd(p.work_counter, 1);
+            w = __shfl_sync(kFull, w, 0);
+            if (w >= total) {
+                fvalid = false;
+                return;
+            }
+            load_item(w, fi);
+            if (fi.nblk == 0) continue;  // a column chunk past the row's last (query, head) pair
+            if (lane == 0) queue[q_tail % kQueue] = w;
+            ++q_tail;
+            if constexpr (kPrefetchQ) {
+                load_q(fi, qpre);
+                qpre_item = w;
+            }
+            fblk = 0;
+            fvalid = true;
             return;
         }
-        if (lane == 0) queue[q_tail % kQueue] = w;
-        ++q_tail;
-        load_item(w, fi);
-        load_q(fi, qpre);
-        qpre_item = w;
-        fblk = 0;
-        fvalid = fi.nblk > 0;  // every listed unit has at least one block
     };
     uint32_t kf = 0;  // blocks issued so far
     auto issue_next = [&]() {
@@ -543,6 +632,159 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
     // ---- compute: the claimed items in order, their blocks in order ---------
     uint32_t kc = 0;  // blocks consumed so far
+    // Walk the item's blocks through the ring; `step(kt, vt, base, nvalid)`
+    // consumes one landed block.  False when a wait gave up.
+    auto for_each_block = [&](const Item& it, auto&& step) -> bool {
+        for (int blk = 0; blk < it.nblk; ++blk, ++kc) {
+            const int slot = static_cast<int>(kc % kDecodeStages);
+            const bool got = mbar_wait(&ring.bars[slot], (kc / kDecodeStages) & 1u);
+            if (__any_sync(kFull, !got)) return false;
+            const int phys = it.bt[blk];
+            if (phys >= 0 && phys < p.num_blocks) {
+                uint8_t* kt = ring.base + slot * Shape::kStageBytes;
+                uint8_t* vt = kt + Shape::kTileBytes;
+                const int base = (it.blk0 + blk) * 16;
+                step(kt, vt, base, min(16, it.tok1 - base));
+            }
+            // the slot is free again: refill it with the block STAGES ahead
+            fence_proxy_async_smem();
+            __syncwarp();
+            issue_next();
+        }
+        return true;
+    };
+
+    // MHA decode row: fp32 FMA path
+    auto run_alu = [&](const Item& it, const uint32_t (&qw)[kQWords]) -> bool {
+        AluState<T, D, kFp8> alu;
+#pragma unroll
+        for (int j = 0; j < kQWords; ++j) {
+            const float2 f = Elem<T>::to_float2(qw[j]);
+            alu.q[2 * j] = f.x * p.scale_log2;
+            alu.q[2 * j + 1] = f.y * p.scale_log2;
+            alu.acc[2 * j] = 0.f;
+            alu.acc[2 * j + 1] = 0.f;
+        }
+        alu.m = -INFINITY;
+        alu.l = 0.f;
+        if (!for_each_block(it, [&](uint8_t* kt, uint8_t* vt, int, int nvalid) { alu.step(kt, vt, nvalid, lane); }))
+            return false;
+        constexpr int DPL = AluState<T, D>::DPL;
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) alu.acc[j] *= p.v_scale;
+        float lsum = alu.l;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
+        const int hq = it.g;
+        if (it.n <= P) {
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            uint16_t* o = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(it.qrow0) * p.num_q_heads + hq) * D +
+                          lane * DPL;
+            if constexpr (DPL == 4) {
+                uint2 v;
+                v.x = Elem<T>::pack(alu.acc[0] * inv, alu.acc[1] * inv);
+                v.y = Elem<T>::pack(alu.acc[2] * inv, alu.acc[3] * inv);
+                *reinterpret_cast<uint2*>(o) = v;
+            } else {
+                *reinterpret_cast<uint32_t*>(o) = Elem<T>::pack(alu.acc[0] * inv, alu.acc[1] * inv);
+            }
+        } else {
+            const int64_t pi = (static_cast<int64_t>(p.row_base[it.b]) * p.num_q_heads + hq) * p.max_parts + it.part;
+            if (lane == 0) {
+                p.ws_m[pi] = alu.m;
+                p.ws_l[pi] = lsum;
+            }
+#pragma unroll
+            for (int j = 0; j < DPL; ++j) p.ws_acc[pi * D + lane * DPL + j] = alu.acc[j];
+        }
+        return true;
+    };
+
+    // (query, head) columns of a decode or verify row: tensor-core path
+    auto run_mma = [&](auto nt_tag, const Item& it, int w) -> bool {
+        constexpr int NT = decltype(nt_tag)::value;
+        MmaState<T, D, NT> mma;
+        if (kPrefetchQ && NT == 1 && qpre_item == w) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                mma.qb[kk][0][0] = qpre[2 * kk];
+                mma.qb[kk][0][1] = qpre[2 * kk + 1];
+            }
+        } else {
+            load_q_mma(it, &mma.qb[0][0][0], NT);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mma.o[kk][nt][e] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                mma.m[nt][e] = -INFINITY;
+                mma.l[nt][e] = 0.f;
+                const int cl = nt * 8 + 2 * (lane & 3) + e;
+                mma.lim[nt][e] = cl < it.ncols ? min(it.tok1, it.n - it.qlen + 1 + (it.col0 + cl) / G) : 0;
+            }
+        }
+        const bool ok = for_each_block(it, [&](uint8_t* kt, uint8_t* vt, int base, int nvalid) {
+            const bool masked = base + 16 > it.lim_min;
+            if constexpr (kFp8) {
+                uint8_t* ck = ring.base + kDecodeStages * Shape::kStageBytes;
+                uint8_t* cv = ck + 16 * D * 2;
+                convert_fp8_tile<T>(kt, ck, lane);
+                convert_fp8_tile<T>(vt, cv, lane);
+                __syncwarp();
+                mma.step(ck, cv, base, nvalid, masked, lane, p.scale_log2);
+                __syncwarp();  // the next block's conversion overwrites ck / cv
+            } else {
+                mma.step(kt, vt, base, nvalid, masked, lane, p.scale_log2);
+            }
+        });
+        if (!ok) return false;
+        const bool split = it.n > P;
+        const int prow = split ? p.row_base[it.b] : 0;
+        const int dr = lane >> 2;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float lh = mma.l[nt][e];
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) lh += __shfl_xor_sync(kFull, lh, off);
+                const int cl = nt * 8 + 2 * (lane & 3) + e;
+                if (cl >= it.ncols) continue;
+                const int c = it.col0 + cl;
+                const int qi = c / G;
+                const int hq = it.g * G + (c - qi * G);
+                if (!split) {
+                    const float inv = lh > 0.f ? p.v_scale / lh : 0.f;
+                    uint16_t* o = static_cast<uint16_t*>(p.out) +
+                                  (static_cast<int64_t>(it.qrow0 + qi) * p.num_q_heads + hq) * D;
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        o[mt * 16 + dr] = Elem<T>::from_float(mma.o[mt][nt][e] * inv);
+                        o[mt * 16 + dr + 8] = Elem<T>::from_float(mma.o[mt][nt][2 + e] * inv);
+                    }
+                } else {
+                    const int64_t pi =
+                        (static_cast<int64_t>(prow + qi) * p.num_q_heads + hq) * p.max_parts + it.part;
+                    if (dr == 0) {
+                        p.ws_m[pi] = mma.m[nt][e];
+                        p.ws_l[pi] = lh;
+                    }
+                    float* a = p.ws_acc + pi * D;
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        a[mt * 16 + dr] = mma.o[mt][nt][e] * p.v_scale;
+                        a[mt * 16 + dr + 8] = mma.o[mt][nt][2 + e] * p.v_scale;
+                    }
+                }
+            }
+        }
+        return true;
+    };
+
     bool failed = false;
     while (q_head != q_tail) {
         __syncwarp();
@@ -550,144 +792,25 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         ++q_head;
         Item it;
         load_item(w, it);
-        const int qrow = p.cu_q_lens ? p.cu_q_lens[it.b] : it.b;
-        const int nparts = it.n > 0 ? (it.n + P - 1) / P : 1;
-        uint32_t qw[kQWords];
-        if (qpre_item == w) {
-#pragma unroll
-            for (int j = 0; j < kQWords; ++j) qw[j] = qpre[j];
-        } else {
-            load_q(it, qw);  // the fetch cursor has moved past this item already
-        }
-
-        AluState<T, D, kFp8> alu;
-        MmaState<T, D> mma;
+        bool ok;
         if constexpr (!kMma) {
+            uint32_t qw[kQWords];
+            if (qpre_item == w) {
 #pragma unroll
-            for (int j = 0; j < kQWords; ++j) {
-                const float2 f = Elem<T>::to_float2(qw[j]);
-                alu.q[2 * j] = f.x * p.scale_log2;
-                alu.q[2 * j + 1] = f.y * p.scale_log2;
-                alu.acc[2 * j] = 0.f;
-                alu.acc[2 * j + 1] = 0.f;
-            }
-            alu.m = -INFINITY;
-            alu.l = 0.f;
-        } else {
-#pragma unroll
-            for (int kk = 0; kk < MmaState<T, D>::KS; ++kk) {
-                mma.qb[kk][0] = qw[2 * kk];
-                mma.qb[kk][1] = qw[2 * kk + 1];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) mma.o[kk][e] = 0.f;
-            }
-            mma.m[0] = mma.m[1] = -INFINITY;
-            mma.l[0] = mma.l[1] = 0.f;
-        }
-
-        for (int blk = 0; blk < it.nblk; ++blk, ++kc) {
-            const int slot = static_cast<int>(kc % kDecodeStages);
-            const bool got = mbar_wait(&ring.bars[slot], (kc / kDecodeStages) & 1u);
-            if (__any_sync(kFull, !got)) {
-                failed = true;
-                break;
-            }
-            const int phys = it.bt[blk];
-            if (phys >= 0 && phys < p.num_blocks) {
-                uint8_t* kt = ring.base + slot * Shape::kStageBytes;
-                uint8_t* vt = kt + Shape::kTileBytes;
-                const int nvalid = min(16, it.tok1 - (it.blk0 + blk) * 16);
-                if constexpr (!kMma) {
-                    alu.step(kt, vt, nvalid, lane);
-                } else if constexpr (kFp8) {
-                    uint8_t* ck = ring.base + kDecodeStages * Shape::kStageBytes;
-                    uint8_t* cv = ck + 16 * D * 2;
-                    convert_fp8_tile<T>(kt, ck, lane);
-                    convert_fp8_tile<T>(vt, cv, lane);
-                    __syncwarp();
-                    mma.step(ck, cv, nvalid, lane, p.scale_log2);
-                    __syncwarp();  // the next block's conversion overwrites ck / cv
-                } else {
-                    mma.step(kt, vt, nvalid, lane, p.scale_log2);
-                }
-            }
-            // the slot is free again: refill it with the block STAGES ahead
-            fence_proxy_async_smem();
-            __syncwarp();
-            issue_next();
-        }
-        if (failed) break;
-
-        // ---- finalise this item: the output row, or the partition's partials
-        if constexpr (!kMma) {
-            constexpr int DPL = AluState<T, D>::DPL;
-#pragma unroll
-            for (int j = 0; j < DPL; ++j) alu.acc[j] *= p.v_scale;
-            float lsum = alu.l;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
-            const int hq = it.g;
-            if (nparts == 1) {
-                const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-                uint16_t* o = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(qrow) * p.num_q_heads + hq) * D +
-                              lane * DPL;
-                if constexpr (DPL == 4) {
-                    uint2 v;
-                    v.x = Elem<T>::pack(alu.acc[0] * inv, alu.acc[1] * inv);
-                    v.y = Elem<T>::pack(alu.acc[2] * inv, alu.acc[3] * inv);
-                    *reinterpret_cast<uint2*>(o) = v;
-                } else {
-                    *reinterpret_cast<uint32_t*>(o) = Elem<T>::pack(alu.acc[0] * inv, alu.acc[1] * inv);
-                }
+                for (int j = 0; j < kQWords; ++j) qw[j] = qpre[j];
             } else {
-                const int64_t pi = (static_cast<int64_t>(it.b) * p.num_q_heads + hq) * p.max_parts + it.part;
-                if (lane == 0) {
-                    p.ws_m[pi] = alu.m;
-                    p.ws_l[pi] = lsum;
-                }
-#pragma unroll
-                for (int j = 0; j < DPL; ++j) p.ws_acc[pi * D + lane * DPL + j] = alu.acc[j];
+                load_q(it, qw);  // the fetch cursor has moved past this item already
             }
+            ok = run_alu(it, qw);
+        } else if constexpr (kMaxNT == 1) {
+            ok = run_mma(std::integral_constant<int, 1>{}, it, w);
         } else {
-#pragma unroll
-            for (int mt = 0; mt < MmaState<T, D>::KS; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) mma.o[mt][e] *= p.v_scale;
-            float l0 = mma.l[0], l1 = mma.l[1];
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                l0 += __shfl_xor_sync(kFull, l0, off);
-                l1 += __shfl_xor_sync(kFull, l1, off);
-            }
-            const int dr = lane >> 2;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int h = 2 * (lane & 3) + e;
-                if (h >= G) continue;
-                const int hq = it.g * G + h;
-                const float lh = e ? l1 : l0;
-                if (nparts == 1) {
-                    const float inv = lh > 0.f ? 1.f / lh : 0.f;
-                    uint16_t* o = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(qrow) * p.num_q_heads + hq) * D;
-#pragma unroll
-                    for (int mt = 0; mt < MmaState<T, D>::KS; ++mt) {
-                        o[mt * 16 + dr] = Elem<T>::from_float(mma.o[mt][e] * inv);
-                        o[mt * 16 + dr + 8] = Elem<T>::from_float(mma.o[mt][2 + e] * inv);
-                    }
-                } else {
-                    const int64_t pi = (static_cast<int64_t>(it.b) * p.num_q_heads + hq) * p.max_parts + it.part;
-                    if (dr == 0) {
-                        p.ws_m[pi] = mma.m[e];
-                        p.ws_l[pi] = lh;
-                    }
-                    float* a = p.ws_acc + pi * D;
-#pragma unroll
-                    for (int mt = 0; mt < MmaState<T, D>::KS; ++mt) {
-                        a[mt * 16 + dr] = mma.o[mt][e];
-                        a[mt * 16 + dr + 8] = mma.o[mt][2 + e];
-                    }
-                }
-            }
+            ok = it.ncols <= 8 ? run_mma(std::integral_constant<int, 1>{}, it, w)
+                               : run_mma(std::integral_constant<int, 2>{}, it, w);
+        }
+        if (!ok) {
+            failed = true;
+            break;
         }
     }
     if (failed) {
@@ -697,79 +820,79 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     }
 }
 
-// Merge the partitions of each (sequence, q head):
+// Merge the partitions of each (query row, q head):
 // out = sum_p acc_p 2^(m_p - M) / sum_p l_p 2^(m_p - M), M = max_p m_p.
-// The per-partition weights are formed once in shared memory; each thread then
-// streams one head dimension of every partition's accumulator.
+// One CTA per q head walks the listed partials rows.  The per-partition
+// weights are formed once in shared memory; each thread then streams one head
+// dimension of every partition's accumulator.
 constexpr int kReduceMaxParts = 1024;   // partitions staged in shared memory per pass
+constexpr int kReduceMaxRowsPerLaunch = 2048;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(D) decode_reduce_kernel(const DecodeParams p) {
     __shared__ float sc[kReduceMaxParts];
     __shared__ float red[D / 32];
     const int hq = blockIdx.x;
-    const int b = blockIdx.y;
     const int d = threadIdx.x;
-    int qrow = b;
-    if (p.cu_q_lens) {
-        const int r0 = p.cu_q_lens[b];
-        if (p.cu_q_lens[b + 1] - r0 != 1) return;
-        qrow = r0;
-    }
-    int n = p.seq_lens[b];
-    if (n < 0 || n > p.max_seq_len || n > p.max_blocks * 16) n = 0;
     const int P = p.partition_tokens;
-    const int nparts = n > 0 ? (n + P - 1) / P : 1;
-    if (nparts <= 1) return;
-    const int64_t base = (static_cast<int64_t>(b) * p.num_q_heads + hq) * p.max_parts;
-    const float* wm = p.ws_m + base;
-    const float* wl = p.ws_l + base;
-    const float* wa = p.ws_acc + base * D;
+    const int nrows = *p.row_count;
+    for (int k = blockIdx.y; k < nrows; k += gridDim.y) {
+        const uint32_t entry = static_cast<uint32_t>(p.rows[k]);
+        const int b = static_cast<int>(entry >> 3);
+        const int qrow = (p.cu_q_lens ? p.cu_q_lens[b] : b) + static_cast<int>(entry & 7u);
+        int n = p.seq_lens[b];
+        if (n < 0 || n > p.max_seq_len || n > p.max_blocks * 16) n = 0;
+        const int nparts = n > 0 ? (n + P - 1) / P : 1;
+        const int64_t base = (static_cast<int64_t>(k) * p.num_q_heads + hq) * p.max_parts;
+        const float* wm = p.ws_m + base;
+        const float* wl = p.ws_l + base;
+        const float* wa = p.ws_acc + base * D;
 
-    // M = max_p m_p (block reduction)
-    float M = -INFINITY;
-    for (int i = d; i < nparts; i += D) M = fmaxf(M, wm[i]);
+        // M = max_p m_p (block reduction)
+        float M = -INFINITY;
+        for (int i = d; i < nparts; i += D) M = fmaxf(M, wm[i]);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-    if ((d & 31) == 0) red[d >> 5] = M;
-    __syncthreads();
-    M = red[0];
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+        if ((d & 31) == 0) red[d >> 5] = M;
+        __syncthreads();
+        M = red[0];
 #pragma unroll
-    for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
-    __syncthreads();
+        for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
+        __syncthreads();
 
-    float L = 0.f, A = 0.f;
-    if (M != -INFINITY) {
-        for (int p0 = 0; p0 < nparts; p0 += kReduceMaxParts) {
-            const int np = min(kReduceMaxParts, nparts - p0);
-            float lpart = 0.f;
-            for (int i = d; i < np; i += D) {
-                const float s = fast_exp2(wm[p0 + i] - M);
-                sc[i] = s;
-                lpart = fmaf(wl[p0 + i], s, lpart);
+        float L = 0.f, A = 0.f;
+        if (M != -INFINITY) {
+            for (int p0 = 0; p0 < nparts; p0 += kReduceMaxParts) {
+                const int np = min(kReduceMaxParts, nparts - p0);
+                float lpart = 0.f;
+                for (int i = d; i < np; i += D) {
+                    const float s = fast_exp2(wm[p0 + i] - M);
+                    sc[i] = s;
+                    lpart = fmaf(wl[p0 + i], s, lpart);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) lpart += __shfl_xor_sync(kFull, lpart, off);
+                if ((d & 31) == 0) red[d >> 5] = lpart;
+                __syncthreads();
+#pragma unroll
+                for (int w = 0; w < D / 32; ++w) L += red[w];
+                const float* a = wa + static_cast<int64_t>(p0) * D + d;
+                int i = 0;
+                for (; i + 8 <= np; i += 8) {
+                    float x[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) x[u] = a[static_cast<int64_t>(i + u) * D];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) A = fmaf(x[u], sc[i + u], A);
+                }
+                for (; i < np; ++i) A = fmaf(a[static_cast<int64_t>(i) * D], sc[i], A);
+                __syncthreads();
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) lpart += __shfl_xor_sync(kFull, lpart, off);
-            if ((d & 31) == 0) red[d >> 5] = lpart;
-            __syncthreads();
-#pragma unroll
-            for (int w = 0; w < D / 32; ++w) L += red[w];
-            const float* a = wa + static_cast<int64_t>(p0) * D + d;
-            int i = 0;
-            for (; i + 8 <= np; i += 8) {
-                float x[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) x[u] = a[static_cast<int64_t>(i + u) * D];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) A = fmaf(x[u], sc[i + u], A);
-            }
-            for (; i < np; ++i) A = fmaf(a[static_cast<int64_t>(i) * D], sc[i], A);
-            __syncthreads();
         }
+        const float v = L > 0.f ? A / L : 0.f;
+        reinterpret_cast<uint16_t*>(p.out)[(static_cast<int64_t>(qrow) * p.num_q_heads + hq) * D + d] =
+            Elem<T>::from_float(v);
     }
-    const float v = L > 0.f ? A / L : 0.f;
-    reinterpret_cast<uint16_t*>(p.out)[(static_cast<int64_t>(qrow) * p.num_q_heads + hq) * D + d] =
-        Elem<T>::from_float(v);
 }
 
 int sm_count() {
@@ -784,11 +907,11 @@ int sm_count() {
     return count[dev];
 }
 
-template <typename T, int D, bool kMma, bool kFp8 = false>
+template <typename T, int D, bool kMma, bool kFp8 = false, int kMaxNT = 1>
 cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t s) {
     constexpr int smem = DecodeShape<D, kFp8, kMma>::kSmemBytes;
-    auto kern = decode_kernel<T, D, kMma, kFp8>;
+    auto kern = decode_kernel<T, D, kMma, kFp8, kMaxNT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, s, p);
@@ -796,14 +919,15 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, cons
     // persistent: as many CTAs as fit on every SM (shared memory bound), fewer
     // when there cannot be that many items
     constexpr int kCtasPerSm = (228 * 1024) / (smem + 2048);
-    const long long max_items = static_cast<long long>(p.num_seqs) * p.max_parts * p.num_kv_heads;
+    const long long max_items =
+        static_cast<long long>(p.num_seqs) * p.max_parts * p.num_kv_heads * p.col_chunks;
     const long long want = (max_items + kDecodeWarps - 1) / kDecodeWarps;
     const int grid = static_cast<int>(
         std::max<long long>(1, std::min<long long>(want, static_cast<long long>(kCtasPerSm) * sm_count())));
     e = launch_pdl(kern, dim3(grid), dim3(kDecodeWarps * 32), smem, s, p, kmap, vmap);
     if (e != cudaSuccess) return e;
     if (p.max_parts > 1) {
-        dim3 rgrid(p.num_q_heads, p.num_seqs);
+        dim3 rgrid(p.num_q_heads, std::min(p.max_rows, kReduceMaxRowsPerLaunch));
         decode_reduce_kernel<T, D><<<rgrid, D, 0, s>>>(p);
         e = cudaGetLastError();
     }
@@ -823,22 +947,22 @@ cudaError_t launch_decode_fp8(const DecodeParams& p, const CUtensorMap& kmap, co
                : launch_decode_t<__nv_bfloat16, 128, false, true>(p, kmap, vmap, s);
 }
 
+template <typename T, int D>
+cudaError_t launch_decode_d(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                            cudaStream_t s) {
+    if (p.max_q * p.group > 8) return launch_decode_t<T, D, true, false, 2>(p, kmap, vmap, s);
+    if (p.group > 1 || p.max_q > 1) return launch_decode_t<T, D, true, false, 1>(p, kmap, vmap, s);
+    return launch_decode_t<T, D, false, false, 1>(p, kmap, vmap, s);
+}
+
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           int head_dim, int dtype, cudaStream_t s) {
     if (p.num_seqs == 0) return cudaSuccess;
-    const bool mma = p.group > 1;
-    if (dtype == 0) {
-        if (head_dim == 128)
-            return mma ? launch_decode_t<__half, 128, true>(p, kmap, vmap, s)
-                       : launch_decode_t<__half, 128, false>(p, kmap, vmap, s);
-        return mma ? launch_decode_t<__half, 64, true>(p, kmap, vmap, s)
-                   : launch_decode_t<__half, 64, false>(p, kmap, vmap, s);
-    }
-    if (head_dim == 128)
-        return mma ? launch_decode_t<__nv_bfloat16, 128, true>(p, kmap, vmap, s)
-                   : launch_decode_t<__nv_bfloat16, 128, false>(p, kmap, vmap, s);
-    return mma ? launch_decode_t<__nv_bfloat16, 64, true>(p, kmap, vmap, s)
-               : launch_decode_t<__nv_bfloat16, 64, false>(p, kmap, vmap, s);
+    if (dtype == 0)
+        return head_dim == 128 ? launch_decode_d<__half, 128>(p, kmap, vmap, s)
+                               : launch_decode_d<__half, 64>(p, kmap, vmap, s);
+    return head_dim == 128 ? launch_decode_d<__nv_bfloat16, 128>(p, kmap, vmap, s)
+                           : launch_decode_d<__nv_bfloat16, 64>(p, kmap, vmap, s);
 }
 
 }  // namespace pa

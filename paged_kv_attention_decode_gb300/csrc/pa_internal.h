@@ -33,18 +33,26 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// Rows of a varlen call whose chunk has 1..PA_VERIFY_MAX_Q_ queries (decode
+// rows, speculative-verify rows) run in the decode kernel; longer chunks run
+// in the prefill kernels.
+#define PA_VERIFY_MAX_Q_ 8
+
 struct DecodeParams {
-    void* out;                    // [rows, Hq, D]
-    const void* q;                // [rows, Hq, D]
+    void* out;                    // [T, Hq, D] (T = B without cu_q_lens)
+    const void* q;                // [T, Hq, D]
     const int32_t* block_tables;  // [B, max_blocks]
     const int32_t* seq_lens;      // [B]
-    const int32_t* cu_q_lens;     // [B+1] or nullptr (row b = sequence b)
-    float* ws_m;                  // [B, Hq, max_parts] running max (log2 units)
-    float* ws_l;                  // [B, Hq, max_parts] running sum
-    float* ws_acc;                // [B, Hq, max_parts, D] unnormalised accumulator
+    const int32_t* cu_q_lens;     // [B+1] or nullptr (row b = sequence b, one query each)
+    float* ws_m;                  // [max_rows, Hq, max_parts] running max (log2 units)
+    float* ws_l;                  // [max_rows, Hq, max_parts] running sum
+    float* ws_acc;                // [max_rows, Hq, max_parts, D] unnormalised accumulator
     int32_t* units;               // [B * max_parts] (sequence << 16 | partition) work list
     int32_t* unit_count;          // number of entries in `units`
     int32_t* work_counter;        // next work item to claim (reset by the plan kernel)
+    int32_t* row_base;            // [B] first partials row of a split sequence
+    int32_t* rows;                // [max_rows] (sequence << 3 | query index) of every partials row
+    int32_t* row_count;           // number of entries in `rows`
     unsigned int* err;            // device error word
     int num_seqs;
     int max_blocks;
@@ -56,6 +64,9 @@ struct DecodeParams {
     int group;                    // num_q_heads / num_kv_heads
     int partition_tokens;         // multiple of 16
     int max_parts;                // ceil(max_seq_len / partition_tokens)
+    int max_q;                    // largest chunk handled here (1..PA_VERIFY_MAX_Q_)
+    int max_rows;                 // partials rows available in the workspace
+    int col_chunks;               // 32-column chunks of (query, head) pairs per (unit, kv head)
     float scale_log2;             // scale * log2(e) (times the K dequantisation scale for FP8)
     float v_scale;                // V dequantisation scale (1 for 16-bit caches)
 };

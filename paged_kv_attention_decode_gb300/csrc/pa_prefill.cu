@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kPreThreads, 2)
 
     const int row0 = p.cu_q_lens[b];
     const int qlen = p.cu_q_lens[b + 1] - row0;
-    if (qlen <= 1) return;                 // decode rows run in the decode kernel
+    if (qlen <= PA_VERIFY_MAX_Q_) return;  // decode and verify rows run in the decode kernel
     const int q0 = qt * QT;
     if (q0 >= qlen) return;
     const int n = p.seq_lens[b];
@@ -363,7 +363,7 @@ cudaError_t launch_prefill_t(const PrefillParams& p, const CUtensorMap& kmap, co
 
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            int head_dim, int dtype, int max_q_len, cudaStream_t s) {
-    if (p.num_seqs == 0 || max_q_len <= 1) return cudaSuccess;
+    if (p.num_seqs == 0 || max_q_len <= PA_VERIFY_MAX_Q_) return cudaSuccess;
     if (dtype == 0)
         return head_dim == 128 ? launch_prefill_t<__half, 128>(p, kmap, vmap, max_q_len, s)
                                : launch_prefill_t<__half, 64>(p, kmap, vmap, max_q_len, s);

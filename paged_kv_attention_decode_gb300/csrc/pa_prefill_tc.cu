@@ -61,8 +61,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 }
 
 // Work list of the chunked-prefill tiles: offsets[b] = number of 128-row tiles
-// of sequences 0..b-1 whose chunk is longer than one token (single-token rows
-// are decodes and belong to the decode kernel); offsets[B] = total.  One CTA.
+// of sequences 0..b-1 whose chunk is longer than PA_VERIFY_MAX_Q_ tokens
+// (shorter chunks are decode or speculative-verify rows and belong to the
+// decode kernel); offsets[B] = total.  One CTA.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __restrict__ cu_q_lens, int num_seqs,
                                                             int q_per_tile, int32_t* __restrict__ offsets) {
     __shared__ int warp_tot[32];
@@ -77,7 +78,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
         int v = 0;
         if (b < num_seqs) {
             const int ql = cu_q_lens[b + 1] - cu_q_lens[b];
-            v = ql > 1 ? (ql + q_per_tile - 1) / q_per_tile : 0;
+            v = ql > PA_VERIFY_MAX_Q_ ? (ql + q_per_tile - 1) / q_per_tile : 0;
         }
         int incl = v;
 #pragma unroll
@@ -504,8 +505,8 @@ cudaError_t launch_t(const PrefillParams& p, int32_t* plan, const CUtensorMap& k
     prefill_plan_kernel<<<1, 1024, 0, s>>>(p.cu_q_lens, p.num_seqs, p.q_per_tile, plan);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // upper bound on the work items: each chunk of length >= 2 has at most
-    // ceil(len / q_per_tile) <= len / 2 tiles, and there are at most max_q_len
+    // upper bound on the work items: each listed chunk (length > 8) has at
+    // most ceil(len / q_per_tile) <= len / 2 tiles, and there are at most max_q_len
     // tokens per chunk
     const long long bound_tiles = std::min<long long>(static_cast<long long>(num_tokens) / 2 + 1,
                                                       static_cast<long long>(p.num_seqs) *
@@ -521,7 +522,7 @@ cudaError_t launch_t(const PrefillParams& p, int32_t* plan, const CUtensorMap& k
 cudaError_t launch_prefill_tc(const PrefillParams& p, int32_t* plan, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, const CUtensorMap& qmap, int head_dim, int dtype,
                               int max_q_len, int num_tokens, cudaStream_t s) {
-    if (p.num_seqs == 0 || max_q_len <= 1) return cudaSuccess;
+    if (p.num_seqs == 0 || max_q_len <= PA_VERIFY_MAX_Q_) return cudaSuccess;
     if (dtype == 0)
         return head_dim == 128 ? launch_t<__half, 128, 2>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s)
                                : launch_t<__half, 64, 2>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s);

@@ -28,6 +28,9 @@ Shapes and distributions of the five named workloads:
                       prefixes U[0,4096] + 2048 decodes at ctx U[256,4096];
                       32/8 heads, bf16; prefill sequences placed at seeded
                       random batch positions.
+* ``spec_verify``     B=64 speculative-decoding verify rows: the last accepted
+                      token + 3 drafts (q_len 4) on cached contexts
+                      U[512,4096]; 32/8 heads, bf16.
 
 q, k and v are N(0,1) in fp32 rounded to the storage dtype.  Seeds are
 ``20261202 + config index``.
@@ -301,7 +304,7 @@ def build_workload(
 # ---------------------------------------------------------------------------
 
 CONFIG_NAMES = ("tiny", "llama7b_decode", "gqa_prefix", "long_context", "mixed", "llama7b_ctx4096",
-                "llama7b_decode_fp8")
+                "llama7b_decode_fp8", "spec_verify")
 
 
 def _seed(idx: int) -> int:
@@ -416,6 +419,19 @@ def config_llama7b_decode_fp8(device="cpu", batch=64, lo=512, hi=4096, **kw) -> 
                           device=device, cache_dtype="fp8", **kw)
 
 
+def config_spec_verify(device="cpu", batch=64, drafts=3, lo=512, hi=4096, **kw) -> Workload:
+    """Speculative-decoding verify step: each sequence appends its last
+    accepted token and `drafts` draft tokens (q_len = drafts + 1) onto a cached
+    context of U[lo, hi] tokens; 32/8 heads, bf16."""
+    seed = _seed(6)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx = rng.integers(lo, hi + 1, size=batch).astype(np.int32)
+    q = drafts + 1
+    return build_workload(name="spec_verify", seq_lens=ctx + q, q_lens=q, num_q_heads=32,
+                          num_kv_heads=8, head_dim=128, dtype="bf16", seed=seed + 1000,
+                          device=device, **kw)
+
+
 CONFIGS = {
     "tiny": config_tiny,
     "llama7b_decode": config_llama7b_decode,
@@ -424,6 +440,7 @@ CONFIGS = {
     "mixed": config_mixed,
     "llama7b_ctx4096": config_llama7b_ctx4096,
     "llama7b_decode_fp8": config_llama7b_decode_fp8,
+    "spec_verify": config_spec_verify,
 }
 
 

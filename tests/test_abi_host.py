@@ -54,18 +54,31 @@ def _align(x):
     return (x + 255) // 256 * 256
 
 
+def _partials(rows, heads, parts, dim=128):
+    n = rows * heads * parts
+    return 2 * _align(n * 4) + _align(n * dim * 4)
+
+
 def test_workspace_sizes(lib):
-    # [unit count: 256 B][work list: B x partitions int32][partials when partitions > 1]
+    # [header 256 B][work list: B x partitions int32]
+    # + when partitions > 1: [row_base: B int32][rows: R int32][partials of R rows]
     assert pa.decode_workspace_bytes(64, 32, 128, 512, 512) == 256 + _align(64 * 4)
-    n = 64 * 32 * 8
-    assert pa.decode_workspace_bytes(64, 32, 128, 4096, 512) == (256 + _align(64 * 8 * 4) + 2 * _align(n * 4)
-                                                                 + _align(n * 128 * 4))
-    n = 8 * 64 * 256
-    assert pa.decode_workspace_bytes(8, 64, 128, 131072, 0) == (256 + _align(8 * 256 * 4) + 2 * _align(n * 4)
-                                                                + _align(n * 128 * 4))
-    assert pa.prefill_workspace_bytes(8, 64, 128, 131072) == _align(9 * 4) + pa.decode_workspace_bytes(8, 64, 128, 131072, 0)
-    assert pa.prefill_workspace_bytes(2052, 32, 128, 300) == _align(2053 * 4) + 256 + _align(2052 * 4)
-    assert pa.prefill_workspace_bytes(0, 32, 128, 300) == 0
+    assert pa.decode_workspace_bytes(64, 32, 128, 4096, 512) == (256 + _align(64 * 8 * 4) + _align(64 * 4)
+                                                                 + _align(64 * 4) + _partials(64, 32, 8))
+    assert pa.decode_workspace_bytes(8, 64, 128, 131072, 0) == (256 + _align(8 * 256 * 4) + 2 * _align(8 * 4)
+                                                                + _partials(8, 64, 256))
+    # prefill: partials rows = min(num_tokens, 8 * num_seqs) (decode and verify chunks)
+    assert pa.prefill_workspace_bytes(8, 8, 64, 128, 131072) == (_align(9 * 4)
+                                                                 + pa.decode_workspace_bytes(8, 64, 128, 131072, 0))
+    assert pa.prefill_workspace_bytes(8, 6000, 64, 128, 131072) == (_align(9 * 4) + 256 + _align(8 * 256 * 4)
+                                                                    + _align(8 * 4) + _align(64 * 4)
+                                                                    + _partials(64, 64, 256))
+    assert pa.prefill_workspace_bytes(4, 12, 32, 128, 1024) == (_align(5 * 4) + 256 + _align(4 * 2 * 4)
+                                                                + _align(4 * 4) + _align(12 * 4)
+                                                                + _partials(12, 32, 2))
+    assert pa.prefill_workspace_bytes(2052, 8192, 32, 128, 300) == _align(2053 * 4) + 256 + _align(2052 * 4)
+    assert pa.prefill_workspace_bytes(0, 0, 32, 128, 300) == 0
+    assert pa.prefill_workspace_bytes(4, -1, 32, 128, 300) == 0
     assert pa.decode_workspace_bytes(0, 32, 128, 300, 0) == 0
 
 

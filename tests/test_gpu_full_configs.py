@@ -65,3 +65,18 @@ def test_full_mixed_step():
     assert pa.device_error() == 0
     del w
     torch.cuda.empty_cache()
+
+
+def test_full_spec_verify():
+    # 64 verify rows of 4 queries (3 drafts) on contexts up to 4K: every row
+    w = W.make("spec_verify", device=DEV)
+    seqs = np.arange(w.batch)
+    snap = snapshot(w, seqs)
+    slots, out = gpu_step(w)
+    _check_cache(w, slots)
+    rows, ref = oracle_rows(w, seqs, snap)
+    err = max_err(out[torch.from_numpy(rows).to(DEV)], ref)
+    assert err <= TOL[w.dtype], err
+    assert pa.device_error() == 0
+    del w
+    torch.cuda.empty_cache()
