@@ -144,6 +144,19 @@ int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, con
                               int head_dim, int block_size, int partition_size, void* workspace,
                               size_t workspace_bytes, int dtype, void* stream);
 
+/*
+ * Copy whole blocks of both pools, the copy-on-write step of a shared block
+ * ("vLLM-Ascend 原理", section 2.1: sequences that share a prefix point at
+ * the same physical blocks and copy before they diverge).  For each i,
+ * block pairs[2i+1] of k_cache and v_cache receives the bytes of block
+ * pairs[2i].  pairs is a device int32 array [num_pairs, 2]; no destination may
+ * also be a source in the same call.  A block is 16 * num_kv_heads * head_dim
+ * elements of elem_bytes bytes (2 for fp16/bf16, 1 for an FP8 cache).  Ids
+ * outside [0, num_blocks) skip the pair and set PA_DEVERR_BLOCK_ID.
+ */
+int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs, int num_blocks,
+                   int num_kv_heads, int head_dim, int elem_bytes, void* stream);
+
 /* Workspace for pa_paged_attention_prefill over num_seqs sequences and
  * num_tokens query rows: the chunk tile work list (num_seqs + 1 int32), the
  * decode kernel's work list, and the split-context partials of up to

@@ -7,6 +7,7 @@ fails loudly if the library has not been built.
 """
 from ._binding import (  # noqa: F401
     PagedAttnError,
+    copy_blocks,
     decode_workspace_bytes,
     library_path,
     load_library,
@@ -19,3 +20,4 @@ from ._binding import (  # noqa: F401
     slot_mapping,
     device_error,
 )
+from .block_manager import BlockManager, BlockManagerError  # noqa: F401,E402

@@ -44,6 +44,7 @@ _SIGNATURES = {
     "pa_paged_kv_write_fp8": (_i32, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _p]),
     "pa_paged_attention_decode_fp8": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _f32, _f32, _f32,
                                              _i32, _i32, _i32, _i32, _i32, _p, _sz, _i32, _p]),
+    "pa_copy_blocks": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _p]),
 }
 
 
@@ -216,6 +217,18 @@ def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
         NB, float(scale), Hq, Hkv, D, bs, _ptr(workspace), ws_bytes, _dt(q), _stream(stream))
     _check(rc, "pa_paged_attention_prefill")
     return out
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, pairs: torch.Tensor, stream=None) -> None:
+    """In place: block pairs[i, 1] of both pools receives block pairs[i, 0]
+    (the copy-on-write step; pairs is a device int32 [n, 2] tensor)."""
+    _cuda(k_cache, v_cache, pairs)
+    _need(pairs.dtype == torch.int32 and pairs.dim() == 2 and pairs.shape[1] == 2, "pairs: int32 [n, 2]")
+    _need(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype, "cache shape/dtype")
+    NB, bs, H, D = k_cache.shape
+    rc = load_library().pa_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), pairs.data_ptr(), pairs.shape[0],
+                                       NB, H, D, k_cache.element_size(), _stream(stream))
+    _check(rc, "pa_copy_blocks")
 
 
 def device_error(clear: bool = True, stream=None) -> int:

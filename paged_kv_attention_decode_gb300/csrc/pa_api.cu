@@ -265,7 +265,8 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
     p.max_rows = max_rows;
     // (query, head) columns per work item: 8, or 16 once a row can have more
     const int cols = max_q * p.group;
-    p.col_chunks = cols > 8 ? (cols + 15) / 16 : 1;
+    const int chunk = (PA_VERIFY_MAX_NT > 1 && cols > 8) ? 16 : 8;
+    p.col_chunks = (cols + chunk - 1) / chunk;
     p.scale_log2 = scale_log2(scale) * k_scale;
     p.v_scale = v_scale;
     carve_workspace(p, workspace);
@@ -409,6 +410,22 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
         p.q_per_tile = 64 / p.group;
         e = pa::launch_prefill(p, kmap, vmap, head_dim, dtype, max_q_len, s);
     }
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs, int num_blocks,
+                   int num_kv_heads, int head_dim, int elem_bytes, void* stream) {
+    if (num_pairs < 0 || num_blocks <= 0 || num_blocks > kMaxPoolBlocks || num_kv_heads <= 0 || head_dim <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (elem_bytes != 1 && elem_bytes != 2) return PA_ERR_UNSUPPORTED;
+    const int64_t block_bytes = static_cast<int64_t>(PA_BLOCK_SIZE) * num_kv_heads * head_dim * elem_bytes;
+    if (block_bytes % 16) return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PA_OK;
+    if (!k_cache || !v_cache || !pairs || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+    unsigned int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_blocks, block_bytes, err,
+                                           static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -6,6 +6,8 @@
 // token's slot is physical block * block_size + offset.  "vLLM-Ascend 原理"
 // section 2.3 ("KV 写缓存") and 2.4 ("KV 追加写"): each new token's k and v are
 // stored into that slot of the separate K and V pools.
+#include <algorithm>
+
 #include "pa_device.cuh"
 
 namespace pa {
@@ -180,6 +182,45 @@ cudaError_t launch_kv_write(const void* key, const void* value, void* k_cache, v
         kv_write_kernel<64><<<static_cast<int>(blocks), threads, 0, s>>>(
             static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
             static_cast<uint4*>(v_cache), slots, num_tokens, num_kv_heads, num_slots, err);
+    return cudaGetLastError();
+}
+
+// Copy whole blocks of both pools: the copy-on-write step of the block
+// manager ("vLLM-Ascend 原理", section 2.1).  pairs[2i] -> pairs[2i+1].
+// One CTA row per pair; its threads stride the block's 16-byte chunks of K
+// and then of V.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                                          const int32_t* __restrict__ pairs, int num_pairs,
+                                                          int num_blocks, int64_t chunks_per_block,
+                                                          unsigned int* err) {
+    pdl_trigger();
+    for (int i = blockIdx.y; i < num_pairs; i += gridDim.y) {
+        const int src = pairs[2 * i];
+        const int dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            if (blockIdx.x == 0 && threadIdx.x == 0) record_error(err, PA_DEVERR_BLOCK_ID_);
+            continue;
+        }
+        if (src == dst) continue;
+        const int64_t s0 = static_cast<int64_t>(src) * chunks_per_block;
+        const int64_t d0 = static_cast<int64_t>(dst) * chunks_per_block;
+        for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks_per_block;
+             c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+            k_cache[d0 + c] = k_cache[s0 + c];
+            v_cache[d0 + c] = v_cache[s0 + c];
+        }
+    }
+}
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs, int num_blocks,
+                               int64_t block_bytes, unsigned int* err, cudaStream_t s) {
+    if (num_pairs == 0) return cudaSuccess;
+    const int64_t chunks = block_bytes / 16;
+    const int threads = 256;
+    const int gx = static_cast<int>(std::min<int64_t>((chunks + threads - 1) / threads, 8));
+    const int gy = std::min(num_pairs, 65535);
+    copy_blocks_kernel<<<dim3(gx, gy), threads, 0, s>>>(static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                                                         pairs, num_pairs, num_blocks, chunks, err);
     return cudaGetLastError();
 }
 

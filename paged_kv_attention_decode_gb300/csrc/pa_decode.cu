@@ -36,6 +36,9 @@ namespace {
 
 constexpr int kDecodeWarps = 4;
 constexpr unsigned kFull = 0xffffffffu;
+// The tensor-core path keeps a column's reference max until a score exceeds
+// it by this much (log2 units), so softmax weights stay within [0, 2^8].
+constexpr float kLazyRescaleLog2 = 8.f;
 
 // Per-warp shared memory: a ring of kStages (K tile, V tile) slots, plus, for
 // the FP8 GQA path, one K and one V tile converted to 16-bit for the MMA.
@@ -46,7 +49,9 @@ template <int D, bool kFp8, bool kMma>
 struct DecodeShape {
     static constexpr int kTileBytes = 16 * D * (kFp8 ? 1 : 2);  // one (block, kv head) tile
     static constexpr int kStageBytes = 2 * kTileBytes;          // K tile + V tile
-    static constexpr int kStages = kFp8 ? (kMma ? 4 : 2) : 3;
+    // The tensor-core kernels are bound by instruction latency per warp, so
+    // they trade ring depth for resident warps (3 CTAs per SM at 2 stages).
+    static constexpr int kStages = kFp8 ? (kMma ? 4 : 2) : (kMma ? PA_MMA_STAGES : 3);
     static constexpr int kConvBytes = (kFp8 && kMma) ? 2 * 16 * D * 2 : 0;
     static constexpr int kWarpBytes = kStages * kStageBytes + kConvBytes;
     static constexpr int kSmemBytes = kDecodeWarps * kWarpBytes + 1024;  // + alignment slack
@@ -264,42 +269,59 @@ struct MmaState {
             }
         }
         const int r0 = lane >> 2;
-        uint32_t b0[NT], b1[NT];
+        float s[NT][4];
+        bool grow = false;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            float s[4];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const bool v0 = !masked || base + r0 < lim[nt][e];
                 const bool v8 = !masked || base + r0 + 8 < lim[nt][e];
-                s[e] = v0 ? c[nt][e] * scale_log2 : -INFINITY;
-                s[2 + e] = v8 ? c[nt][2 + e] * scale_log2 : -INFINITY;
+                s[nt][e] = v0 ? c[nt][e] * scale_log2 : -INFINITY;
+                s[nt][2 + e] = v8 ? c[nt][2 + e] * scale_log2 : -INFINITY;
             }
-            float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+            float mx0 = fmaxf(s[nt][0], s[nt][2]), mx1 = fmaxf(s[nt][1], s[nt][3]);
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
             }
-            const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-            // a column that has seen no visible token yet keeps m = -inf; its
-            // weights are then exp2(-inf - 0) = 0, never exp2(-inf + inf)
-            const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-            const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float al0 = fast_exp2(m[nt][0] - mu0), al1 = fast_exp2(m[nt][1] - mu1);
-            m[nt][0] = mn0;
-            m[nt][1] = mn1;
-            const float p0 = fast_exp2(s[0] - mu0), p1 = fast_exp2(s[1] - mu1);
-            const float p2 = fast_exp2(s[2] - mu0), p3 = fast_exp2(s[3] - mu1);
-            l[nt][0] = l[nt][0] * al0 + p0 + p2;
-            l[nt][1] = l[nt][1] * al1 + p1 + p3;
+            c[nt][0] = mx0;   // the block maxima, kept for the rescale below
+            c[nt][1] = mx1;
+            // lazy rescale: a column's reference max m moves only when a score
+            // exceeds it by more than kLazyRescaleLog2 (weights stay <= 2^8)
+            grow |= mx0 > m[nt][0] + kLazyRescaleLog2 || mx1 > m[nt][1] + kLazyRescaleLog2;
+        }
+        if (__any_sync(kFull, grow)) {
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                o[mt][nt][0] *= al0;
-                o[mt][nt][1] *= al1;
-                o[mt][nt][2] *= al0;
-                o[mt][nt][3] *= al1;
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float mx = c[nt][e];
+                    if (!(mx > m[nt][e] + kLazyRescaleLog2)) continue;
+                    // a column that saw no token yet has m = -inf: al = 0
+                    const float al = fast_exp2(m[nt][e] - mx);
+                    m[nt][e] = mx;
+                    l[nt][e] *= al;
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        o[mt][nt][e] *= al;
+                        o[mt][nt][2 + e] *= al;
+                    }
+                }
             }
+        }
+        uint32_t b0[NT], b1[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            // a column that has seen no visible token keeps m = -inf; its
+            // weights are then exp2(-inf - 0) = 0, never exp2(-inf + inf)
+            const float mu0 = m[nt][0] == -INFINITY ? 0.f : m[nt][0];
+            const float mu1 = m[nt][1] == -INFINITY ? 0.f : m[nt][1];
+            const float p0 = fast_exp2(s[nt][0] - mu0), p1 = fast_exp2(s[nt][1] - mu1);
+            const float p2 = fast_exp2(s[nt][2] - mu0), p3 = fast_exp2(s[nt][3] - mu1);
+            l[nt][0] += p0 + p2;
+            l[nt][1] += p1 + p3;
             // P^T as the B operand: lane l needs P[token 2*(l%4)+e (+8)][column l/4].
             const uint32_t lo = Elem<T>::pack(p0, p1);
             const uint32_t hi = Elem<T>::pack(p2, p3);
@@ -482,7 +504,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
 // the warp's HBM pipeline never drains between items.  Warps never wait for
 // one another.
 template <typename T, int D, bool kMma, bool kFp8, int kMaxNT>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
+__global__ void __launch_bounds__(kDecodeWarps * 32, (kMma && !kFp8) ? PA_MMA_MIN_CTAS : 1)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap) {
     static_assert(kMma || kMaxNT == 1, "the FMA path handles one query per row");
@@ -950,7 +972,7 @@ cudaError_t launch_decode_fp8(const DecodeParams& p, const CUtensorMap& kmap, co
 template <typename T, int D>
 cudaError_t launch_decode_d(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t s) {
-    if (p.max_q * p.group > 8) return launch_decode_t<T, D, true, false, 2>(p, kmap, vmap, s);
+    if (PA_VERIFY_MAX_NT > 1 && p.max_q * p.group > 8) return launch_decode_t<T, D, true, false, 2>(p, kmap, vmap, s);
     if (p.group > 1 || p.max_q > 1) return launch_decode_t<T, D, true, false, 1>(p, kmap, vmap, s);
     return launch_decode_t<T, D, false, false, 1>(p, kmap, vmap, s);
 }

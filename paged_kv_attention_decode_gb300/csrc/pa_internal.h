@@ -38,6 +38,19 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 // in the prefill kernels.
 #define PA_VERIFY_MAX_Q_ 8
 
+// Tuning of the tensor-core decode kernel (decode rows with group > 1,
+// verify rows): ring depth, resident CTAs per SM it is compiled for, and the
+// most 8-column tiles one work item takes (1: 8 columns, 2: 16 columns).
+#ifndef PA_MMA_STAGES
+#define PA_MMA_STAGES 2
+#endif
+#ifndef PA_MMA_MIN_CTAS
+#define PA_MMA_MIN_CTAS 3
+#endif
+#ifndef PA_VERIFY_MAX_NT
+#define PA_VERIFY_MAX_NT 2
+#endif
+
 struct DecodeParams {
     void* out;                    // [T, Hq, D] (T = B without cu_q_lens)
     const void* q;                // [T, Hq, D]
@@ -105,6 +118,9 @@ cudaError_t launch_kv_write_fp8(const void* key, const void* value, void* k_cach
                                 const int64_t* slots, int num_tokens, int num_blocks, int num_kv_heads,
                                 int src_dtype, float k_inv_scale, float v_inv_scale, unsigned int* err,
                                 cudaStream_t s);
+// pairs: device int32 [num_pairs, 2] (source block, destination block).
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs, int num_blocks,
+                               int64_t block_bytes, unsigned int* err, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            int head_dim, int dtype, int max_q_len, cudaStream_t s);
 // tcgen05 prefill: groups of 1, 2, 4 or 8 q heads per kv head; q_per_tile = 128 / group.

@@ -13,7 +13,8 @@ import paged_kv_attention_decode_gb300 as pa
 from paged_kv_attention_decode_gb300 import _binding
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -25,15 +26,18 @@ def lib():
 
 
 def header_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_path(lib):
     names = header_functions()
     for want in ("pa_slot_mapping", "pa_paged_kv_write", "pa_paged_attention_decode",
-                 "pa_paged_attention_prefill", "pa_decode_workspace_bytes", "pa_get_device_error"):
+                 "pa_paged_attention_prefill", "pa_decode_workspace_bytes", "pa_get_device_error",
+                 "pa_copy_blocks", "pa_bm_create", "pa_bm_allocate_slots", "pa_bm_build_step"):
         assert want in names
 
 
@@ -135,3 +139,13 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_binding, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(_binding.PagedAttnError):
         _binding.load_library()
+
+
+def test_copy_blocks_rejects_bad_arguments_on_the_host(lib):
+    f = lib.pa_copy_blocks
+    assert f(FAKE, FAKE, FAKE, -1, 8, 8, 128, 2, None) == 1         # negative pair count
+    assert f(FAKE, FAKE, FAKE, 1, 0, 8, 128, 2, None) == 1          # empty pool
+    assert f(FAKE, FAKE, FAKE, 1, 8, 8, 128, 4, None) == 2          # 4-byte elements
+    assert f(FAKE, FAKE, None, 1, 8, 8, 128, 2, None) == 1          # no pair list
+    assert f(FAKE + 8, FAKE, FAKE, 1, 8, 8, 128, 2, None) == 1      # misaligned pool
+    assert f(None, None, None, 0, 8, 8, 128, 2, None) == 0          # nothing to copy
