@@ -145,6 +145,25 @@ int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, con
                               size_t workspace_bytes, int dtype, void* stream);
 
 /*
+ * Test support: gather each sequence's cached K/V through its block table into
+ * contiguous rows ("vLLM 在 CANN 上的推理优化", read_kv: position t of a
+ * sequence lives at offset t % block_size of block table[t / block_size]).
+ * The attention calls never do this (the paged design avoids the gathered
+ * copy); it exists to check the index translation byte for byte.
+ *   k_out, v_out  [cu_seq_lens[num_seqs], num_kv_heads, head_dim], device
+ *   cu_seq_lens   device int32 [num_seqs + 1], exclusive prefix sum of seq_lens
+ *   elem_bytes    2 (fp16/bf16 pools) or 1 (FP8 pools)
+ * Row b, t receives cache[table[b][t / 16], t % 16] for t < seq_lens[b].  A
+ * table entry outside [0, num_blocks) zero-fills its rows and sets
+ * PA_DEVERR_BLOCK_ID; a length that disagrees with cu_seq_lens or exceeds the
+ * table sets PA_DEVERR_SEQ_LEN and skips the sequence.
+ */
+int pa_paged_kv_gather(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                       const int32_t* cu_seq_lens, int num_seqs, int max_seq_len, int num_blocks,
+                       int num_kv_heads, int head_dim, int elem_bytes, void* stream);
+
+/*
  * Copy whole blocks of both pools, the copy-on-write step of a shared block
  * ("vLLM-Ascend 原理", section 2.1: sequences that share a prefix point at
  * the same physical blocks and copy before they diverge).  For each i,

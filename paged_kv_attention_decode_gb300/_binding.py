@@ -45,6 +45,7 @@ _SIGNATURES = {
     "pa_paged_attention_decode_fp8": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _f32, _f32, _f32,
                                              _i32, _i32, _i32, _i32, _i32, _p, _sz, _i32, _p]),
     "pa_copy_blocks": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _p]),
+    "pa_paged_kv_gather": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _p]),
 }
 
 
@@ -229,6 +230,28 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, pairs: torch.Tenso
     rc = load_library().pa_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), pairs.data_ptr(), pairs.shape[0],
                                        NB, H, D, k_cache.element_size(), _stream(stream))
     _check(rc, "pa_copy_blocks")
+
+
+def paged_kv_gather(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                    seq_lens: torch.Tensor, max_seq_len: int, stream=None):
+    """Test support: every sequence's live K/V rows, gathered through its block
+    table into contiguous [sum(seq_lens), Hkv, D] tensors."""
+    _cuda(k_cache, v_cache, block_tables, seq_lens)
+    _need(block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32, "int32 tables")
+    _need(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype, "cache shape/dtype")
+    NB, bs, H, D = k_cache.shape
+    B = seq_lens.shape[0]
+    cu = torch.zeros(B + 1, dtype=torch.int32, device=seq_lens.device)
+    torch.cumsum(seq_lens, 0, out=cu[1:])
+    total = int(cu[-1])
+    k_out = torch.empty(total, H, D, dtype=k_cache.dtype, device=k_cache.device)
+    v_out = torch.empty_like(k_out)
+    rc = load_library().pa_paged_kv_gather(k_out.data_ptr(), v_out.data_ptr(), k_cache.data_ptr(),
+                                           v_cache.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
+                                           seq_lens.data_ptr(), cu.data_ptr(), B, max_seq_len, NB, H, D,
+                                           k_cache.element_size(), _stream(stream))
+    _check(rc, "pa_paged_kv_gather")
+    return k_out, v_out
 
 
 def device_error(clear: bool = True, stream=None) -> int:

@@ -265,7 +265,7 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
     p.max_rows = max_rows;
     // (query, head) columns per work item: 8, or 16 once a row can have more
     const int cols = max_q * p.group;
-    const int chunk = (PA_VERIFY_MAX_NT > 1 && cols > 8) ? 16 : 8;
+    const int chunk = cols > 8 ? 16 : 8;
     p.col_chunks = (cols + chunk - 1) / chunk;
     p.scale_log2 = scale_log2(scale) * k_scale;
     p.v_scale = v_scale;
@@ -426,6 +426,29 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_p
     if (!err) return PA_ERR_CUDA;
     cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_blocks, block_bytes, err,
                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_paged_kv_gather(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                       const int32_t* cu_seq_lens, int num_seqs, int max_seq_len, int num_blocks, int num_kv_heads,
+                       int head_dim, int elem_bytes, void* stream) {
+    if (num_seqs < 0 || num_seqs > kMaxGrid || max_seq_len < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (num_blocks <= 0 || num_blocks > kMaxPoolBlocks || num_kv_heads <= 0 || head_dim <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (elem_bytes != 1 && elem_bytes != 2) return PA_ERR_UNSUPPORTED;
+    const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * elem_bytes;
+    if (row_bytes % 16) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!k_out || !v_out || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_out) || !aligned16(v_out) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    unsigned int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    cudaError_t e = pa::launch_kv_gather(k_out, v_out, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
+                                         cu_seq_lens, num_seqs, num_blocks, row_bytes, max_seq_len, err,
+                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

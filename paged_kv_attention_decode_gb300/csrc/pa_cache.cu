@@ -224,4 +224,52 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pair
     return cudaGetLastError();
 }
 
+// Gather every live token row of each sequence through its block table into
+// contiguous rows: out[cu_seq_lens[b] + t] = cache[table[b][t / 16], t % 16]
+// ("vLLM 在 CANN 上的推理优化", read_kv: logical index -> block, offset).  One
+// CTA row (blockIdx.y) per sequence; each warp moves whole token rows with
+// 16-byte loads.  A table entry outside the pool zero-fills its rows.
+__global__ void __launch_bounds__(256) kv_gather_kernel(uint4* __restrict__ k_out, uint4* __restrict__ v_out,
+                                                        const uint4* __restrict__ k_cache,
+                                                        const uint4* __restrict__ v_cache,
+                                                        const int32_t* __restrict__ block_tables, int max_blocks,
+                                                        const int32_t* __restrict__ seq_lens,
+                                                        const int32_t* __restrict__ cu_seq_lens, int num_blocks,
+                                                        int row_chunks, unsigned int* err) {
+    const int b = blockIdx.y;
+    int n = seq_lens[b];
+    const int64_t base = cu_seq_lens[b];
+    if (n < 0 || n > max_blocks * 16 || cu_seq_lens[b + 1] - base != n) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) record_error(err, PA_DEVERR_SEQ_LEN_);
+        return;
+    }
+    const int lane = threadIdx.x & 31;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n; t += warps) {
+        const int phys = block_tables[static_cast<int64_t>(b) * max_blocks + (t >> 4)];
+        const bool ok = phys >= 0 && phys < num_blocks;
+        if (!ok && lane == 0) record_error(err, PA_DEVERR_BLOCK_ID_);
+        const int64_t src = (static_cast<int64_t>(phys) * 16 + (t & 15)) * row_chunks;
+        const int64_t dst = (base + t) * row_chunks;
+        for (int c = lane; c < row_chunks; c += 32) {
+            k_out[dst + c] = ok ? k_cache[src + c] : make_uint4(0, 0, 0, 0);
+            v_out[dst + c] = ok ? v_cache[src + c] : make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+cudaError_t launch_kv_gather(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                             const int32_t* cu_seq_lens, int num_seqs, int num_blocks, int64_t row_bytes,
+                             int max_seq_len, unsigned int* err, cudaStream_t s) {
+    if (num_seqs == 0) return cudaSuccess;
+    const int threads = 256;
+    const int gx = std::max(1, std::min((max_seq_len + 7) / 8, 64));   // 8 token rows per CTA pass
+    kv_gather_kernel<<<dim3(gx, num_seqs), threads, 0, s>>>(
+        static_cast<uint4*>(k_out), static_cast<uint4*>(v_out), static_cast<const uint4*>(k_cache),
+        static_cast<const uint4*>(v_cache), block_tables, max_blocks, seq_lens, cu_seq_lens, num_blocks,
+        static_cast<int>(row_bytes / 16), err);
+    return cudaGetLastError();
+}
+
 }  // namespace pa

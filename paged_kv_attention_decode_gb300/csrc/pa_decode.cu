@@ -45,13 +45,16 @@ constexpr float kLazyRescaleLog2 = 8.f;
 // A warp handles one block at a time, so it moves bytes at (tile bytes) /
 // (block latency); FP8 tiles are half the bytes, so the FP8 MHA kernel keeps
 // small rings and runs more CTAs (warps) per SM instead.
-template <int D, bool kFp8, bool kMma>
+template <int D, bool kFp8, bool kMma, int kMaxNT = 1>
 struct DecodeShape {
     static constexpr int kTileBytes = 16 * D * (kFp8 ? 1 : 2);  // one (block, kv head) tile
     static constexpr int kStageBytes = 2 * kTileBytes;          // K tile + V tile
-    // The tensor-core kernels are bound by instruction latency per warp, so
-    // they trade ring depth for resident warps (3 CTAs per SM at 2 stages).
-    static constexpr int kStages = kFp8 ? (kMma ? 4 : 2) : (kMma ? PA_MMA_STAGES : 3);
+    // The 16-bit tensor-core kernels are bound by instruction latency per
+    // warp: the single-tile one (group heads of decode rows) runs best with
+    // 2-stage rings and 3 CTAs (12 warps) per SM; the two-tile one (verify
+    // rows, 16 columns) with 3-stage rings and 2 CTAs per SM.
+    static constexpr int kStages = kFp8 ? (kMma ? 4 : 2) : (kMma ? (kMaxNT > 1 ? 3 : 2) : 3);
+    static constexpr int kMinCtasPerSm = (kMma && !kFp8) ? (kMaxNT > 1 ? 2 : 3) : 1;
     static constexpr int kConvBytes = (kFp8 && kMma) ? 2 * 16 * D * 2 : 0;
     static constexpr int kWarpBytes = kStages * kStageBytes + kConvBytes;
     static constexpr int kSmemBytes = kDecodeWarps * kWarpBytes + 1024;  // + alignment slack
@@ -63,10 +66,10 @@ struct WarpRing {
     uint64_t* bars;     // STAGES mbarriers
 };
 
-template <int D, bool kFp8, bool kMma>
+template <int D, bool kFp8, bool kMma, int kMaxNT>
 __device__ __forceinline__ void issue_tile(const WarpRing& ring, int slot, int phys, int kv_head,
                                           const CUtensorMap* kmap, const CUtensorMap* vmap) {
-    using Shape = DecodeShape<D, kFp8, kMma>;
+    using Shape = DecodeShape<D, kFp8, kMma, kMaxNT>;
     uint8_t* dst = ring.base + slot * Shape::kStageBytes;
     mbar_arrive_expect_tx(&ring.bars[slot], Shape::kStageBytes);
     if constexpr (kFp8) {
@@ -504,11 +507,11 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
 // the warp's HBM pipeline never drains between items.  Warps never wait for
 // one another.
 template <typename T, int D, bool kMma, bool kFp8, int kMaxNT>
-__global__ void __launch_bounds__(kDecodeWarps * 32, (kMma && !kFp8) ? PA_MMA_MIN_CTAS : 1)
+__global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, kMaxNT>::kMinCtasPerSm)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap) {
     static_assert(kMma || kMaxNT == 1, "the FMA path handles one query per row");
-    using Shape = DecodeShape<D, kFp8, kMma>;
+    using Shape = DecodeShape<D, kFp8, kMma, kMaxNT>;
     constexpr int kDecodeStages = Shape::kStages;
     constexpr int kQueue = 8;  // claimed items not yet computed (<= STAGES + 1 in use)
     constexpr int kChunkCols = 8 * kMaxNT;
@@ -639,7 +642,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kMma && !kFp8) ? PA_MMA_MI
         const int phys = fi.bt[fblk];
         if (lane == 0) {
             if (phys >= 0 && phys < p.num_blocks) {
-                issue_tile<D, kFp8, kMma>(ring, slot, phys, fi.g, &kmap, &vmap);
+                issue_tile<D, kFp8, kMma, kMaxNT>(ring, slot, phys, fi.g, &kmap, &vmap);
             } else {
                 record_error(p.err, PA_DEVERR_BLOCK_ID_);
                 mbar_arrive(&ring.bars[slot]);  // complete the phase without data
@@ -932,7 +935,7 @@ int sm_count() {
 template <typename T, int D, bool kMma, bool kFp8 = false, int kMaxNT = 1>
 cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t s) {
-    constexpr int smem = DecodeShape<D, kFp8, kMma>::kSmemBytes;
+    constexpr int smem = DecodeShape<D, kFp8, kMma, kMaxNT>::kSmemBytes;
     auto kern = decode_kernel<T, D, kMma, kFp8, kMaxNT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -972,7 +975,7 @@ cudaError_t launch_decode_fp8(const DecodeParams& p, const CUtensorMap& kmap, co
 template <typename T, int D>
 cudaError_t launch_decode_d(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t s) {
-    if (PA_VERIFY_MAX_NT > 1 && p.max_q * p.group > 8) return launch_decode_t<T, D, true, false, 2>(p, kmap, vmap, s);
+    if (p.max_q * p.group > 8) return launch_decode_t<T, D, true, false, 2>(p, kmap, vmap, s);
     if (p.group > 1 || p.max_q > 1) return launch_decode_t<T, D, true, false, 1>(p, kmap, vmap, s);
     return launch_decode_t<T, D, false, false, 1>(p, kmap, vmap, s);
 }

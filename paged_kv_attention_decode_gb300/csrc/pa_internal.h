@@ -38,18 +38,6 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 // in the prefill kernels.
 #define PA_VERIFY_MAX_Q_ 8
 
-// Tuning of the tensor-core decode kernel (decode rows with group > 1,
-// verify rows): ring depth, resident CTAs per SM it is compiled for, and the
-// most 8-column tiles one work item takes (1: 8 columns, 2: 16 columns).
-#ifndef PA_MMA_STAGES
-#define PA_MMA_STAGES 2
-#endif
-#ifndef PA_MMA_MIN_CTAS
-#define PA_MMA_MIN_CTAS 3
-#endif
-#ifndef PA_VERIFY_MAX_NT
-#define PA_VERIFY_MAX_NT 2
-#endif
 
 struct DecodeParams {
     void* out;                    // [T, Hq, D] (T = B without cu_q_lens)
@@ -121,6 +109,10 @@ cudaError_t launch_kv_write_fp8(const void* key, const void* value, void* k_cach
 // pairs: device int32 [num_pairs, 2] (source block, destination block).
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs, int num_blocks,
                                int64_t block_bytes, unsigned int* err, cudaStream_t s);
+cudaError_t launch_kv_gather(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                             const int32_t* cu_seq_lens, int num_seqs, int num_blocks, int64_t row_bytes,
+                             int max_seq_len, unsigned int* err, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            int head_dim, int dtype, int max_q_len, cudaStream_t s);
 // tcgen05 prefill: groups of 1, 2, 4 or 8 q heads per kv head; q_per_tile = 128 / group.

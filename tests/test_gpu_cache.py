@@ -74,3 +74,42 @@ def test_out_of_range_table_entry_gives_slot_minus_one_and_flag():
     slots = pa.slot_mapping(bt, sl, None, 2, 4)
     assert slots.cpu().tolist() == [1 * 16 + 3, -1]
     assert pa.device_error() == 1
+
+
+@pytest.mark.parametrize("name,fp8", [("gqa_prefix", False), ("llama7b_decode_fp8", True), ("tiny", False)])
+def test_gather_matches_numpy_fancy_index(name, fp8):
+    """pa_paged_kv_gather returns, byte for byte, the rows a NumPy fancy-index
+    gather of the pool through the block tables returns."""
+    kw = {"batch": 24} if name != "tiny" else {}
+    w = W.make(name, device=DEV, **kw)
+    bt = torch.from_numpy(w.block_tables).to(DEV)
+    sl = torch.from_numpy(w.seq_lens).to(DEV)
+    k, v = pa.paged_kv_gather(w.k_cache, w.v_cache, bt, sl, w.max_seq_len)
+    torch.cuda.synchronize()
+    assert pa.device_error() == 0
+    rows = []
+    for b in range(w.batch):
+        t = np.arange(int(w.seq_lens[b]))
+        rows.append(w.block_tables[b, t // 16].astype(np.int64) * 16 + t % 16)
+    idx = np.concatenate(rows)
+    H, D = w.num_kv_heads, w.head_dim
+    view = torch.uint8 if fp8 else torch.int16
+    kc = w.k_cache.view(view).cpu().numpy().reshape(-1, H, D)
+    vc = w.v_cache.view(view).cpu().numpy().reshape(-1, H, D)
+    assert np.array_equal(k.view(view).cpu().numpy(), kc[idx])
+    assert np.array_equal(v.view(view).cpu().numpy(), vc[idx])
+
+
+def test_gather_out_of_pool_entry_zero_fills_and_flags():
+    w = W.make("tiny", device=DEV)
+    tables = w.block_tables.copy()
+    tables[3, 2] = w.num_blocks + 5            # a live entry of the 100-token sequence
+    bt = torch.from_numpy(tables).to(DEV)
+    sl = torch.from_numpy(w.seq_lens).to(DEV)
+    pa.device_error()
+    k, v = pa.paged_kv_gather(w.k_cache, w.v_cache, bt, sl, w.max_seq_len)
+    torch.cuda.synchronize()
+    assert pa.device_error() == 1
+    start = int(w.seq_lens[:3].sum())
+    assert float(k[start + 32: start + 48].float().abs().max()) == 0.0
+    assert float(k[start: start + 32].float().abs().max()) > 0.0
