@@ -847,14 +847,103 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
 
 // Merge the partitions of each (query row, q head):
 // out = sum_p acc_p 2^(m_p - M) / sum_p l_p 2^(m_p - M), M = max_p m_p.
-// One CTA per q head walks the listed partials rows.  The per-partition
-// weights are formed once in shared memory; each thread then streams one head
-// dimension of every partition's accumulator.
-constexpr int kReduceMaxParts = 1024;   // partitions staged in shared memory per pass
-constexpr int kReduceMaxRowsPerLaunch = 2048;
+// One warp per (listed partials row, q head); persistent CTAs of 8 warps
+// stride over all of them.  A warp forms its partition weights once in shared
+// memory (in passes of kReducePass partitions), then each lane streams
+// D / 32 dimensions of every partition's accumulator with vector loads.
+constexpr int kReduceWarps = 8;
+constexpr int kReducePass = 256;   // partition weights staged per warp per pass
 
 template <typename T, int D>
-__global__ void __launch_bounds__(D) decode_reduce_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const DecodeParams p) {
+    constexpr int DPL = D / 32;
+    __shared__ float sc_all[kReduceWarps][kReducePass];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    float* sc = sc_all[warp];
+    const int P = p.partition_tokens;
+    const int64_t pairs = static_cast<int64_t>(*p.row_count) * p.num_q_heads;
+    for (int64_t w = static_cast<int64_t>(blockIdx.x) * kReduceWarps + warp; w < pairs;
+         w += static_cast<int64_t>(gridDim.x) * kReduceWarps) {
+        const int k = static_cast<int>(w / p.num_q_heads);
+        const int hq = static_cast<int>(w - static_cast<int64_t>(k) * p.num_q_heads);
+        const uint32_t entry = static_cast<uint32_t>(p.rows[k]);
+        const int b = static_cast<int>(entry >> 3);
+        const int qrow = (p.cu_q_lens ? p.cu_q_lens[b] : b) + static_cast<int>(entry & 7u);
+        int n = p.seq_lens[b];
+        if (n < 0 || n > p.max_seq_len || n > p.max_blocks * 16) n = 0;
+        const int nparts = n > 0 ? (n + P - 1) / P : 1;
+        const int64_t base = (static_cast<int64_t>(k) * p.num_q_heads + hq) * p.max_parts;
+        const float* wm = p.ws_m + base;
+        const float* wl = p.ws_l + base;
+        const float* wa = p.ws_acc + base * D + lane * DPL;
+
+        float M = -INFINITY;
+        for (int i = lane; i < nparts; i += 32) M = fmaxf(M, wm[i]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+
+        float L = 0.f, acc[DPL];
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
+        if (M != -INFINITY) {
+            for (int p0 = 0; p0 < nparts; p0 += kReducePass) {
+                const int np = min(kReducePass, nparts - p0);
+                float lpart = 0.f;
+                for (int i = lane; i < np; i += 32) {
+                    const float s = fast_exp2(wm[p0 + i] - M);
+                    sc[i] = s;
+                    lpart = fmaf(wl[p0 + i], s, lpart);
+                }
+                L += lpart;
+                __syncwarp();
+                const float* a = wa + static_cast<int64_t>(p0) * D;
+#pragma unroll 4
+                for (int i = 0; i < np; ++i) {
+                    const float s = sc[i];
+                    if constexpr (DPL == 4) {
+                        const float4 x = *reinterpret_cast<const float4*>(a + static_cast<int64_t>(i) * D);
+                        acc[0] = fmaf(x.x, s, acc[0]);
+                        acc[1] = fmaf(x.y, s, acc[1]);
+                        acc[2] = fmaf(x.z, s, acc[2]);
+                        acc[3] = fmaf(x.w, s, acc[3]);
+                    } else {
+                        const float2 x = *reinterpret_cast<const float2*>(a + static_cast<int64_t>(i) * D);
+                        acc[0] = fmaf(x.x, s, acc[0]);
+                        acc[1] = fmaf(x.y, s, acc[1]);
+                    }
+                }
+                __syncwarp();   // sc is rewritten by the next pass or pair
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + (static_cast<int64_t>(qrow) * p.num_q_heads + hq) * D +
+                      lane * DPL;
+        if constexpr (DPL == 4) {
+            uint2 v;
+            v.x = Elem<T>::pack(acc[0] * inv, acc[1] * inv);
+            v.y = Elem<T>::pack(acc[2] * inv, acc[3] * inv);
+            *reinterpret_cast<uint2*>(o) = v;
+        } else {
+            *reinterpret_cast<uint32_t*>(o) = Elem<T>::pack(acc[0] * inv, acc[1] * inv);
+        }
+    }
+}
+
+// The same merge with a whole CTA per (listed partials row, q head): for
+// launches with few pairs and many partitions (long contexts), where one warp
+// per pair would leave most SMs idle.  The per-partition weights are formed
+// once in shared memory; each thread then streams one head dimension of every
+// partition's accumulator.
+constexpr int kReduceMaxParts = 1024;   // partitions staged in shared memory per pass
+constexpr int kReduceMaxRowsPerLaunch = 2048;
+// below this many (row, q head) pairs a whole CTA merges each pair
+constexpr long long kReduceWarpPairsMin = 1024;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(D) decode_reduce_cta_kernel(const DecodeParams p) {
     __shared__ float sc[kReduceMaxParts];
     __shared__ float red[D / 32];
     const int hq = blockIdx.x;
@@ -952,8 +1041,16 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, cons
     e = launch_pdl(kern, dim3(grid), dim3(kDecodeWarps * 32), smem, s, p, kmap, vmap);
     if (e != cudaSuccess) return e;
     if (p.max_parts > 1) {
-        dim3 rgrid(p.num_q_heads, std::min(p.max_rows, kReduceMaxRowsPerLaunch));
-        decode_reduce_kernel<T, D><<<rgrid, D, 0, s>>>(p);
+        const long long pairs = static_cast<long long>(p.max_rows) * p.num_q_heads;
+        if (pairs >= kReduceWarpPairsMin) {
+            // persistent: a few waves of 8-warp CTAs, one warp per pair
+            const int rgrid = static_cast<int>(std::max<long long>(
+                1, std::min<long long>((pairs + kReduceWarps - 1) / kReduceWarps, 8LL * sm_count())));
+            decode_reduce_kernel<T, D><<<rgrid, kReduceWarps * 32, 0, s>>>(p);
+        } else {
+            dim3 rgrid(p.num_q_heads, std::min(p.max_rows, kReduceMaxRowsPerLaunch));
+            decode_reduce_cta_kernel<T, D><<<rgrid, D, 0, s>>>(p);
+        }
         e = cudaGetLastError();
     }
     return e;
