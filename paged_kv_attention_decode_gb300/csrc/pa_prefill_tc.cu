@@ -5,23 +5,31 @@
 // 2.4: a later chunk reads the KV earlier chunks wrote), for query groups of
 // 1, 2, 4 or 8 heads per kv head.
 //
-// One CTA = 128 rows = (query, q head) pairs of one kv group; TMEM lane r
-// holds row r.  Warp specialisation:
-//   * warp 4, lane 0: TMA (Q once; K/V 64-key tiles gathered block by block
-//     through the block table into a ring of stages) and every tcgen05.mma;
-//   * warps 0-3, thread r = row r: the softmax of its row.
-// Per 64-key tile j:
-//   S(j) = Q K^T     M=128 N=64 K=16 x D/16 into one of two TMEM S buffers,
-//                    issued as soon as K(j) has landed, so it overlaps the
-//                    softmax of tile j-1;
-//   softmax(j)       tcgen05.ld of the S row, running reference m_ref and sum
-//                    l, P row (bf16/fp16) into shared memory, 128-byte swizzled;
-//   O += P(j) V(j)   M=128 N=D K=16 x 4 (V read MN-major), accumulated in TMEM.
-// O stays in TMEM for the whole key range.  A row rescales O and l only when
-// its running maximum exceeds m_ref by more than 2^8 (so P <= 256); then the
-// row's O is read, scaled and written back in TMEM before P(j) V is issued.
-// Only the tiles that cross the causal diagonal are masked; V rows past the
-// tile's last query position are cleared so that 0 * NaN cannot reach O.
+// One persistent CTA per SM.  A work item is a pair of adjacent 128-row query
+// tiles, A and B (rows = (query, q head) pairs of one kv group; TMEM lane r =
+// row r), that share one stream of 64-key K/V tiles: every K/V byte loaded
+// feeds two tiles of MMAs.  Warp roles:
+//   * warps 0-3: softmax of tile A, warps 4-7: softmax of tile B (thread r of
+//     a group = row r);
+//   * warp 8, lane 0: every tcgen05.mma;
+//   * warps 9-11: the TMA loads (Q tiles; K and V tiles gathered block by
+//     block through the block table into separate rings of kStages stages).
+//     TMA issue is costly per SM sub-partition, so the boxes of a tile are
+//     split over three warps on three sub-partitions.
+// Tensor memory (512 columns): S_A[2] | S_B[2] (64 columns each) | O_A | O_B.
+// Per key tile j and query tile X:
+//   S_X(j) = Q_X K(j)^T   M=128 N=64 into S_X[j & 1], issued as soon as K(j)
+//                          has landed, so that it overlaps the softmax of j-1;
+//   softmax_X(j)          tcgen05.ld of the S row, running reference m_ref and
+//                          sum l; P (bf16/fp16) is stored over the row's S;
+//   O_X += P_X(j) V(j)    M=128 N=D K=64, A read from tensor memory.
+// While one tile's softmax runs, the tensor cores work on the other tile.
+// K(j)'s stage is refilled once both S(j) are done, V(j)'s once both P V are
+// (k_free / v_free, committed by the MMA warp).
+// A row rescales O and l only when its maximum exceeds m_ref by more than 2^8
+// (so P <= 256).  Only tiles that cross the causal diagonal are masked; V rows
+// past the pair's last query position (or in blocks outside the pool) are
+// cleared so that 0 * NaN cannot reach O.
 #include <algorithm>
 #include <type_traits>
 
@@ -31,23 +39,26 @@ namespace pa {
 
 namespace {
 
-constexpr int kTcSoftmaxWarps = 4;
-constexpr int kTcThreads = (kTcSoftmaxWarps + 1) * 32;
+constexpr int kTcSoftmaxWarps = 4;                                   // per query tile
+constexpr int kTcTiles = 2;                                          // query tiles per item (A, B)
+constexpr int kTcMmaWarp = kTcTiles * kTcSoftmaxWarps;                // warp 8
+constexpr int kTcLoaders = 3;                                        // warps 9-11
+constexpr int kTcThreads = (kTcMmaWarp + 1 + kTcLoaders) * 32;      // 384
 constexpr int kTcKeys = 64;
-constexpr uint32_t kTmemCols = 256;  // S0 (64) | S1 (64) | O (<= 128)
+constexpr uint32_t kTmemCols = 512;  // S_A[2] S_B[2] (64 each) | O_A | O_B
 constexpr float kRescaleLog2 = 8.f;
 constexpr unsigned kFullMask = 0xffffffffu;
 
-template <int D, int ST>
+template <int D>
 struct TcShape {
     static constexpr int kKeyHalf = kTcKeys * 128;          // 64 keys x one 64-dim half
-    static constexpr int kKV = (D / 64) * kKeyHalf;         // K (or V) of one stage: [half][key][128 B]
-    static constexpr int kStage = 2 * kKV;
+    static constexpr int kKV = (D / 64) * kKeyHalf;         // K or V of one tile: [half][key][128 B]
     static constexpr int kQHalf = 128 * 128;                // 128 rows x one half
-    static constexpr int kQ = (D / 64) * kQHalf;
-    static constexpr int kP = 128 * 128;                    // 128 rows x 64 keys x 2 B
-    static constexpr bool kPInK = kKV >= kP;                // P(j) reuses the K region of its stage
-    static constexpr int kSmem = kQ + ST * kStage + (kPInK ? 0 : ST * kP) + 1024;
+    static constexpr int kQ = (D / 64) * kQHalf;            // one query tile
+    static constexpr int kBudget = 227 * 1024 - 1024;      // dynamic shared memory less alignment slack
+    static constexpr int kStagesFit = (kBudget - kTcTiles * kQ) / (2 * kKV);
+    static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;     // 5 at D = 128, 6 at D = 64
+    static constexpr int kSmem = kTcTiles * kQ + kStages * 2 * kKV + 1024;
 };
 
 // Bounded mbarrier wait that also gives up when another thread of the CTA has
@@ -60,10 +71,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     return false;
 }
 
-// Work list of the chunked-prefill tiles: offsets[b] = number of 128-row tiles
-// of sequences 0..b-1 whose chunk is longer than PA_VERIFY_MAX_Q_ tokens
-// (shorter chunks are decode or speculative-verify rows and belong to the
-// decode kernel); offsets[B] = total.  One CTA.
+// Work list of the chunked-prefill items: offsets[b] = number of query-tile
+// pairs (two 128-row tiles) of sequences 0..b-1 whose chunk is longer than
+// PA_VERIFY_MAX_Q_ tokens (shorter chunks are decode or speculative-verify
+// rows and belong to the decode kernel); offsets[B] = total.  One CTA.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __restrict__ cu_q_lens, int num_seqs,
                                                             int q_per_tile, int32_t* __restrict__ offsets) {
     __shared__ int warp_tot[32];
@@ -78,7 +89,8 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
         int v = 0;
         if (b < num_seqs) {
             const int ql = cu_q_lens[b + 1] - cu_q_lens[b];
-            v = ql > PA_VERIFY_MAX_Q_ ? (ql + q_per_tile - 1) / q_per_tile : 0;
+            const int tiles = ql > PA_VERIFY_MAX_Q_ ? (ql + q_per_tile - 1) / q_per_tile : 0;
+            v = (tiles + kTcTiles - 1) / kTcTiles;
         }
         int incl = v;
 #pragma unroll
@@ -108,26 +120,36 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
 }
 
 // Persistent: each CTA walks work items w = blockIdx.x, blockIdx.x + gridDim.x, ...
-// over (tile, kv head) pairs of the plan; within a sequence the tiles nearest
+// over (tile pair, kv head) of the plan; within a sequence the pairs nearest
 // the end (the longest key ranges) come first.
-// Two CTAs share an SM: ten warps, so one SM sub-partition runs three of them
-// and its 16K registers allow at most 168 per thread.
-template <typename T, int D, int ST>
-__global__ void __maxnreg__(168)
+template <typename T, int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const int32_t* __restrict__ plan,
                       const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const __grid_constant__ CUtensorMap qmap) {
-    using Sh = TcShape<D, ST>;
+    using Sh = TcShape<D>;
+    constexpr int NS = Sh::kStages;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdescS = mma_idesc_f16(128, kTcKeys, kBf16, false);
     constexpr uint32_t kIdescPV = mma_idesc_f16(128, D, kBf16, true);
 
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t full_bar[ST];
-    __shared__ uint64_t s_full[2];
-    __shared__ uint64_t p_full[2];   // per tile parity: one arrival per softmax warp
-    __shared__ uint64_t o_done;
-    __shared__ uint32_t bad_mask[ST];
+    __shared__ uint64_t k_full[NS];               // K tile landed (one arrival per loader)
+    __shared__ uint64_t v_full[NS];               // V tile landed (one arrival per loader)
+    __shared__ uint64_t k_free[NS];               // every S of the stage's tile complete
+    __shared__ uint64_t v_free[NS];               // every P V of the stage's tile complete
+    __shared__ uint64_t q_full;                   // the item's query tiles landed
+    __shared__ uint64_t item_done;                // every MMA of an item complete
+    __shared__ uint64_t s_full[kTcTiles][2];      // S_X(j) complete, by tile parity
+    __shared__ uint64_t p_full[kTcTiles][2];      // P_X(j) stored: one arrival per softmax warp, by parity
+    // P_X(j) V(j) complete, by tile parity.  A parity wait is only sound when
+    // the barrier's previous phase is known complete: with one barrier per
+    // parity, waiting for P V(T) needs P V(T-2) done, which every waiter has
+    // (S(T) is issued only after it); one barrier would need P V(T-1), which
+    // may still run when the last tile's softmax ends.  A completed phase
+    // also means every earlier MMA completed (tcgen05.commit tracks all of them).
+    __shared__ uint64_t o_done[kTcTiles][2];
+    __shared__ int32_t stage_blocks[kTcLoaders][NS][4];   // each loader's record of its stages' block ids
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -141,22 +163,31 @@ __global__ void __maxnreg__(168)
 
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    uint8_t* qs = smem;
-    auto kst = [&](int s) { return smem + Sh::kQ + s * Sh::kStage; };
-    auto vst = [&](int s) { return smem + Sh::kQ + s * Sh::kStage + Sh::kKV; };
-    auto pst = [&](int s) { return Sh::kPInK ? kst(s) : smem + Sh::kQ + ST * Sh::kStage + s * Sh::kP; };
+    auto qs = [&](int x) { return smem + x * Sh::kQ; };
+    auto kst = [&](int s) { return smem + kTcTiles * Sh::kQ + s * 2 * Sh::kKV; };
+    auto vst = [&](int s) { return smem + kTcTiles * Sh::kQ + s * 2 * Sh::kKV + Sh::kKV; };
 
     if (warp == 0) {
         tmem_alloc(&tmem_slot, kTmemCols);
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int s = 0; s < ST; ++s) mbar_init(&full_bar[s], 1);
-        mbar_init(&s_full[0], 1);
-        mbar_init(&s_full[1], 1);
-        mbar_init(&p_full[0], kTcSoftmaxWarps);
-        mbar_init(&p_full[1], kTcSoftmaxWarps);
-        mbar_init(&o_done, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&k_full[s], kTcLoaders);
+            mbar_init(&v_full[s], kTcLoaders);
+            mbar_init(&k_free[s], 1);
+            mbar_init(&v_free[s], 1);
+        }
+        mbar_init(&q_full, 1);
+        mbar_init(&item_done, 1);
+        for (int x = 0; x < kTcTiles; ++x) {
+            mbar_init(&s_full[x][0], 1);
+            mbar_init(&s_full[x][1], 1);
+            mbar_init(&p_full[x][0], kTcSoftmaxWarps);
+            mbar_init(&p_full[x][1], kTcSoftmaxWarps);
+            mbar_init(&o_done[x][0], 1);
+            mbar_init(&o_done[x][1], 1);
+        }
         abort_flag = 0;
         fence_barrier_init();
     }
@@ -164,17 +195,21 @@ __global__ void __maxnreg__(168)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_slot;
-    const uint32_t o_tm = tmem + 128;
     volatile int* abort_v = &abort_flag;
 
-    // per-CTA running counters (identical in every role): tiles processed so far
-    int J0 = 0;
+    // running counters (identical in every role): key tiles loaded so far (the
+    // ring position), tiles processed so far per query-tile slot, items so far
+    int kv0 = 0;
+    int t0[kTcTiles] = {0, 0};
+    int items = 0;
     bool ok = true;
-    // producer bookkeeping for the abort path
-    int s_issued = 0, pv_issued = 0, kv_issued = 0, kv_seen = 0;
+    // MMA warp bookkeeping for the abort path
+    int s_issued[kTcTiles] = {0, 0}, pv_issued[kTcTiles] = {0, 0};
+    int k_total = 0, v_total = 0;   // loader: K and V tiles issued so far (ring order)
 
-    for (int w = blockIdx.x; ok && w < total_items; w += gridDim.x) {
+    for (int w0 = blockIdx.x; ok && w0 < total_items; w0 += gridDim.x) {
         // ---- decode the work item -------------------------------------------
+        const int w = w0;
         const int g = w % p.num_kv_heads;
         const int l = w / p.num_kv_heads;
         int lo = 0, hi = p.num_seqs - 1;  // last b with plan[b] <= l
@@ -186,69 +221,42 @@ __global__ void __maxnreg__(168)
         const int row0 = p.cu_q_lens[b];
         const int qlen = p.cu_q_lens[b + 1] - row0;
         const int ntiles = (qlen + QT - 1) / QT;
-        const int qt = ntiles - 1 - (l - plan[b]);
+        const int npairs = (ntiles + kTcTiles - 1) / kTcTiles;
+        const int pr = npairs - 1 - (l - plan[b]);
         const int n = p.seq_lens[b];
         if (n < qlen || n > p.max_seq_len || n > p.max_blocks * 16) {
-            if (qt == ntiles - 1 && g == 0 && tid == 0) record_error(p.err, PA_DEVERR_SEQ_LEN_);
+            if (pr == npairs - 1 && g == 0 && tid == 0) record_error(p.err, PA_DEVERR_SEQ_LEN_);
             continue;
         }
-        const int q0 = qt * QT;
-        const int q_last = min(qlen, q0 + QT) - 1;
-        const int pos_min = n - qlen + q0;
-        const int pos_max = n - qlen + q_last;
-        const int nkt = (pos_max + kTcKeys) / kTcKeys;
-        const int nblk_live = (pos_max + 16) >> 4;
+        // query tiles A (x = 0) and B (x = 1, absent past the chunk's last tile)
+        int q0[kTcTiles], nkx[kTcTiles], pos_lo[kTcTiles], pos_hi[kTcTiles];
+#pragma unroll
+        for (int x = 0; x < kTcTiles; ++x) {
+            const int qt = pr * kTcTiles + x;
+            q0[x] = qt * QT;
+            if (qt < ntiles) {
+                const int q_last = min(qlen, q0[x] + QT) - 1;
+                pos_lo[x] = n - qlen + q0[x];
+                pos_hi[x] = n - qlen + q_last;
+                nkx[x] = (pos_hi[x] + kTcKeys) / kTcKeys;
+            } else {
+                pos_lo[x] = pos_hi[x] = 0;
+                nkx[x] = 0;
+            }
+        }
+        const int nkt = max(nkx[0], nkx[1]);                 // key tiles of the pair
+        const int pos_pair = nkx[1] ? pos_hi[1] : pos_hi[0];  // the pair's last query position
+        const int nblk_live = (pos_pair + 16) >> 4;
         const int32_t* bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
 
-        if (warp == kTcSoftmaxWarps) {
-            // ===================== producer / MMA issuer =====================
-            if (lane == 0) {
-                auto issue_kv = [&](int j, bool with_q) {
-                    const int s = (J0 + j) % ST;
-                    uint32_t bytes = with_q ? static_cast<uint32_t>(Sh::kQ) : 0u;
-                    uint32_t bad = 0;
-                    int phys[4];
-#pragma unroll
-                    for (int jb = 0; jb < 4; ++jb) {
-                        const int blk = j * 4 + jb;
-                        phys[jb] = -1;
-                        if (blk < nblk_live) {
-                            const int id = bt[blk];
-                            if (id >= 0 && id < p.num_blocks) {
-                                phys[jb] = id;
-                                bytes += 2 * (D / 64) * 2048;
-                            } else {
-                                bad |= 1u << jb;
-                                record_error(p.err, PA_DEVERR_BLOCK_ID_);
-                            }
-                        }
-                    }
-                    bad_mask[s] = bad;
-                    fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(&full_bar[s], bytes);
-                    if (with_q) {
-#pragma unroll
-                        for (int h = 0; h < D / 64; ++h)
-                            tma_load_4d(qs + h * Sh::kQHalf, &qmap, &full_bar[s], 0, h, g * G, row0 + q0);
-                    }
-#pragma unroll
-                    for (int jb = 0; jb < 4; ++jb) {
-                        if (phys[jb] < 0) continue;
-#pragma unroll
-                        for (int h = 0; h < D / 64; ++h) {
-                            tma_load_4d(kst(s) + h * Sh::kKeyHalf + jb * 2048, &kmap, &full_bar[s], 0, h, g,
-                                        phys[jb] * 16);
-                            tma_load_4d(vst(s) + h * Sh::kKeyHalf + jb * 2048, &vmap, &full_bar[s], 0, h, g,
-                                        phys[jb] * 16);
-                        }
-                    }
-                    ++kv_issued;
-                };
-                auto issue_s = [&](int j) {
-                    const int J = J0 + j;
-                    const uint32_t qa = smem_addr(qs);
-                    const uint32_t ka = smem_addr(kst(J % ST));
-                    const uint32_t d_tm = tmem + static_cast<uint32_t>((J & 1) * kTcKeys);
+        if (warp == kTcMmaWarp) {
+            // ============================ MMA issuer ============================
+            auto issue_s = [&](int x, int j) {
+                const int Tx = t0[x] + j;
+                if (lane == 0) {
+                    const uint32_t qa = smem_addr(qs(x));
+                    const uint32_t ka = smem_addr(kst((kv0 + j) % NS));
+                    const uint32_t d_tm = tmem + static_cast<uint32_t>(x * 128 + (Tx & 1) * kTcKeys);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint64_t a = smem_desc_sw128(qa + (kk >> 2) * Sh::kQHalf + (kk & 3) * 32, 16, 1024);
@@ -256,223 +264,362 @@ __global__ void __maxnreg__(168)
                             smem_desc_sw128(ka + (kk >> 2) * Sh::kKeyHalf + (kk & 3) * 32, 16, 1024);
                         tc_mma_f16(d_tm, a, bd, kIdescS, kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(&s_full[J & 1]);
-                    ++s_issued;
-                };
-                auto issue_pv = [&](int j) {
-                    const int s = (J0 + j) % ST;
-                    const uint32_t pa = smem_addr(pst(s));
-                    const uint32_t va = smem_addr(vst(s));
+                    tc_commit(&s_full[x][Tx & 1]);
+                }
+                __syncwarp();
+                ++s_issued[x];
+            };
+            // O_X += P_X(j) V(j): P is read from tensor memory, where the softmax
+            // stored it over the first 32 columns of S_X(j)
+            auto issue_pv = [&](int x, int j) {
+                const int Tx = t0[x] + j;
+                if (lane == 0) {
+                    const uint32_t p_tm = tmem + static_cast<uint32_t>(x * 128 + (Tx & 1) * kTcKeys);
+                    const uint32_t o_tm = tmem + static_cast<uint32_t>(256 + x * D);
+                    const uint32_t va = smem_addr(vst((kv0 + j) % NS));
 #pragma unroll
                     for (int kp = 0; kp < kTcKeys / 16; ++kp) {
-                        const uint64_t a = smem_desc_sw128(pa + kp * 32, 16, 1024);
                         const uint64_t bd = smem_desc_sw128(va + kp * 2048, Sh::kKeyHalf, 1024);
-                        tc_mma_f16(o_tm, a, bd, kIdescPV, (j > 0 || kp > 0) ? 1u : 0u);
+                        tc_mma_f16_ta(o_tm, p_tm + static_cast<uint32_t>(kp * 8), bd, kIdescPV,
+                                      (j > 0 || kp > 0) ? 1u : 0u);
                     }
-                    tc_commit(&o_done);
-                    ++pv_issued;
-                };
+                    tc_commit(&o_done[x][Tx & 1]);
+                }
+                __syncwarp();
+                ++pv_issued[x];
+            };
+            auto commit = [&](uint64_t* bar) {
+                if (lane == 0) tc_commit(bar);
+                __syncwarp();
+            };
+            auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+                return __all_sync(kFullMask, wait_or_abort(bar, parity, abort_v));
+            };
+            auto wait_o = [&](int x, int Tx) { return wait_all(&o_done[x][Tx & 1], (Tx >> 1) & 1); };
 
-                // the previous item's last P V must be done before Q and the
-                // stages are overwritten
-                if (J0 > 0) ok = wait_or_abort(&o_done, (J0 - 1) & 1, abort_v);
-                if (ok) {
-                    for (int t = 0; t < ST && t < nkt; ++t) issue_kv(t, t == 0);
-                    ok = wait_or_abort(&full_bar[J0 % ST], (J0 / ST) & 1, abort_v);
-                }
-                if (ok) {
-                    ++kv_seen;
-                    tc_fence_after_sync();
-                    issue_s(0);
-                }
-                for (int j = 0; ok && j < nkt; ++j) {
-                    const int J = J0 + j;
-                    if (j + 1 < nkt) {
-                        // S(j+1): its K has to be in; its TMEM buffer was last read
-                        // by the softmax of tile J-1, whose P we already waited for
-                        ok = wait_or_abort(&full_bar[(J + 1) % ST], ((J + 1) / ST) & 1, abort_v);
-                        if (!ok) break;
-                        ++kv_seen;
-                        tc_fence_after_sync();
-                        issue_s(j + 1);
-                    }
-                    // two barriers by tile parity: S(J+1) is already issued, so the
-                    // softmax warps may finish tiles J and J+1 before this wait; a
-                    // single barrier would then be two phases ahead of it
-                    ok = wait_or_abort(&p_full[J & 1], (J >> 1) & 1, abort_v);
+            // the previous item's MMAs must be complete: its S/P buffers and
+            // accumulators are reused
+            if (items > 0) ok = wait_all(&item_done, (items - 1) & 1);
+            if (ok) ok = wait_all(&q_full, items & 1) && wait_all(&k_full[kv0 % NS], (kv0 / NS) & 1);
+            if (ok) {
+                tc_fence_after_sync();
+#pragma unroll
+                for (int x = 0; x < kTcTiles; ++x)
+                    if (nkx[x]) issue_s(x, 0);
+                commit(&k_free[kv0 % NS]);
+            }
+            for (int j = 0; ok && j < nkt; ++j) {
+                const int J = kv0 + j;
+                if (j + 1 < nkt) {
+                    // S(j+1) as soon as K(j+1) is in; S_X[(j+1) & 1] last held
+                    // P_X(j-1), so that P V has to be complete
+                    ok = wait_all(&k_full[(J + 1) % NS], ((J + 1) / NS) & 1);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    issue_pv(j);
-                    if (j + ST < nkt) {
-                        // the stage is free once P(j) V(j) has completed
-                        ok = wait_or_abort(&o_done, J & 1, abort_v);
-                        if (!ok) break;
-                        issue_kv(j + ST, false);
+#pragma unroll
+                    for (int x = 0; x < kTcTiles; ++x) {
+                        if (j + 1 >= nkx[x]) continue;
+                        if (j >= 1 && !(ok = wait_o(x, t0[x] + j - 1))) break;
+                        tc_fence_after_sync();
+                        issue_s(x, j + 1);
+                    }
+                    if (!ok) break;
+                    commit(&k_free[(J + 1) % NS]);   // K(j+1)'s stage, once both S are done
+                }
+                ok = wait_all(&v_full[J % NS], (J / NS) & 1);
+                if (!ok) break;
+                // two barriers by tile parity: S_X(j+1) is already issued, so
+                // the softmax may finish tiles j and j+1 before this wait
+#pragma unroll
+                for (int x = 0; x < kTcTiles; ++x) {
+                    if (j >= nkx[x]) continue;
+                    const int Tx = t0[x] + j;
+                    if (!(ok = wait_all(&p_full[x][Tx & 1], (Tx >> 1) & 1))) break;
+                    tc_fence_after_sync();
+                    issue_pv(x, j);
+                }
+                if (!ok) break;
+                commit(&v_free[J % NS]);   // V(j)'s stage, once both P V are done
+            }
+            if (ok) commit(&item_done);
+            if (!ok && lane == 0) *abort_v = 1;
+        } else if (warp > kTcMmaWarp) {
+            // ============================== loaders =============================
+            // Loader li issues the boxes b = li, li + 3, ... of each K and V
+            // tile, box b = one 64-dim half (b % (D/64)) of one 16-token block
+            // (b / (D/64)); lane 0 issues, and arrives on the tile's barrier
+            // with its bytes.  Before a stage is refilled, the MMA warp's
+            // k_free / v_free for the stage's previous tile is awaited.
+            const int li = warp - kTcMmaWarp - 1;
+            constexpr int kHalves = D / 64;
+            constexpr int kBoxes = 4 * kHalves;
+            if (lane == 0) {
+                auto ids_of = [&](int j, int s) {
+                    // this loader's blocks of tile j, recorded for the V issue
+#pragma unroll
+                    for (int blk = 0; blk < 4; ++blk) {
+                        bool mine = false;
+#pragma unroll
+                        for (int h = 0; h < kHalves; ++h) mine |= (blk * kHalves + h) % kTcLoaders == li;
+                        int id = -1;
+                        if (mine && j * 4 + blk < nblk_live) {
+                            id = bt[j * 4 + blk];
+                            if (id < 0 || id >= p.num_blocks) {
+                                record_error(p.err, PA_DEVERR_BLOCK_ID_);
+                                id = -1;
+                            }
+                        }
+                        stage_blocks[li][s][blk] = id;
+                    }
+                };
+                auto issue = [&](int j, bool v) {
+                    const int J = kv0 + j;
+                    const int s = J % NS;
+                    if (J >= NS && !wait_or_abort(v ? &v_free[s] : &k_free[s], ((J - NS) / NS) & 1, abort_v))
+                        return false;
+                    if (!v) ids_of(j, s);
+                    uint32_t bytes = 0;
+                    for (int b = li; b < kBoxes; b += kTcLoaders)
+                        if (stage_blocks[li][s][b / kHalves] >= 0) bytes += 2048;
+                    uint64_t* bar = v ? &v_full[s] : &k_full[s];
+                    mbar_arrive_expect_tx(bar, bytes);
+                    uint8_t* dst = v ? vst(s) : kst(s);
+                    const CUtensorMap* map = v ? &vmap : &kmap;
+                    for (int b = li; b < kBoxes; b += kTcLoaders) {
+                        const int blk = b / kHalves, h = b % kHalves;
+                        const int id = stage_blocks[li][s][blk];
+                        if (id >= 0) tma_load_4d(dst + h * Sh::kKeyHalf + blk * 2048, map, bar, 0, h, g, id * 16);
+                    }
+                    if (v) ++v_total; else ++k_total;
+                    return true;
+                };
+                // the item's query tiles, once the previous item's MMAs are done
+                if (li == 0) {
+                    if (items > 0) ok = wait_or_abort(&item_done, (items - 1) & 1, abort_v);
+                    if (ok) {
+                        mbar_arrive_expect_tx(&q_full, static_cast<uint32_t>((nkx[1] ? 2 : 1) * Sh::kQ));
+#pragma unroll
+                        for (int x = 0; x < kTcTiles; ++x) {
+                            if (!nkx[x]) continue;
+#pragma unroll
+                            for (int h = 0; h < D / 64; ++h)
+                                tma_load_4d(qs(x) + h * Sh::kQHalf, &qmap, &q_full, 0, h, g * G, row0 + q0[x]);
+                        }
                     }
                 }
+                for (int j = 0; ok && j < nkt; ++j) ok = issue(j, false) && issue(j, true);
                 if (!ok) *abort_v = 1;
             }
+            __syncwarp();
         } else {
             // ========================== softmax rows ==========================
-            const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-            const int qi_row = q0 + tid / G;
-            const bool row_ok = tid < QT * G && qi_row < qlen;
-            const int pos_row = row_ok ? n - qlen + qi_row : pos_max;
-            float m_ref = -INFINITY, l_run = 0.f;
-            for (int j = 0; j < nkt; ++j) {
-                const int J = J0 + j;
-                const int s = J % ST;
-                // p_full counts one arrival per softmax warp per tile: a warp may
-                // start tile J only after every warp has arrived for tile J-2 (the
-                // previous use of the same barrier), or its arrival could be
-                // counted towards J-2; waiting for J-1 covers that.
-                bool got = (J == 0 || wait_or_abort(&p_full[(J - 1) & 1], ((J - 1) >> 1) & 1, abort_v)) &&
-                           wait_or_abort(&s_full[J & 1], (J >> 1) & 1, abort_v) &&
-                           wait_or_abort(&full_bar[s], (J / ST) & 1, abort_v);
-                if (!__all_sync(kFullMask, got)) {
-                    ok = false;
-                    break;
+            const int x = warp / kTcSoftmaxWarps;
+            const int wq = warp % kTcSoftmaxWarps;
+            const int r = wq * 32 + lane;                       // row = TMEM lane
+            const int nk = nkx[x];
+            if (nk > 0) {
+                const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+                const uint32_t o_tm = tmem + lane_base + static_cast<uint32_t>(256 + x * D);
+                const int qi_row = q0[x] + r / G;
+                const bool row_ok = r < QT * G && qi_row < qlen;
+                const int pos_row = row_ok ? n - qlen + qi_row : pos_hi[x];
+                // does the item's live table hold an id outside the pool?  (One
+                // scan per item keeps table loads off the per-tile path.)
+                bool any_bad = false;
+                for (int blk = lane; blk < nblk_live; blk += 32) {
+                    const int id = bt[blk];
+                    any_bad |= id < 0 || id >= p.num_blocks;
                 }
-                tc_fence_after_sync();
-                float sv[kTcKeys];
-                {
-                    uint32_t r[32];
-                    const uint32_t s_tm = tmem + lane_base + static_cast<uint32_t>((J & 1) * kTcKeys);
-                    tmem_ld32(s_tm, r);
-                    tmem_ld_wait();
+                any_bad = __any_sync(kFullMask, any_bad);
+                float m_ref = -INFINITY, l_run = 0.f;
+                for (int j = 0; j < nk; ++j) {
+                    const int Tx = t0[x] + j;
+                    const int J = kv0 + j;
+                    // blocks of this tile outside the pool (their keys are masked
+                    // and their V rows cleared), from the table as the producer saw it
+                    uint32_t bad = 0;
+                    if (any_bad) {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) sv[c] = __uint_as_float(r[c]);
-                    tmem_ld32(s_tm + 32, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) sv[32 + c] = __uint_as_float(r[c]);
-                }
-                const int key0 = j * kTcKeys;
-                const uint32_t bad = bad_mask[s];
-                const bool need_mask = (key0 + kTcKeys - 1 > pos_min) || bad;
-                float mx = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < kTcKeys; ++c) {
-                    float v = sv[c] * p.scale_log2;
-                    if (need_mask) {
-                        const bool dead = key0 + c > pos_row || ((bad >> (c >> 4)) & 1u);
-                        v = dead ? -INFINITY : v;
+                        for (int jb = 0; jb < 4; ++jb) {
+                            const int blk = j * 4 + jb;
+                            if (blk < nblk_live) {
+                                const int id = bt[blk];
+                                if (id < 0 || id >= p.num_blocks) bad |= 1u << jb;
+                            }
+                        }
                     }
-                    sv[c] = v;
-                    mx = fmaxf(mx, v);
-                }
-                // lazy rescale: move the reference only when the maximum has
-                // grown by more than 2^8 (warp-wide: tcgen05.ld/st are collective)
-                if (__any_sync(kFullMask, mx > m_ref + kRescaleLog2)) {
-                    const float new_ref = fmaxf(m_ref, mx);
-                    const float alpha = new_ref == -INFINITY ? 1.f : fast_exp2(m_ref - new_ref);
-                    if (j > 0) {
-                        got = wait_or_abort(&o_done, (J - 1) & 1, abort_v);
+                    // p_full counts one arrival per warp per tile: a warp may start
+                    // tile T only after every warp of its group has arrived for
+                    // T-2 (the previous use of the barrier); waiting for T-1 covers it
+                    bool got = (Tx == 0 ||
+                                wait_or_abort(&p_full[x][(Tx - 1) & 1], ((Tx - 1) >> 1) & 1, abort_v)) &&
+                               wait_or_abort(&s_full[x][Tx & 1], (Tx >> 1) & 1, abort_v);
+                    if (!__all_sync(kFullMask, got)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t s_tm =
+                        tmem + lane_base + static_cast<uint32_t>(x * 128 + (Tx & 1) * kTcKeys);
+                    float sv[kTcKeys];
+                    {
+                        uint32_t rr[32];
+                        tmem_ld32(s_tm, rr);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) sv[c] = __uint_as_float(rr[c]);
+                        tmem_ld32(s_tm + 32, rr);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) sv[32 + c] = __uint_as_float(rr[c]);
+                    }
+                    const int key0 = j * kTcKeys;
+                    const bool need_mask = (key0 + kTcKeys - 1 > pos_lo[x]) || bad;
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < kTcKeys; ++c) {
+                        float v = sv[c] * p.scale_log2;
+                        if (need_mask) {
+                            const bool dead = key0 + c > pos_row || ((bad >> (c >> 4)) & 1u);
+                            v = dead ? -INFINITY : v;
+                        }
+                        sv[c] = v;
+                        mx = fmaxf(mx, v);
+                    }
+                    // lazy rescale: move the reference only when the maximum has
+                    // grown by more than 2^8 (warp-wide: tcgen05.ld/st are collective)
+                    if (__any_sync(kFullMask, mx > m_ref + kRescaleLog2)) {
+                        const float new_ref = fmaxf(m_ref, mx);
+                        const float alpha = new_ref == -INFINITY ? 1.f : fast_exp2(m_ref - new_ref);
+                        if (j > 0) {
+                            got = wait_or_abort(&o_done[x][(Tx - 1) & 1], ((Tx - 1) >> 1) & 1, abort_v);
+                            if (!__all_sync(kFullMask, got)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after_sync();
+#pragma unroll
+                            for (int c0 = 0; c0 < D / 32; ++c0) {
+                                uint32_t rr[32];
+                                tmem_ld32(o_tm + static_cast<uint32_t>(c0 * 32), rr);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int u = 0; u < 32; ++u) rr[u] = __float_as_uint(__uint_as_float(rr[u]) * alpha);
+                                tmem_st32(o_tm + static_cast<uint32_t>(c0 * 32), rr);
+                            }
+                            tmem_st_wait();
+                        }
+                        l_run *= alpha;
+                        m_ref = new_ref;
+                    }
+                    const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+                    float rs = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kTcKeys; ++c) {
+                        const float e = fast_exp2(sv[c] - ref);
+                        sv[c] = e;
+                        rs += e;
+                    }
+                    l_run += rs;
+                    {
+                        // P row -> tensor memory over this row's S: two 16-bit
+                        // values per 32-bit column, keys in order
+                        uint32_t pw[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) pw[c] = Elem<T>::pack(sv[2 * c], sv[2 * c + 1]);
+                        tmem_st32(s_tm, pw);
+                    }
+                    // V rows that must contribute nothing (past the pair's last
+                    // query position, or in a block outside the pool) may hold
+                    // anything, NaN included: the first tile of the pair that
+                    // reads this key tile clears them before its P V (the other
+                    // tile's P V is issued after it)
+                    const bool clearer = x == 0 || j >= nkx[0];
+                    if (clearer && (j == nkt - 1 || bad)) {
+                        got = wait_or_abort(&v_full[J % NS], (J / NS) & 1, abort_v);
                         if (!__all_sync(kFullMask, got)) {
                             ok = false;
                             break;
                         }
+                        constexpr int CPR = D / 8;
+                        uint8_t* vt = vst(J % NS);
+                        for (int idx = r; idx < kTcKeys * CPR; idx += kTcSoftmaxWarps * 32) {
+                            const int key = idx / CPR;
+                            const int c = idx - key * CPR;
+                            if (key0 + key > pos_pair || ((bad >> (key >> 4)) & 1u))
+                                *reinterpret_cast<uint4*>(vt + (c >> 3) * Sh::kKeyHalf + key * 128 +
+                                                          (((c & 7) ^ (key & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    tmem_st_wait();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[x][Tx & 1]);
+                }
+                if (ok) {
+                    const int Tl = t0[x] + nk - 1;
+                    const bool got = wait_or_abort(&o_done[x][Tl & 1], (Tl >> 1) & 1, abort_v);
+                    if (__all_sync(kFullMask, got)) {
                         tc_fence_after_sync();
+                        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                        const int64_t grow =
+                            static_cast<int64_t>(row0 + qi_row) * p.num_q_heads + g * G + (r % G);
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + grow * D);
 #pragma unroll
                         for (int c0 = 0; c0 < D / 32; ++c0) {
-                            uint32_t r[32];
-                            tmem_ld32(o_tm + lane_base + static_cast<uint32_t>(c0 * 32), r);
+                            uint32_t rr[32];
+                            tmem_ld32(o_tm + static_cast<uint32_t>(c0 * 32), rr);
                             tmem_ld_wait();
+                            if (row_ok) {
 #pragma unroll
-                            for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * alpha);
-                            tmem_st32(o_tm + lane_base + static_cast<uint32_t>(c0 * 32), r);
-                        }
-                        tmem_st_wait();
-                    }
-                    l_run *= alpha;
-                    m_ref = new_ref;
-                }
-                const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-                float rs = 0.f;
-#pragma unroll
-                for (int c = 0; c < kTcKeys; ++c) {
-                    const float e = fast_exp2(sv[c] - ref);
-                    sv[c] = e;
-                    rs += e;
-                }
-                l_run += rs;
-                {
-                    // P row -> shared memory: K-major, 128-byte swizzled, 128 B per row
-                    uint8_t* prow = pst(s) + tid * 128;
-#pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        uint4 v4;
-                        v4.x = Elem<T>::pack(sv[8 * c8 + 0], sv[8 * c8 + 1]);
-                        v4.y = Elem<T>::pack(sv[8 * c8 + 2], sv[8 * c8 + 3]);
-                        v4.z = Elem<T>::pack(sv[8 * c8 + 4], sv[8 * c8 + 5]);
-                        v4.w = Elem<T>::pack(sv[8 * c8 + 6], sv[8 * c8 + 7]);
-                        *reinterpret_cast<uint4*>(prow + ((c8 ^ (tid & 7)) << 4)) = v4;
-                    }
-                }
-                if (j == nkt - 1 || bad) {
-                    // V rows that must contribute nothing (past the tile's last
-                    // query position, or in a block with an invalid table entry)
-                    // may hold anything, NaN included: clear them.
-                    constexpr int CPR = D / 8;
-                    for (int idx = tid; idx < kTcKeys * CPR; idx += kTcSoftmaxWarps * 32) {
-                        const int key = idx / CPR;
-                        const int c = idx - key * CPR;
-                        if (key0 + key > pos_max || ((bad >> (key >> 4)) & 1u))
-                            *reinterpret_cast<uint4*>(vst(s) + (c >> 3) * Sh::kKeyHalf + key * 128 +
-                                                      (((c & 7) ^ (key & 7)) << 4)) = make_uint4(0, 0, 0, 0);
-                    }
-                }
-                fence_proxy_async_smem();
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[J & 1]);
-            }
-            if (ok) {
-                const bool got = wait_or_abort(&o_done, (J0 + nkt - 1) & 1, abort_v);
-                if (__all_sync(kFullMask, got)) {
-                    tc_fence_after_sync();
-                    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-                    const int64_t grow = static_cast<int64_t>(row0 + qi_row) * p.num_q_heads + g * G + (tid % G);
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + grow * D);
-#pragma unroll
-                    for (int c0 = 0; c0 < D / 32; ++c0) {
-                        uint32_t r[32];
-                        tmem_ld32(o_tm + lane_base + static_cast<uint32_t>(c0 * 32), r);
-                        tmem_ld_wait();
-                        if (row_ok) {
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                uint4 v4;
-                                v4.x = Elem<T>::pack(__uint_as_float(r[8 * c + 0]) * inv,
-                                                     __uint_as_float(r[8 * c + 1]) * inv);
-                                v4.y = Elem<T>::pack(__uint_as_float(r[8 * c + 2]) * inv,
-                                                     __uint_as_float(r[8 * c + 3]) * inv);
-                                v4.z = Elem<T>::pack(__uint_as_float(r[8 * c + 4]) * inv,
-                                                     __uint_as_float(r[8 * c + 5]) * inv);
-                                v4.w = Elem<T>::pack(__uint_as_float(r[8 * c + 6]) * inv,
-                                                     __uint_as_float(r[8 * c + 7]) * inv);
-                                dst[c0 * 4 + c] = v4;
+                                for (int c = 0; c < 4; ++c) {
+                                    uint4 v4;
+                                    v4.x = Elem<T>::pack(__uint_as_float(rr[8 * c + 0]) * inv,
+                                                         __uint_as_float(rr[8 * c + 1]) * inv);
+                                    v4.y = Elem<T>::pack(__uint_as_float(rr[8 * c + 2]) * inv,
+                                                         __uint_as_float(rr[8 * c + 3]) * inv);
+                                    v4.z = Elem<T>::pack(__uint_as_float(rr[8 * c + 4]) * inv,
+                                                         __uint_as_float(rr[8 * c + 5]) * inv);
+                                    v4.w = Elem<T>::pack(__uint_as_float(rr[8 * c + 6]) * inv,
+                                                         __uint_as_float(rr[8 * c + 7]) * inv);
+                                    dst[c0 * 4 + c] = v4;
+                                }
                             }
                         }
+                        tc_fence_before_sync();
+                    } else {
+                        ok = false;
                     }
-                    tc_fence_before_sync();
-                } else {
-                    ok = false;
                 }
             }
             if (!ok) *abort_v = 1;
         }
-        J0 += nkt;
+        kv0 += nkt;
+        t0[0] += nkx[0];
+        t0[1] += nkx[1];
+        ++items;
         if (*abort_v) ok = false;
     }
 
     if (!ok || *abort_v) {
         if (tid == 0) record_error(p.err, PA_DEVERR_TIMEOUT_);
-        if (warp == kTcSoftmaxWarps && lane == 0) {
-            // let work still in flight finish before the CTA's memory is reused
-            if (s_issued) (void)mbar_wait(&s_full[(s_issued - 1) & 1], ((s_issued - 1) >> 1) & 1);
-            if (pv_issued) (void)mbar_wait(&o_done, (pv_issued - 1) & 1);
-            for (int t = kv_seen; t < kv_issued; ++t) (void)mbar_wait(&full_bar[t % ST], (t / ST) & 1);
+        if (warp == kTcMmaWarp && lane == 0) {
+            // let MMAs still in flight finish before the CTA's memory is reused
+#pragma unroll
+            for (int x = 0; x < kTcTiles; ++x) {
+                if (s_issued[x])
+                    (void)mbar_wait(&s_full[x][(s_issued[x] - 1) & 1], ((s_issued[x] - 1) >> 1) & 1);
+                if (pv_issued[x]) {
+                    const int Tl = pv_issued[x] - 1;
+                    (void)mbar_wait(&o_done[x][Tl & 1], (Tl >> 1) & 1);
+                }
+            }
+        }
+        if (warp > kTcMmaWarp && lane == 0) {
+            // and this loader's copies: each stage's last issued phase
+            for (int t = max(0, k_total - NS); t < k_total; ++t) (void)mbar_wait(&k_full[t % NS], (t / NS) & 1);
+            for (int t = max(0, v_total - NS); t < v_total; ++t) (void)mbar_wait(&v_full[t % NS], (t / NS) & 1);
         }
     }
     tc_fence_before_sync();
@@ -495,24 +642,24 @@ int sm_count() {
     return count[dev];
 }
 
-template <typename T, int D, int ST>
+template <typename T, int D>
 cudaError_t launch_t(const PrefillParams& p, int32_t* plan, const CUtensorMap& kmap, const CUtensorMap& vmap,
                      const CUtensorMap& qmap, int max_q_len, int num_tokens, cudaStream_t s) {
-    constexpr int smem = TcShape<D, ST>::kSmem;
-    auto kern = prefill_tc_kernel<T, D, ST>;
+    constexpr int smem = TcShape<D>::kSmem;
+    auto kern = prefill_tc_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     prefill_plan_kernel<<<1, 1024, 0, s>>>(p.cu_q_lens, p.num_seqs, p.q_per_tile, plan);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // upper bound on the work items: each listed chunk (length > 8) has at
-    // most ceil(len / q_per_tile) <= len / 2 tiles, and there are at most max_q_len
-    // tokens per chunk
+    // most ceil(len / q_per_tile) <= len / 2 tiles, and there are at most
+    // max_q_len tokens per chunk; an item is a pair of tiles.  One CTA per SM.
     const long long bound_tiles = std::min<long long>(static_cast<long long>(num_tokens) / 2 + 1,
                                                       static_cast<long long>(p.num_seqs) *
                                                           ((max_q_len + p.q_per_tile - 1) / p.q_per_tile));
-    const long long items = bound_tiles * p.num_kv_heads;
-    const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(items, 2LL * sm_count())));
+    const long long items = (bound_tiles + p.num_seqs) / kTcTiles * p.num_kv_heads + p.num_kv_heads;
+    const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(items, sm_count())));
     kern<<<grid, kTcThreads, smem, s>>>(p, plan, kmap, vmap, qmap);
     return cudaGetLastError();
 }
@@ -524,10 +671,10 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int32_t* plan, const CUten
                               int max_q_len, int num_tokens, cudaStream_t s) {
     if (p.num_seqs == 0 || max_q_len <= PA_VERIFY_MAX_Q_) return cudaSuccess;
     if (dtype == 0)
-        return head_dim == 128 ? launch_t<__half, 128, 2>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s)
-                               : launch_t<__half, 64, 2>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s);
-    return head_dim == 128 ? launch_t<__nv_bfloat16, 128, 2>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s)
-                           : launch_t<__nv_bfloat16, 64, 2>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s);
+        return head_dim == 128 ? launch_t<__half, 128>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s)
+                               : launch_t<__half, 64>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s);
+    return head_dim == 128 ? launch_t<__nv_bfloat16, 128>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s)
+                           : launch_t<__nv_bfloat16, 64>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s);
 }
 
 }  // namespace pa
