@@ -61,6 +61,27 @@ bool make_kv_map(CUtensorMap* map, const void* base, int num_blocks, int num_kv_
     return r == CUDA_SUCCESS;
 }
 
+// Tensor map over one pool whose box is a whole (16-token block, head) tile:
+// dims (64-element row piece, token slot, D/64 pieces, head) with strides
+// Hkv*D*2, 128 B and D*2 bytes; one box {64, 16, D/64, 1} lands as
+// [piece][token][128 B], 128-byte swizzled -- byte for byte what D/64 boxes
+// of make_kv_map would write, in one TMA operation.
+bool make_kv_map_block(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads, int head_dim,
+                       int dtype) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(num_blocks) * 16, static_cast<cuuint64_t>(head_dim / 64),
+                                static_cast<cuuint64_t>(num_kv_heads)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2, 128,
+                                   static_cast<cuuint64_t>(head_dim) * 2};
+    const cuuint32_t box[4] = {64, 16, static_cast<cuuint32_t>(head_dim / 64), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Tensor map over the query rows [T, Hq, D] viewed as 4-D (64-element row
 // piece, D/64 pieces, q head, token); one box = one 64-dim half of the `group`
 // heads of `q_per_tile` consecutive tokens, i.e. 128 rows of 128 bytes whose
@@ -241,8 +262,8 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
     CUtensorMap kmap, vmap;
     const bool maps_ok = fp8 ? make_kv_map_fp8(&kmap, k_cache, num_blocks, num_kv_heads) &&
                                    make_kv_map_fp8(&vmap, v_cache, num_blocks, num_kv_heads)
-                             : make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) &&
-                                   make_kv_map(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype);
+                             : make_kv_map_block(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) &&
+                                   make_kv_map_block(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype);
     if (!maps_ok) return PA_ERR_CUDA;
     pa::DecodeParams p{};
     p.out = out;

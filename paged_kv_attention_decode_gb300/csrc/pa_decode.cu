@@ -15,9 +15,10 @@
 //    warp, which handles the `group` query heads that share the kv head, so
 //    every K/V byte is read once and no CTA is launched without work.
 //  * each warp owns a private ring of STAGES shared-memory slots; its lane 0
-//    fetches whole (16-token block, kv head) tiles of K and V with 4-D TMA
-//    loads (one per 64-dim half, 128-byte swizzle), completing on a per-slot
-//    mbarrier, and keeps fetching ahead across the warp's items.
+//    fetches whole (16-token block, kv head) tiles of K and V with one 4-D
+//    TMA load each (both 64-dim halves, 128-byte swizzle: a TMA issue costs
+//    the issuing thread hundreds of cycles, so one box per tile), completing
+//    on a per-slot mbarrier, and keeps fetching ahead across the warp's items.
 //  * MHA (group 1): fp32 FMA dot products, a 16-way transpose-reduction
 //    across the warp (16 shuffles per block), register-resident (m, l, acc).
 //  * GQA (group 2..8): the query group x K-block product is a dense
@@ -76,12 +77,9 @@ __device__ __forceinline__ void issue_tile(const WarpRing& ring, int slot, int p
         tma_load_3d(dst, kmap, &ring.bars[slot], 0, kv_head, phys * 16);
         tma_load_3d(dst + Shape::kTileBytes, vmap, &ring.bars[slot], 0, kv_head, phys * 16);
     } else {
-#pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-            tma_load_4d(dst + h * TileGeom<D>::kHalfBytes, kmap, &ring.bars[slot], 0, h, kv_head, phys * 16);
-            tma_load_4d(dst + Shape::kTileBytes + h * TileGeom<D>::kHalfBytes, vmap, &ring.bars[slot], 0, h,
-                        kv_head, phys * 16);
-        }
+        // one box per tile: both 64-dim halves of the 16 rows (block tensor map)
+        tma_load_4d(dst, kmap, &ring.bars[slot], 0, phys * 16, 0, kv_head);
+        tma_load_4d(dst + Shape::kTileBytes, vmap, &ring.bars[slot], 0, phys * 16, 0, kv_head);
     }
 }
 
