@@ -122,6 +122,15 @@ bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) 
 size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
 
 constexpr int kMaxGrid = 65535;
+// Share of the SMs the tcgen05 prefill keeps while decode rows run beside it.
+#ifndef PA_OVERLAP_NUM
+#define PA_OVERLAP_NUM 1
+#endif
+#ifndef PA_OVERLAP_DEN
+#define PA_OVERLAP_DEN 4
+#endif
+constexpr int kOverlapPrefillNum = PA_OVERLAP_NUM;
+constexpr int kOverlapPrefillDen = PA_OVERLAP_DEN;
 constexpr int kMaxPoolBlocks = (1 << 27) - 1;  // token-row coordinate stays below 2^31
 
 int check_shape(int num_q_heads, int num_kv_heads, int head_dim, int block_size, int dtype, int num_blocks) {
@@ -245,12 +254,20 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, in
     return decode_ws_bytes(num_seqs, num_seqs, num_q_heads, head_dim, parts_for(max_seq_len, part));
 }
 
-static int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
-                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
-                       const int32_t* cu_q_lens, int num_seqs, int max_seq_len, int num_blocks, float scale,
-                       int num_q_heads, int num_kv_heads, int head_dim, int partition_size, void* workspace,
-                       size_t workspace_bytes, int dtype, cudaStream_t stream, int max_q, int max_rows,
-                       bool fp8 = false, float k_scale = 1.f, float v_scale = 1.f) {
+// Everything a decode launch needs, prepared and validated on the host.
+struct DecodeCall {
+    pa::DecodeParams p;
+    CUtensorMap kmap, vmap;
+    int head_dim, dtype;
+    bool fp8;
+};
+
+static int decode_prepare(DecodeCall& c, void* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                          const int32_t* cu_q_lens, int num_seqs, int max_seq_len, int num_blocks, float scale,
+                          int num_q_heads, int num_kv_heads, int head_dim, int partition_size, void* workspace,
+                          size_t workspace_bytes, int dtype, int max_q, int max_rows, bool fp8 = false,
+                          float k_scale = 1.f, float v_scale = 1.f) {
     const int part = partition_size ? partition_size : PA_DEFAULT_PARTITION;
     const int parts = parts_for(max_seq_len, part);
     if (parts > 65535) return PA_ERR_INVALID_ARG;   // partition index is a 16-bit field of the work list
@@ -259,13 +276,13 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
     if (!aligned256(workspace)) return PA_ERR_INVALID_ARG;
     unsigned int* err = error_word();
     if (!err) return PA_ERR_CUDA;
-    CUtensorMap kmap, vmap;
-    const bool maps_ok = fp8 ? make_kv_map_fp8(&kmap, k_cache, num_blocks, num_kv_heads) &&
-                                   make_kv_map_fp8(&vmap, v_cache, num_blocks, num_kv_heads)
-                             : make_kv_map_block(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) &&
-                                   make_kv_map_block(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype);
+    const bool maps_ok = fp8 ? make_kv_map_fp8(&c.kmap, k_cache, num_blocks, num_kv_heads) &&
+                                   make_kv_map_fp8(&c.vmap, v_cache, num_blocks, num_kv_heads)
+                             : make_kv_map_block(&c.kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) &&
+                                   make_kv_map_block(&c.vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype);
     if (!maps_ok) return PA_ERR_CUDA;
-    pa::DecodeParams p{};
+    pa::DecodeParams& p = c.p;
+    p = pa::DecodeParams{};
     p.out = out;
     p.q = q;
     p.block_tables = block_tables;
@@ -291,9 +308,30 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
     p.scale_log2 = scale_log2(scale) * k_scale;
     p.v_scale = v_scale;
     carve_workspace(p, workspace);
-    cudaError_t e = fp8 ? pa::launch_decode_fp8(p, kmap, vmap, dtype, stream)
-                        : pa::launch_decode(p, kmap, vmap, head_dim, dtype, stream);
+    c.head_dim = head_dim;
+    c.dtype = dtype;
+    c.fp8 = fp8;
+    return PA_OK;
+}
+
+static int decode_launch(const DecodeCall& c, cudaStream_t stream) {
+    cudaError_t e = c.fp8 ? pa::launch_decode_fp8(c.p, c.kmap, c.vmap, c.dtype, stream)
+                          : pa::launch_decode(c.p, c.kmap, c.vmap, c.head_dim, c.dtype, stream);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+static int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                       const int32_t* cu_q_lens, int num_seqs, int max_seq_len, int num_blocks, float scale,
+                       int num_q_heads, int num_kv_heads, int head_dim, int partition_size, void* workspace,
+                       size_t workspace_bytes, int dtype, cudaStream_t stream, int max_q, int max_rows,
+                       bool fp8 = false, float k_scale = 1.f, float v_scale = 1.f) {
+    DecodeCall c;
+    const int rc = decode_prepare(c, out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens,
+                                  num_seqs, max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim,
+                                  partition_size, workspace, workspace_bytes, dtype, max_q, max_rows, fp8, k_scale,
+                                  v_scale);
+    return rc ? rc : decode_launch(c, stream);
 }
 
 int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -389,20 +427,19 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
         return PA_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned256(workspace)) return PA_ERR_INVALID_ARG;
     int32_t* plan = static_cast<int32_t*>(workspace);
+    const int group = num_q_heads / num_kv_heads;
+    const bool tc = group == 1 || group == 2 || group == 4 || group == 8;
     // decode rows (q_len == 1) and speculative-verify rows (q_len <= PA_VERIFY_MAX_Q)
     // through the decode kernel
     const int max_q = std::max(1, std::min(max_q_len, PA_VERIFY_MAX_Q));
-    rc = decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens, num_seqs,
-                     max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, 0,
-                     static_cast<uint8_t*>(workspace) + pb, workspace_bytes - pb, dtype, s, max_q,
-                     verify_rows_bound(num_seqs, num_tokens));
+    DecodeCall dc;
+    rc = decode_prepare(dc, out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens, num_seqs,
+                        max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, 0,
+                        static_cast<uint8_t*>(workspace) + pb, workspace_bytes - pb, dtype, max_q,
+                        verify_rows_bound(num_seqs, num_tokens));
     if (rc) return rc;
-    if (max_q_len <= PA_VERIFY_MAX_Q) return PA_OK;
+    if (max_q_len <= PA_VERIFY_MAX_Q) return decode_launch(dc, s);
     unsigned int* err = error_word();
-    CUtensorMap kmap, vmap;
-    if (!make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) ||
-        !make_kv_map(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype))
-        return PA_ERR_CUDA;
     pa::PrefillParams p{};
     p.out = out;
     p.q = q;
@@ -416,21 +453,36 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
     p.num_blocks = num_blocks;
     p.num_q_heads = num_q_heads;
     p.num_kv_heads = num_kv_heads;
-    p.group = num_q_heads / num_kv_heads;
+    p.group = group;
     p.scale_log2 = scale_log2(scale);
+    CUtensorMap kmap, vmap;
     cudaError_t e;
-    if (p.group == 1 || p.group == 2 || p.group == 4 || p.group == 8) {
-        // 128-row tiles on the tcgen05 tensor cores
-        p.q_per_tile = 128 / p.group;
-        CUtensorMap qmap;
-        if (!make_q_map(&qmap, q, num_tokens, num_q_heads, head_dim, p.group, p.q_per_tile, dtype))
+    if (tc) {
+        // 128-row tiles on the tcgen05 tensor cores, running beside the decode
+        // rows: the decode plan and the prefill kernel go first; the decode
+        // kernel then starts on the SMs the prefill kernel leaves free
+        if (!make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) ||
+            !make_kv_map(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype))
             return PA_ERR_CUDA;
+        p.q_per_tile = 128 / group;
+        CUtensorMap qmap;
+        if (!make_q_map(&qmap, q, num_tokens, num_q_heads, head_dim, group, p.q_per_tile, dtype)) return PA_ERR_CUDA;
+        if (pa::launch_decode_plan(dc.p, s) != cudaSuccess) return PA_ERR_CUDA;
+        p.decode_units = dc.p.unit_count;
+        p.overlap_ctas = std::max(1, pa::sm_count() * kOverlapPrefillNum / kOverlapPrefillDen);
         e = pa::launch_prefill_tc(p, plan, kmap, vmap, qmap, head_dim, dtype, max_q_len, num_tokens, s);
-    } else {
-        // other groupings: 64-row mma.sync tiles
-        p.q_per_tile = 64 / p.group;
-        e = pa::launch_prefill(p, kmap, vmap, head_dim, dtype, max_q_len, s);
+        if (e != cudaSuccess) return PA_ERR_CUDA;
+        dc.p.overlap = 1;
+        return decode_launch(dc, s);
     }
+    // other groupings: 64-row mma.sync tiles after the decode rows
+    rc = decode_launch(dc, s);
+    if (rc) return rc;
+    if (!make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) ||
+        !make_kv_map(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype))
+        return PA_ERR_CUDA;
+    p.q_per_tile = 64 / group;
+    e = pa::launch_prefill(p, kmap, vmap, head_dim, dtype, max_q_len, s);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

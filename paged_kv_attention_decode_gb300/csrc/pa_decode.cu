@@ -534,7 +534,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
     __syncwarp();
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
-    pdl_wait();  // the work list (and, through it, the KV write) is complete
+    // the work list (and, through it, the KV write) is complete; with
+    // p.overlap the preceding kernel is a prefill kernel this one runs beside,
+    // and the list was built before that kernel started
+    if (!p.overlap) pdl_wait();
     const int total = *p.unit_count * H * C;
     if (total == 0) return;
     int* queue = claimed[warp];
@@ -1007,17 +1010,6 @@ __global__ void __launch_bounds__(D) decode_reduce_cta_kernel(const DecodeParams
     }
 }
 
-int sm_count() {
-    static int count[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (!count[dev]) {
-        int c = 0;
-        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 148;
-        count[dev] = c;
-    }
-    return count[dev];
-}
 
 template <typename T, int D, bool kMma, bool kFp8 = false, int kMaxNT = 1>
 cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -1026,8 +1018,10 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, cons
     auto kern = decode_kernel<T, D, kMma, kFp8, kMaxNT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, s, p);
-    if (e != cudaSuccess) return e;
+    if (!p.overlap) {
+        e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, s, p);
+        if (e != cudaSuccess) return e;
+    }
     // persistent: as many CTAs as fit on every SM (shared memory bound), fewer
     // when there cannot be that many items
     constexpr int kCtasPerSm = (228 * 1024) / (smem + 2048);
@@ -1055,6 +1049,24 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, cons
 }
 
 }  // namespace
+
+int sm_count() {
+    static int count[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!count[dev]) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 148;
+        count[dev] = c;
+    }
+    return count[dev];
+}
+
+cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t s) {
+    if (p.num_seqs == 0) return cudaSuccess;
+    decode_plan_kernel<<<1, 1024, 0, s>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_decode_fp8(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                               int dtype, cudaStream_t s) {

@@ -70,6 +70,11 @@ struct DecodeParams {
     int col_chunks;               // 32-column chunks of (query, head) pairs per (unit, kv head)
     float scale_log2;             // scale * log2(e) (times the K dequantisation scale for FP8)
     float v_scale;                // V dequantisation scale (1 for 16-bit caches)
+    // 1: the plan kernel has already run (launched on its own) and the decode
+    // kernel is launched right after a prefill kernel that allows dependent
+    // launch; everything the decode kernel reads completed before that
+    // prefill kernel started, so it does not wait for it
+    int overlap;
 };
 
 struct PrefillParams {
@@ -88,6 +93,10 @@ struct PrefillParams {
     int group;
     int q_per_tile;               // queries per CTA tile (rows = q_per_tile * group <= 64)
     float scale_log2;
+    // when *decode_units > 0 (decode rows will run next to this kernel), only
+    // the first overlap_ctas CTAs take prefill work; the others leave their SMs
+    const int32_t* decode_units;
+    int overlap_ctas;
 };
 
 // Launchers (return cudaError_t of the launch).
@@ -99,6 +108,9 @@ cudaError_t launch_kv_write(const void* key, const void* value, void* k_cache, v
                             int head_dim, unsigned int* err, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           int head_dim, int dtype, cudaStream_t s);
+// The work-list plan alone (for p.overlap launches, which skip it).
+cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t s);
+int sm_count();
 // FP8 (E4M3) cache, head_dim 128; q/out of `dtype`.
 cudaError_t launch_decode_fp8(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                               int dtype, cudaStream_t s);

@@ -158,8 +158,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int lane = tid & 31;
     const int G = p.group;
     const int QT = p.q_per_tile;  // 128 / G
+    // a decode kernel launched after this one may start now (it reads
+    // nothing this kernel writes); when it has work, only overlap_ctas CTAs
+    // stay, so that it gets the other SMs
+    pdl_trigger();
+    int ctas = static_cast<int>(gridDim.x);
+    if (p.decode_units && *p.decode_units > 0) ctas = min(ctas, p.overlap_ctas);
     const int total_items = plan[p.num_seqs] * p.num_kv_heads;
-    if (static_cast<int>(blockIdx.x) >= total_items) return;
+    if (static_cast<int>(blockIdx.x) >= total_items || static_cast<int>(blockIdx.x) >= ctas) return;
 
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int s_issued[kTcTiles] = {0, 0}, pv_issued[kTcTiles] = {0, 0};
     int k_total = 0, v_total = 0;   // loader: K and V tiles issued so far (ring order)
 
-    for (int w0 = blockIdx.x; ok && w0 < total_items; w0 += gridDim.x) {
+    for (int w0 = blockIdx.x; ok && w0 < total_items; w0 += ctas) {
         // ---- decode the work item -------------------------------------------
         const int w = w0;
         const int g = w % p.num_kv_heads;
@@ -630,17 +636,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
-int sm_count() {
-    static int count[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (!count[dev]) {
-        int c = 0;
-        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 148;
-        count[dev] = c;
-    }
-    return count[dev];
-}
 
 template <typename T, int D>
 cudaError_t launch_t(const PrefillParams& p, int32_t* plan, const CUtensorMap& kmap, const CUtensorMap& vmap,

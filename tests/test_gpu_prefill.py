@@ -79,3 +79,29 @@ def test_long_chunks_many_tiles_per_cta():
     rows, ref = oracle_rows(w, seqs, snap, q_rows_per_seq=pick)
     err = max_err(out[torch.from_numpy(rows).to(DEV)], ref)
     assert err <= TOL["bf16"], err
+
+
+def test_call_completes_in_stream_order():
+    """The prefill kernel and the decode kernel run side by side inside one
+    call; work queued after the call on the same stream, with no device
+    synchronisation, must see every row of both."""
+    w = W.make("mixed", device=DEV, n_prefill=3, chunk=1536, n_decode=64, prefix_hi=3000)
+    bt = torch.from_numpy(w.block_tables).to(DEV)
+    sl = torch.from_numpy(w.seq_lens).to(DEV)
+    cu = torch.from_numpy(w.cu_q_lens).to(DEV)
+    seqs = np.arange(w.batch)
+    snap = snapshot(w, seqs)
+    slots = pa.slot_mapping(bt, sl, cu, w.num_tokens, w.num_blocks)
+    pa.paged_kv_write(w.key, w.value, w.k_cache, w.v_cache, slots)
+    out = torch.full_like(w.q, float("nan"))
+    pa.paged_attention_prefill(w.q, w.k_cache, w.v_cache, bt, sl, cu, w.scale, w.max_q_len, w.max_seq_len, out=out)
+    copy = out.clone()          # same stream, queued right behind the call
+    torch.cuda.synchronize()
+    assert pa.device_error() == 0
+    assert torch.equal(copy.view(torch.int16), out.view(torch.int16))
+
+    def pick(b, ql):
+        return [0] if ql == 1 else [0, 1, ql // 2, ql - 1]
+
+    rows, ref = oracle_rows(w, seqs, snap, q_rows_per_seq=pick)
+    assert max_err(copy[torch.from_numpy(rows).to(DEV)], ref) <= TOL["bf16"]
