@@ -261,13 +261,26 @@ struct MmaState {
         {
             const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
             const int dsub = ((lane >> 4) & 1) * 8;
+            // two independent accumulation chains (even and odd k-steps)
+            float c2[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) c2[nt][e] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
                 uint32_t a[4];
                 ldsm_x4(ka + tile_off<D>(tok, kk * 16 + dsub), a[0], a[1], a[2], a[3]);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) Mma<T>::run(c[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (kk & 1) Mma<T>::run(c2[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
+                    else Mma<T>::run(c[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
+                }
             }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) c[nt][e] += c2[nt][e];
         }
         const int r0 = lane >> 2;
         float s[NT][4];
@@ -516,6 +529,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bars[kDecodeWarps * kDecodeStages];
     __shared__ int claimed[kDecodeWarps][kQueue];
+    __shared__ uint8_t slot_ok[kDecodeWarps][kDecodeStages];   // the slot's block id was inside the pool
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -640,8 +654,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
     auto issue_next = [&]() {
         if (!fvalid) return;
         const int slot = static_cast<int>(kf % kDecodeStages);
-        const int phys = fi.bt[fblk];
         if (lane == 0) {
+            const int phys = fi.bt[fblk];
+            slot_ok[warp][slot] = phys >= 0 && phys < p.num_blocks;
             if (phys >= 0 && phys < p.num_blocks) {
                 issue_tile<D, kFp8, kMma, kMaxNT>(ring, slot, phys, fi.g, &kmap, &vmap);
             } else {
@@ -665,8 +680,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
             const int slot = static_cast<int>(kc % kDecodeStages);
             const bool got = mbar_wait(&ring.bars[slot], (kc / kDecodeStages) & 1u);
             if (__any_sync(kFull, !got)) return false;
-            const int phys = it.bt[blk];
-            if (phys >= 0 && phys < p.num_blocks) {
+            const bool valid = slot_ok[warp][slot];   // written by lane 0 before the slot's TMA
+            if (valid) {
                 uint8_t* kt = ring.base + slot * Shape::kStageBytes;
                 uint8_t* vt = kt + Shape::kTileBytes;
                 const int base = (it.blk0 + blk) * 16;
