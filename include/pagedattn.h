@@ -203,8 +203,12 @@ size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_q_heads,
  *   max_q_len, max_seq_len  host-side upper bounds (grid sizing, routing).
  *   workspace     >= pa_prefill_workspace_bytes(num_seqs, num_tokens, ...) bytes,
  *                 256-byte aligned.
- * A chunk longer than its seq_len, or a decode/verify chunk longer than
- * max_q_len, sets PA_DEVERR_SEQ_LEN and gets zero rows.
+ * Errors on the device set PA_DEVERR_SEQ_LEN: a decode/verify chunk longer
+ * than its seq_len or than max_q_len gets zero rows; a longer chunk that
+ * exceeds its seq_len is left unwritten.
+ * The call only enqueues work on `stream` (the prefill and decode kernels may
+ * run side by side inside it); work queued after it on the same stream sees
+ * every output row.
  */
 int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* block_tables, int max_blocks_per_seq,

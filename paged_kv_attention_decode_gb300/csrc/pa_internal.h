@@ -53,7 +53,7 @@ struct DecodeParams {
     int32_t* work_counter;        // next work item to claim (reset by the plan kernel)
     int32_t* row_base;            // [B] first partials row of a split sequence
     int32_t* rows;                // [max_rows] (sequence << 3 | query index) of every partials row
-    int32_t* row_count;           // number of entries in `rows`
+    int32_t* row_count;           // number of entries in `rows` (header of the workspace)
     unsigned int* err;            // device error word
     int num_seqs;
     int max_blocks;
@@ -67,7 +67,7 @@ struct DecodeParams {
     int max_parts;                // ceil(max_seq_len / partition_tokens)
     int max_q;                    // largest chunk handled here (1..PA_VERIFY_MAX_Q_)
     int max_rows;                 // partials rows available in the workspace
-    int col_chunks;               // 32-column chunks of (query, head) pairs per (unit, kv head)
+    int col_chunks;               // chunks of 8 or 16 (query, head) columns per (unit, kv head)
     float scale_log2;             // scale * log2(e) (times the K dequantisation scale for FP8)
     float v_scale;                // V dequantisation scale (1 for 16-bit caches)
     // 1: the plan kernel has already run (launched on its own) and the decode
@@ -91,7 +91,7 @@ struct PrefillParams {
     int num_q_heads;
     int num_kv_heads;
     int group;
-    int q_per_tile;               // queries per CTA tile (rows = q_per_tile * group <= 64)
+    int q_per_tile;               // queries per tile: rows = q_per_tile * group (128 tcgen05, 64 mma.sync)
     float scale_log2;
     // when *decode_units > 0 (decode rows will run next to this kernel), only
     // the first overlap_ctas CTAs take prefill work; the others leave their SMs
@@ -128,7 +128,7 @@ cudaError_t launch_kv_gather(void* k_out, void* v_out, const void* k_cache, cons
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            int head_dim, int dtype, int max_q_len, cudaStream_t s);
 // tcgen05 prefill: groups of 1, 2, 4 or 8 q heads per kv head; q_per_tile = 128 / group.
-// `plan` is device scratch of num_seqs + 1 int32 (the tile work list).
+// `plan` is device scratch of num_seqs + 1 int32 (the work list of query-tile pairs).
 cudaError_t launch_prefill_tc(const PrefillParams& p, int32_t* plan, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, const CUtensorMap& qmap, int head_dim, int dtype,
                               int max_q_len, int num_tokens, cudaStream_t s);
