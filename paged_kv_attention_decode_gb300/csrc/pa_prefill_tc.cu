@@ -71,6 +71,34 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     return false;
 }
 
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// Paired fp32 arithmetic (one instruction for two values on sm_100 and
+// later), rounded to nearest like the scalar operations:
+// (x, y) <- (x * s, y * s), (x + a, y + b), (x * s + a, y * s + a).
+__device__ __forceinline__ void mul2(float& x, float& y, float s) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 b, {%2, %2};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(x), "+f"(y)
+        : "f"(s));
+}
+__device__ __forceinline__ void add2(float& x, float& y, float a, float b) {
+    asm("{\n\t.reg .b64 p, q, d;\n\tmov.b64 p, {%0, %1};\n\tmov.b64 q, {%2, %3};\n\t"
+        "add.rn.f32x2 d, p, q;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(x), "+f"(y)
+        : "f"(a), "f"(b));
+}
+__device__ __forceinline__ void fma2(float& x, float& y, float s, float a) {
+    asm("{\n\t.reg .b64 p, q, r, d;\n\tmov.b64 p, {%0, %1};\n\tmov.b64 q, {%2, %2};\n\t"
+        "mov.b64 r, {%3, %3};\n\tfma.rn.f32x2 d, p, q, r;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(x), "+f"(y)
+        : "f"(s), "f"(a));
+}
+
 // Work list of the chunked-prefill items: offsets[b] = number of query-tile
 // pairs (two 128-row tiles) of sequences 0..b-1 whose chunk is longer than
 // PA_VERIFY_MAX_Q_ tokens (shorter chunks are decode or speculative-verify
@@ -438,6 +466,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 any_bad = __any_sync(kFullMask, any_bad);
                 float m_ref = -INFINITY, l_run = 0.f;
+                const bool fold = p.scale_log2 > 0.f;   // scale folded into the exponent's FMA
                 for (int j = 0; j < nk; ++j) {
                     const int Tx = t0[x] + j;
                     const int J = kv0 + j;
@@ -469,29 +498,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tmem + lane_base + static_cast<uint32_t>(x * 128 + (Tx & 1) * kTcKeys);
                     float sv[kTcKeys];
                     {
-                        uint32_t rr[32];
-                        tmem_ld32(s_tm, rr);
+                        // both halves of the row in flight before one wait
+                        uint32_t r0[32], r1[32];
+                        tmem_ld32(s_tm, r0);
+                        tmem_ld32(s_tm + 32, r1);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) sv[c] = __uint_as_float(rr[c]);
-                        tmem_ld32(s_tm + 32, rr);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) sv[32 + c] = __uint_as_float(rr[c]);
+                        for (int c = 0; c < 32; ++c) {
+                            sv[c] = __uint_as_float(r0[c]);
+                            sv[32 + c] = __uint_as_float(r1[c]);
+                        }
                     }
                     const int key0 = j * kTcKeys;
                     const bool need_mask = (key0 + kTcKeys - 1 > pos_lo[x]) || bad;
-                    float mx = -INFINITY;
+                    // A positive scale is applied after the row maximum (the
+                    // maximum of the scaled scores is the scaled maximum, as
+                    // rounding is monotonic), fused with the subtraction below.
+                    if (!fold) {
 #pragma unroll
-                    for (int c = 0; c < kTcKeys; ++c) {
-                        float v = sv[c] * p.scale_log2;
-                        if (need_mask) {
-                            const bool dead = key0 + c > pos_row || ((bad >> (c >> 4)) & 1u);
-                            v = dead ? -INFINITY : v;
-                        }
-                        sv[c] = v;
-                        mx = fmaxf(mx, v);
+                        for (int c = 0; c < kTcKeys; c += 2) mul2(sv[c], sv[c + 1], p.scale_log2);
                     }
+                    if (need_mask) {
+#pragma unroll
+                        for (int c = 0; c < kTcKeys; ++c) {
+                            const bool dead = key0 + c > pos_row || ((bad >> (c >> 4)) & 1u);
+                            sv[c] = dead ? -INFINITY : sv[c];
+                        }
+                    }
+                    float mx;
+                    {
+                        // four independent chains of three-input maxima
+                        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                        for (int c = 0; c < kTcKeys; c += 8) {
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) mq[u] = fmax3(mq[u], sv[c + 2 * u], sv[c + 2 * u + 1]);
+                        }
+                        mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
+                    }
+                    if (fold) mx *= p.scale_log2;
                     // lazy rescale: move the reference only when the maximum has
                     // grown by more than 2^8 (warp-wide: tcgen05.ld/st are collective)
                     if (__any_sync(kFullMask, mx > m_ref + kRescaleLog2)) {
@@ -519,14 +564,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         m_ref = new_ref;
                     }
                     const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-                    float rs = 0.f;
+                    if (fold) {
 #pragma unroll
-                    for (int c = 0; c < kTcKeys; ++c) {
-                        const float e = fast_exp2(sv[c] - ref);
-                        sv[c] = e;
-                        rs += e;
+                        for (int c = 0; c < kTcKeys; c += 2) fma2(sv[c], sv[c + 1], p.scale_log2, -ref);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < kTcKeys; c += 2) add2(sv[c], sv[c + 1], -ref, -ref);
                     }
-                    l_run += rs;
+#pragma unroll
+                    for (int c = 0; c < kTcKeys; ++c) sv[c] = fast_exp2(sv[c]);
+                    {
+                        float sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int c = 0; c < kTcKeys; c += 4) {
+                            add2(sq[0], sq[1], sv[c], sv[c + 1]);
+                            add2(sq[2], sq[3], sv[c + 2], sv[c + 3]);
+                        }
+                        l_run += (sq[0] + sq[1]) + (sq[2] + sq[3]);
+                    }
                     {
                         // P row -> tensor memory over this row's S: two 16-bit
                         // values per 32-bit column, keys in order

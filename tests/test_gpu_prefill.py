@@ -34,6 +34,25 @@ def test_prefill_parity(Hq, Hkv, D, dtype):
     assert pa.device_error() == 0
 
 
+@pytest.mark.parametrize("scale", [-0.09, 0.0, 3.0])
+def test_prefill_any_scale(scale):
+    """Scale is any finite number: negative (the softmax favours the smallest
+    scores), zero (uniform weights over the visible keys) and large; the
+    tensor-core kernel takes a different softmax path for non-positive scales."""
+    q_lens = [c[0] for c in CASES]
+    seq_lens = [c[0] + c[1] for c in CASES]
+    w = W.build_workload(name="pre_scale", seq_lens=seq_lens, q_lens=q_lens, num_q_heads=8, num_kv_heads=2,
+                         head_dim=128, dtype="bf16", seed=91, device=DEV, poison=True, pool_slack=0.2, scale=scale)
+    assert w.scale == scale
+    seqs = np.arange(w.batch)
+    snap = snapshot(w, seqs)
+    _, out = gpu_step(w, prefill=True)
+    rows, ref = oracle_rows(w, seqs, snap)
+    err = max_err(out[torch.from_numpy(rows).to(DEV)], ref)
+    assert err <= TOL["bf16"], err
+    assert pa.device_error() == 0
+
+
 def test_mixed_step_small():
     w = W.make("mixed", device=DEV, poison=True, n_prefill=3, chunk=150, n_decode=40, prefix_hi=700,
                dec_lo=1, dec_hi=900)
