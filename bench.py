@@ -40,6 +40,17 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s): the measured burst figure (a cuBLAS
+    GEMM timed alone), else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -210,7 +221,11 @@ def cpu_baseline(w, seconds: float = 10.0) -> dict:
 def _workload_kw(args) -> dict:
     if not args.batch:
         return {}
-    return {"n_decode": args.batch} if args.workload == "mixed" else {"batch": args.batch}
+    if args.workload == "mixed":
+        return {"n_decode": args.batch}
+    if args.workload == "prefill":
+        return {"n_prefill": args.batch}
+    return {"batch": args.batch}
 
 
 def run_reference(args):
@@ -455,6 +470,15 @@ def run_ours(args):
     }
     if ab["kv"] != ab["kv_unique"]:
         line["roofline"]["logical_gbs"] = ab["total_logical"] / (attn_ms / 1e3) / 1e9
+    if not decode and int(w.q_lens.min()) > 8:
+        # chunked prefill only: the tcgen05 kernel is bound by the tensor pipe
+        tpeak, tkind = _tensor_peak()
+        fl = _prefill_flops(w)
+        tf = fl / (attn_ms / 1e3) / 1e12
+        line["roofline"] = {"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s", "frac": tf / tpeak,
+                            "traffic": None, "kernel": "prefill call (prefill plan + tcgen05 prefill kernel)",
+                            "peak_kind": f"{tkind} dense bf16 GEMM (burst)", "algorithmic_flops_per_launch": fl,
+                            "ms_per_launch": attn_ms}
     if not decode:
         line["prefill_gflop_per_step"] = _prefill_flops(w) / 1e9
     if ws == 1 and decode and not fp8 and not args.no_cpu_baseline:

@@ -7,24 +7,29 @@
 //
 // One persistent CTA per SM.  A work item is a pair of adjacent 128-row query
 // tiles, A and B (rows = (query, q head) pairs of one kv group; TMEM lane r =
-// row r), that share one stream of 64-key K/V tiles: every K/V byte loaded
+// row r), that share one stream of 128-key K/V tiles: every K/V byte loaded
 // feeds two tiles of MMAs.  Warp roles:
 //   * warps 0-3: softmax of tile A, warps 4-7: softmax of tile B (thread r of
 //     a group = row r);
 //   * warp 8, lane 0: every tcgen05.mma;
 //   * warps 9-11: the TMA loads (Q tiles; K and V tiles gathered block by
-//     block through the block table into separate rings of kStages stages).
-//     TMA issue is costly per SM sub-partition, so the boxes of a tile are
-//     split over three warps on three sub-partitions.
-// Tensor memory (512 columns): S_A[2] | S_B[2] (64 columns each) | O_A | O_B.
+//     block through the block table into a ring of K stages and a ring of V
+//     stages).  TMA issue is costly per issuing thread, so the boxes of a
+//     tile are split over three warps.
+// Tensor memory (512 columns): S_A | S_B (128 columns each) | O_A | O_B.
 // Per key tile j and query tile X:
-//   S_X(j) = Q_X K(j)^T   M=128 N=64 into S_X[j & 1], issued as soon as K(j)
-//                          has landed, so that it overlaps the softmax of j-1;
-//   softmax_X(j)          tcgen05.ld of the S row, running reference m_ref and
-//                          sum l; P (bf16/fp16) is stored over the row's S;
-//   O_X += P_X(j) V(j)    M=128 N=D K=64, A read from tensor memory.
-// While one tile's softmax runs, the tensor cores work on the other tile.
-// K(j)'s stage is refilled once both S(j) are done, V(j)'s once both P V are
+//   S_X(j) = Q_X K(j)^T   M=128 N=128, eight MMAs of K=16;
+//   softmax_X(j)          tcgen05.ld of the S row (two passes: maximum, then
+//                          exponentials), running reference m_ref and sum l;
+//                          P (bf16/fp16) is stored over the row's S;
+//   O_X += P_X(j) V(j)    M=128 N=D, eight MMAs of K=16, A read from tensor
+//                          memory.
+// A tcgen05.mma instruction of M=128 costs the tensor pipe about the same time
+// for any N up to 128, so 128-key tiles (N=128 for S) do twice the work per
+// instruction of 64-key ones.  S_X is single-buffered: S_X(j+1) is issued
+// once P_X(j) V(j) has completed (it overwrites P_X(j)), so while one tile's
+// softmax runs, the tensor pipe works on the other tile (ping-pong).  K(j)'s
+// stage is refilled once both S(j) are done, V(j)'s once both P V are
 // (k_free / v_free, committed by the MMA warp).
 // A row rescales O and l only when its maximum exceeds m_ref by more than 2^8
 // (so P <= 256).  Only tiles that cross the causal diagonal are masked; V rows
@@ -44,21 +49,24 @@ constexpr int kTcTiles = 2;                                          // query ti
 constexpr int kTcMmaWarp = kTcTiles * kTcSoftmaxWarps;                // warp 8
 constexpr int kTcLoaders = 3;                                        // warps 9-11
 constexpr int kTcThreads = (kTcMmaWarp + 1 + kTcLoaders) * 32;      // 384
-constexpr int kTcKeys = 64;
-constexpr uint32_t kTmemCols = 512;  // S_A[2] S_B[2] (64 each) | O_A | O_B
+constexpr int kTcKeys = 128;                                         // keys per K/V tile
+constexpr int kTcBlocks = kTcKeys / 16;                               // cache blocks per tile
+constexpr uint32_t kTmemCols = 512;  // S_A | S_B (128 each) | O_A | O_B
 constexpr float kRescaleLog2 = 8.f;
 constexpr unsigned kFullMask = 0xffffffffu;
 
 template <int D>
 struct TcShape {
-    static constexpr int kKeyHalf = kTcKeys * 128;          // 64 keys x one 64-dim half
+    static constexpr int kKeyHalf = kTcKeys * 128;          // 128 keys x one 64-dim half
     static constexpr int kKV = (D / 64) * kKeyHalf;         // K or V of one tile: [half][key][128 B]
     static constexpr int kQHalf = 128 * 128;                // 128 rows x one half
     static constexpr int kQ = (D / 64) * kQHalf;            // one query tile
     static constexpr int kBudget = 227 * 1024 - 1024;      // dynamic shared memory less alignment slack
-    static constexpr int kStagesFit = (kBudget - kTcTiles * kQ) / (2 * kKV);
-    static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;     // 5 at D = 128, 6 at D = 64
-    static constexpr int kSmem = kTcTiles * kQ + kStages * 2 * kKV + 1024;
+    static constexpr int kRingFit = (kBudget - kTcTiles * kQ) / kKV;   // K and V stages together
+    // K is needed one softmax earlier than V: the K ring gets the odd stage
+    static constexpr int kVStages = kRingFit / 2 > 4 ? 4 : kRingFit / 2;          // 2 at D = 128, 4 at D = 64
+    static constexpr int kKStages = kRingFit - kVStages > 4 ? 4 : kRingFit - kVStages;   // 3 at D = 128
+    static constexpr int kSmem = kTcTiles * kQ + (kKStages + kVStages) * kKV + 1024;
 };
 
 // Bounded mbarrier wait that also gives up when another thread of the CTA has
@@ -156,28 +164,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const __grid_constant__ CUtensorMap qmap) {
     using Sh = TcShape<D>;
-    constexpr int NS = Sh::kStages;
+    constexpr int NK = Sh::kKStages;
+    constexpr int NV = Sh::kVStages;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdescS = mma_idesc_f16(128, kTcKeys, kBf16, false);
     constexpr uint32_t kIdescPV = mma_idesc_f16(128, D, kBf16, true);
 
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t k_full[NS];               // K tile landed (one arrival per loader)
-    __shared__ uint64_t v_full[NS];               // V tile landed (one arrival per loader)
-    __shared__ uint64_t k_free[NS];               // every S of the stage's tile complete
-    __shared__ uint64_t v_free[NS];               // every P V of the stage's tile complete
+    __shared__ uint64_t k_full[NK];               // K tile landed (one arrival per loader)
+    __shared__ uint64_t v_full[NV];               // V tile landed (one arrival per loader)
+    __shared__ uint64_t k_free[NK];               // every S of the stage's tile complete
+    __shared__ uint64_t v_free[NV];               // every P V of the stage's tile complete
     __shared__ uint64_t q_full;                   // the item's query tiles landed
     __shared__ uint64_t item_done;                // every MMA of an item complete
-    __shared__ uint64_t s_full[kTcTiles][2];      // S_X(j) complete, by tile parity
-    __shared__ uint64_t p_full[kTcTiles][2];      // P_X(j) stored: one arrival per softmax warp, by parity
+    // S_X(j) complete (one phase per tile of X).  S_X(j+1) is issued only
+    // after P_X(j) V(j) completed, which needs the softmax of tile j, so the
+    // barrier never runs more than one phase ahead of a waiter.
+    __shared__ uint64_t s_full[kTcTiles];
+    // P_X(j) stored: one arrival per softmax warp.  A warp reaches tile j+1
+    // only after S_X(j+1), which the MMA warp issues after it saw this phase
+    // complete, so no warp arrives twice in one phase.
+    __shared__ uint64_t p_full[kTcTiles];
     // P_X(j) V(j) complete, by tile parity.  A parity wait is only sound when
-    // the barrier's previous phase is known complete: with one barrier per
-    // parity, waiting for P V(T) needs P V(T-2) done, which every waiter has
-    // (S(T) is issued only after it); one barrier would need P V(T-1), which
-    // may still run when the last tile's softmax ends.  A completed phase
-    // also means every earlier MMA completed (tcgen05.commit tracks all of them).
+    // the barrier's previous phase is known complete: waiting for P V(T)
+    // needs P V(T-2) done, which every waiter has (S(T) is issued only after
+    // P V(T-1) completed).  A completed phase also means every earlier MMA
+    // completed (tcgen05.commit tracks all of them).
     __shared__ uint64_t o_done[kTcTiles][2];
-    __shared__ int32_t stage_blocks[kTcLoaders][NS][4];   // each loader's record of its stages' block ids
+    __shared__ int32_t stage_blocks[kTcLoaders][NK][kTcBlocks];   // each loader's block ids per K stage
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -198,27 +212,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     auto qs = [&](int x) { return smem + x * Sh::kQ; };
-    auto kst = [&](int s) { return smem + kTcTiles * Sh::kQ + s * 2 * Sh::kKV; };
-    auto vst = [&](int s) { return smem + kTcTiles * Sh::kQ + s * 2 * Sh::kKV + Sh::kKV; };
+    auto kst = [&](int s) { return smem + kTcTiles * Sh::kQ + s * Sh::kKV; };
+    auto vst = [&](int s) { return smem + kTcTiles * Sh::kQ + (NK + s) * Sh::kKV; };
 
     if (warp == 0) {
         tmem_alloc(&tmem_slot, kTmemCols);
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < NK; ++s) {
             mbar_init(&k_full[s], kTcLoaders);
-            mbar_init(&v_full[s], kTcLoaders);
             mbar_init(&k_free[s], 1);
+        }
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(&v_full[s], kTcLoaders);
             mbar_init(&v_free[s], 1);
         }
         mbar_init(&q_full, 1);
         mbar_init(&item_done, 1);
         for (int x = 0; x < kTcTiles; ++x) {
-            mbar_init(&s_full[x][0], 1);
-            mbar_init(&s_full[x][1], 1);
-            mbar_init(&p_full[x][0], kTcSoftmaxWarps);
-            mbar_init(&p_full[x][1], kTcSoftmaxWarps);
+            mbar_init(&s_full[x], 1);
+            mbar_init(&p_full[x], kTcSoftmaxWarps);
             mbar_init(&o_done[x][0], 1);
             mbar_init(&o_done[x][1], 1);
         }
@@ -286,11 +300,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (warp == kTcMmaWarp) {
             // ============================ MMA issuer ============================
             auto issue_s = [&](int x, int j) {
-                const int Tx = t0[x] + j;
                 if (lane == 0) {
                     const uint32_t qa = smem_addr(qs(x));
-                    const uint32_t ka = smem_addr(kst((kv0 + j) % NS));
-                    const uint32_t d_tm = tmem + static_cast<uint32_t>(x * 128 + (Tx & 1) * kTcKeys);
+                    const uint32_t ka = smem_addr(kst((kv0 + j) % NK));
+                    const uint32_t d_tm = tmem + static_cast<uint32_t>(x * kTcKeys);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint64_t a = smem_desc_sw128(qa + (kk >> 2) * Sh::kQHalf + (kk & 3) * 32, 16, 1024);
@@ -298,19 +311,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             smem_desc_sw128(ka + (kk >> 2) * Sh::kKeyHalf + (kk & 3) * 32, 16, 1024);
                         tc_mma_f16(d_tm, a, bd, kIdescS, kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(&s_full[x][Tx & 1]);
+                    tc_commit(&s_full[x]);
                 }
                 __syncwarp();
                 ++s_issued[x];
             };
             // O_X += P_X(j) V(j): P is read from tensor memory, where the softmax
-            // stored it over the first 32 columns of S_X(j)
+            // stored it over the first 64 columns of S_X
             auto issue_pv = [&](int x, int j) {
                 const int Tx = t0[x] + j;
                 if (lane == 0) {
-                    const uint32_t p_tm = tmem + static_cast<uint32_t>(x * 128 + (Tx & 1) * kTcKeys);
-                    const uint32_t o_tm = tmem + static_cast<uint32_t>(256 + x * D);
-                    const uint32_t va = smem_addr(vst((kv0 + j) % NS));
+                    const uint32_t p_tm = tmem + static_cast<uint32_t>(x * kTcKeys);
+                    const uint32_t o_tm = tmem + static_cast<uint32_t>(kTcTiles * kTcKeys + x * D);
+                    const uint32_t va = smem_addr(vst((kv0 + j) % NV));
 #pragma unroll
                     for (int kp = 0; kp < kTcKeys / 16; ++kp) {
                         const uint64_t bd = smem_desc_sw128(va + kp * 2048, Sh::kKeyHalf, 1024);
@@ -329,51 +342,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             auto wait_all = [&](uint64_t* bar, uint32_t parity) {
                 return __all_sync(kFullMask, wait_or_abort(bar, parity, abort_v));
             };
-            auto wait_o = [&](int x, int Tx) { return wait_all(&o_done[x][Tx & 1], (Tx >> 1) & 1); };
 
             // the previous item's MMAs must be complete: its S/P buffers and
             // accumulators are reused
             if (items > 0) ok = wait_all(&item_done, (items - 1) & 1);
-            if (ok) ok = wait_all(&q_full, items & 1) && wait_all(&k_full[kv0 % NS], (kv0 / NS) & 1);
+            if (ok) ok = wait_all(&q_full, items & 1) && wait_all(&k_full[kv0 % NK], (kv0 / NK) & 1);
             if (ok) {
                 tc_fence_after_sync();
 #pragma unroll
                 for (int x = 0; x < kTcTiles; ++x)
                     if (nkx[x]) issue_s(x, 0);
-                commit(&k_free[kv0 % NS]);
+                commit(&k_free[kv0 % NK]);
             }
             for (int j = 0; ok && j < nkt; ++j) {
                 const int J = kv0 + j;
-                if (j + 1 < nkt) {
-                    // S(j+1) as soon as K(j+1) is in; S_X[(j+1) & 1] last held
-                    // P_X(j-1), so that P V has to be complete
-                    ok = wait_all(&k_full[(J + 1) % NS], ((J + 1) / NS) & 1);
-                    if (!ok) break;
-                    tc_fence_after_sync();
-#pragma unroll
-                    for (int x = 0; x < kTcTiles; ++x) {
-                        if (j + 1 >= nkx[x]) continue;
-                        if (j >= 1 && !(ok = wait_o(x, t0[x] + j - 1))) break;
-                        tc_fence_after_sync();
-                        issue_s(x, j + 1);
-                    }
-                    if (!ok) break;
-                    commit(&k_free[(J + 1) % NS]);   // K(j+1)'s stage, once both S are done
-                }
-                ok = wait_all(&v_full[J % NS], (J / NS) & 1);
+                ok = wait_all(&v_full[J % NV], (J / NV) & 1);
                 if (!ok) break;
-                // two barriers by tile parity: S_X(j+1) is already issued, so
-                // the softmax may finish tiles j and j+1 before this wait
+                bool k_next = false;   // K(j+1) seen landed
+                // per tile: P V(j) once its softmax stored P, then S(j+1) into
+                // the same columns once that P V has completed; the other
+                // tile's softmax runs meanwhile
 #pragma unroll
                 for (int x = 0; x < kTcTiles; ++x) {
                     if (j >= nkx[x]) continue;
                     const int Tx = t0[x] + j;
-                    if (!(ok = wait_all(&p_full[x][Tx & 1], (Tx >> 1) & 1))) break;
+                    if (!(ok = wait_all(&p_full[x], Tx & 1))) break;
                     tc_fence_after_sync();
                     issue_pv(x, j);
+                    if (j + 1 >= nkx[x]) continue;
+                    if (!k_next) {
+                        if (!(ok = wait_all(&k_full[(J + 1) % NK], ((J + 1) / NK) & 1))) break;
+                        k_next = true;
+                    }
+                    if (!(ok = wait_all(&o_done[x][Tx & 1], (Tx >> 1) & 1))) break;
+                    tc_fence_after_sync();
+                    issue_s(x, j + 1);
                 }
                 if (!ok) break;
-                commit(&v_free[J % NS]);   // V(j)'s stage, once both P V are done
+                commit(&v_free[J % NV]);                          // V(j)'s stage, once both P V are done
+                if (j + 1 < nkt) commit(&k_free[(J + 1) % NK]);   // K(j+1)'s, once both S are done
             }
             if (ok) commit(&item_done);
             if (!ok && lane == 0) *abort_v = 1;
@@ -386,42 +393,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // k_free / v_free for the stage's previous tile is awaited.
             const int li = warp - kTcMmaWarp - 1;
             constexpr int kHalves = D / 64;
-            constexpr int kBoxes = 4 * kHalves;
+            constexpr int kBoxes = kTcBlocks * kHalves;
             if (lane == 0) {
-                auto ids_of = [&](int j, int s) {
+                auto ids_of = [&](int j, int sk) {
                     // this loader's blocks of tile j, recorded for the V issue
 #pragma unroll
-                    for (int blk = 0; blk < 4; ++blk) {
+                    for (int blk = 0; blk < kTcBlocks; ++blk) {
                         bool mine = false;
 #pragma unroll
                         for (int h = 0; h < kHalves; ++h) mine |= (blk * kHalves + h) % kTcLoaders == li;
                         int id = -1;
-                        if (mine && j * 4 + blk < nblk_live) {
-                            id = bt[j * 4 + blk];
+                        if (mine && j * kTcBlocks + blk < nblk_live) {
+                            id = bt[j * kTcBlocks + blk];
                             if (id < 0 || id >= p.num_blocks) {
                                 record_error(p.err, PA_DEVERR_BLOCK_ID_);
                                 id = -1;
                             }
                         }
-                        stage_blocks[li][s][blk] = id;
+                        stage_blocks[li][sk][blk] = id;
                     }
                 };
                 auto issue = [&](int j, bool v) {
                     const int J = kv0 + j;
-                    const int s = J % NS;
-                    if (J >= NS && !wait_or_abort(v ? &v_free[s] : &k_free[s], ((J - NS) / NS) & 1, abort_v))
+                    const int N = v ? NV : NK;
+                    const int s = J % N;
+                    if (J >= N && !wait_or_abort(v ? &v_free[s] : &k_free[s], ((J - N) / N) & 1, abort_v))
                         return false;
-                    if (!v) ids_of(j, s);
+                    // K(J) is issued before V(J), and K(J + NK) after it: the
+                    // K stage's record still holds tile J's ids for the V issue
+                    const int sk = J % NK;
+                    if (!v) ids_of(j, sk);
                     uint32_t bytes = 0;
                     for (int b = li; b < kBoxes; b += kTcLoaders)
-                        if (stage_blocks[li][s][b / kHalves] >= 0) bytes += 2048;
+                        if (stage_blocks[li][sk][b / kHalves] >= 0) bytes += 2048;
                     uint64_t* bar = v ? &v_full[s] : &k_full[s];
                     mbar_arrive_expect_tx(bar, bytes);
                     uint8_t* dst = v ? vst(s) : kst(s);
                     const CUtensorMap* map = v ? &vmap : &kmap;
                     for (int b = li; b < kBoxes; b += kTcLoaders) {
                         const int blk = b / kHalves, h = b % kHalves;
-                        const int id = stage_blocks[li][s][blk];
+                        const int id = stage_blocks[li][sk][blk];
                         if (id >= 0) tma_load_4d(dst + h * Sh::kKeyHalf + blk * 2048, map, bar, 0, h, g, id * 16);
                     }
                     if (v) ++v_total; else ++k_total;
@@ -453,7 +464,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int nk = nkx[x];
             if (nk > 0) {
                 const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-                const uint32_t o_tm = tmem + lane_base + static_cast<uint32_t>(256 + x * D);
+                const uint32_t s_tm = tmem + lane_base + static_cast<uint32_t>(x * kTcKeys);
+                const uint32_t o_tm = tmem + lane_base + static_cast<uint32_t>(kTcTiles * kTcKeys + x * D);
                 const int qi_row = q0[x] + r / G;
                 const bool row_ok = r < QT * G && qi_row < qlen;
                 const int pos_row = row_ok ? n - qlen + qi_row : pos_hi[x];
@@ -475,80 +487,72 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     uint32_t bad = 0;
                     if (any_bad) {
 #pragma unroll
-                        for (int jb = 0; jb < 4; ++jb) {
-                            const int blk = j * 4 + jb;
+                        for (int jb = 0; jb < kTcBlocks; ++jb) {
+                            const int blk = j * kTcBlocks + jb;
                             if (blk < nblk_live) {
                                 const int id = bt[blk];
                                 if (id < 0 || id >= p.num_blocks) bad |= 1u << jb;
                             }
                         }
                     }
-                    // p_full counts one arrival per warp per tile: a warp may start
-                    // tile T only after every warp of its group has arrived for
-                    // T-2 (the previous use of the barrier); waiting for T-1 covers it
-                    bool got = (Tx == 0 ||
-                                wait_or_abort(&p_full[x][(Tx - 1) & 1], ((Tx - 1) >> 1) & 1, abort_v)) &&
-                               wait_or_abort(&s_full[x][Tx & 1], (Tx >> 1) & 1, abort_v);
-                    if (!__all_sync(kFullMask, got)) {
+                    if (!__all_sync(kFullMask, wait_or_abort(&s_full[x], Tx & 1, abort_v))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t s_tm =
-                        tmem + lane_base + static_cast<uint32_t>(x * 128 + (Tx & 1) * kTcKeys);
-                    float sv[kTcKeys];
-                    {
-                        // both halves of the row in flight before one wait
+                    const int key0 = j * kTcKeys;
+                    // Scores of keys c0 .. c0 + 63 of the row: a positive scale
+                    // is applied after the row maximum (the maximum of the
+                    // scaled scores is the scaled maximum, as rounding is
+                    // monotonic), fused with the subtraction of the exponent.
+                    auto load64 = [&](int c0, float (&sv)[64]) {
                         uint32_t r0[32], r1[32];
-                        tmem_ld32(s_tm, r0);
-                        tmem_ld32(s_tm + 32, r1);
+                        tmem_ld32(s_tm + static_cast<uint32_t>(c0), r0);
+                        tmem_ld32(s_tm + static_cast<uint32_t>(c0 + 32), r1);
                         tmem_ld_wait();
 #pragma unroll
                         for (int c = 0; c < 32; ++c) {
                             sv[c] = __uint_as_float(r0[c]);
                             sv[32 + c] = __uint_as_float(r1[c]);
                         }
-                    }
-                    const int key0 = j * kTcKeys;
-                    const bool need_mask = (key0 + kTcKeys - 1 > pos_lo[x]) || bad;
-                    // A positive scale is applied after the row maximum (the
-                    // maximum of the scaled scores is the scaled maximum, as
-                    // rounding is monotonic), fused with the subtraction below.
-                    if (!fold) {
+                        if (!fold) {
 #pragma unroll
-                        for (int c = 0; c < kTcKeys; c += 2) mul2(sv[c], sv[c + 1], p.scale_log2);
-                    }
-                    if (need_mask) {
-#pragma unroll
-                        for (int c = 0; c < kTcKeys; ++c) {
-                            const bool dead = key0 + c > pos_row || ((bad >> (c >> 4)) & 1u);
-                            sv[c] = dead ? -INFINITY : sv[c];
+                            for (int c = 0; c < 64; c += 2) mul2(sv[c], sv[c + 1], p.scale_log2);
                         }
-                    }
+                        const bool need_mask = (key0 + c0 + 63 > pos_lo[x]) || ((bad >> (c0 >> 4)) & 0xfu);
+                        if (need_mask) {
+#pragma unroll
+                            for (int c = 0; c < 64; ++c) {
+                                const bool dead = key0 + c0 + c > pos_row || ((bad >> ((c0 + c) >> 4)) & 1u);
+                                sv[c] = dead ? -INFINITY : sv[c];
+                            }
+                        }
+                    };
+                    // pass 1: the row maximum (four chains of three-input maxima)
                     float mx;
                     {
-                        // four independent chains of three-input maxima
                         float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+                        for (int hh = 0; hh < kTcKeys / 64; ++hh) {
+                            float sv[64];
+                            load64(hh * 64, sv);
 #pragma unroll
-                        for (int c = 0; c < kTcKeys; c += 8) {
+                            for (int c = 0; c < 64; c += 8) {
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) mq[u] = fmax3(mq[u], sv[c + 2 * u], sv[c + 2 * u + 1]);
+                                for (int u = 0; u < 4; ++u) mq[u] = fmax3(mq[u], sv[c + 2 * u], sv[c + 2 * u + 1]);
+                            }
                         }
                         mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
+                        if (fold) mx *= p.scale_log2;
                     }
-                    if (fold) mx *= p.scale_log2;
                     // lazy rescale: move the reference only when the maximum has
-                    // grown by more than 2^8 (warp-wide: tcgen05.ld/st are collective)
+                    // grown by more than 2^8 (warp-wide: tcgen05.ld/st are
+                    // collective).  P V(j-1) is complete (S(j) was issued after
+                    // it), so O can be rescaled in place.
                     if (__any_sync(kFullMask, mx > m_ref + kRescaleLog2)) {
                         const float new_ref = fmaxf(m_ref, mx);
                         const float alpha = new_ref == -INFINITY ? 1.f : fast_exp2(m_ref - new_ref);
                         if (j > 0) {
-                            got = wait_or_abort(&o_done[x][(Tx - 1) & 1], ((Tx - 1) >> 1) & 1, abort_v);
-                            if (!__all_sync(kFullMask, got)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after_sync();
 #pragma unroll
                             for (int c0 = 0; c0 < D / 32; ++c0) {
                                 uint32_t rr[32];
@@ -563,33 +567,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         l_run *= alpha;
                         m_ref = new_ref;
                     }
+                    // pass 2: P = 2^(s - m_ref) and its sum; keys c0 .. c0 + 63
+                    // go to the 32 columns c0 / 2 .. c0 / 2 + 31 (two 16-bit
+                    // values per column, keys in order), which hold scores this
+                    // pass has already read
                     const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-                    if (fold) {
+                    float sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                    for (int hh = 0; hh < kTcKeys / 64; ++hh) {
+                        float sv[64];
+                        load64(hh * 64, sv);
+                        if (fold) {
 #pragma unroll
-                        for (int c = 0; c < kTcKeys; c += 2) fma2(sv[c], sv[c + 1], p.scale_log2, -ref);
-                    } else {
+                            for (int c = 0; c < 64; c += 2) fma2(sv[c], sv[c + 1], p.scale_log2, -ref);
+                        } else {
 #pragma unroll
-                        for (int c = 0; c < kTcKeys; c += 2) add2(sv[c], sv[c + 1], -ref, -ref);
-                    }
+                            for (int c = 0; c < 64; c += 2) add2(sv[c], sv[c + 1], -ref, -ref);
+                        }
 #pragma unroll
-                    for (int c = 0; c < kTcKeys; ++c) sv[c] = fast_exp2(sv[c]);
-                    {
-                        float sq[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int c = 0; c < 64; ++c) sv[c] = fast_exp2(sv[c]);
 #pragma unroll
-                        for (int c = 0; c < kTcKeys; c += 4) {
+                        for (int c = 0; c < 64; c += 4) {
                             add2(sq[0], sq[1], sv[c], sv[c + 1]);
                             add2(sq[2], sq[3], sv[c + 2], sv[c + 3]);
                         }
-                        l_run += (sq[0] + sq[1]) + (sq[2] + sq[3]);
-                    }
-                    {
-                        // P row -> tensor memory over this row's S: two 16-bit
-                        // values per 32-bit column, keys in order
                         uint32_t pw[32];
 #pragma unroll
                         for (int c = 0; c < 32; ++c) pw[c] = Elem<T>::pack(sv[2 * c], sv[2 * c + 1]);
-                        tmem_st32(s_tm, pw);
+                        tmem_st32(s_tm + static_cast<uint32_t>(hh * 32), pw);
                     }
+                    l_run += (sq[0] + sq[1]) + (sq[2] + sq[3]);
                     // V rows that must contribute nothing (past the pair's last
                     // query position, or in a block outside the pool) may hold
                     // anything, NaN included: the first tile of the pair that
@@ -597,13 +604,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // tile's P V is issued after it)
                     const bool clearer = x == 0 || j >= nkx[0];
                     if (clearer && (j == nkt - 1 || bad)) {
-                        got = wait_or_abort(&v_full[J % NS], (J / NS) & 1, abort_v);
-                        if (!__all_sync(kFullMask, got)) {
+                        if (!__all_sync(kFullMask, wait_or_abort(&v_full[J % NV], (J / NV) & 1, abort_v))) {
                             ok = false;
                             break;
                         }
                         constexpr int CPR = D / 8;
-                        uint8_t* vt = vst(J % NS);
+                        uint8_t* vt = vst(J % NV);
                         for (int idx = r; idx < kTcKeys * CPR; idx += kTcSoftmaxWarps * 32) {
                             const int key = idx / CPR;
                             const int c = idx - key * CPR;
@@ -616,7 +622,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tmem_st_wait();
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&p_full[x][Tx & 1]);
+                    if (lane == 0) mbar_arrive(&p_full[x]);
                 }
                 if (ok) {
                     const int Tl = t0[x] + nk - 1;
@@ -669,8 +675,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // let MMAs still in flight finish before the CTA's memory is reused
 #pragma unroll
             for (int x = 0; x < kTcTiles; ++x) {
-                if (s_issued[x])
-                    (void)mbar_wait(&s_full[x][(s_issued[x] - 1) & 1], ((s_issued[x] - 1) >> 1) & 1);
+                if (s_issued[x]) (void)mbar_wait(&s_full[x], (s_issued[x] - 1) & 1);
                 if (pv_issued[x]) {
                     const int Tl = pv_issued[x] - 1;
                     (void)mbar_wait(&o_done[x][Tl & 1], (Tl >> 1) & 1);
@@ -679,8 +684,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (warp > kTcMmaWarp && lane == 0) {
             // and this loader's copies: each stage's last issued phase
-            for (int t = max(0, k_total - NS); t < k_total; ++t) (void)mbar_wait(&k_full[t % NS], (t / NS) & 1);
-            for (int t = max(0, v_total - NS); t < v_total; ++t) (void)mbar_wait(&v_full[t % NS], (t / NS) & 1);
+            for (int t = max(0, k_total - NK); t < k_total; ++t) (void)mbar_wait(&k_full[t % NK], (t / NK) & 1);
+            for (int t = max(0, v_total - NV); t < v_total; ++t) (void)mbar_wait(&v_full[t % NV], (t / NV) & 1);
         }
     }
     tc_fence_before_sync();

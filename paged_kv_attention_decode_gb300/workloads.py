@@ -409,6 +409,16 @@ def config_mixed(device="cpu", n_prefill=4, chunk=1536, n_decode=2048,
                           device=device, **kw)
 
 
+def config_prefill(device="cpu", n_prefill=16, chunk=1536, prefix_hi=4096, **kw) -> Workload:
+    """Chunked prefill on its own: ``n_prefill`` chunks of ``chunk`` tokens on
+    cached prefixes U[0, prefix_hi] (the mixed step's chunk length and prefix
+    distribution; its first four prefixes are the mixed step's), no decode
+    rows.  16 chunks read about 0.24 GB of cache per step, more than L2."""
+    w = config_mixed(device=device, n_prefill=n_prefill, chunk=chunk, n_decode=0, prefix_hi=prefix_hi, **kw)
+    w.name = "prefill"
+    return w
+
+
 def config_llama7b_decode_fp8(device="cpu", batch=64, lo=512, hi=4096, **kw) -> Workload:
     """The LLaMA-2-7B-shaped decode workload with an FP8 (E4M3) cache."""
     seed = _seed(1)
@@ -441,6 +451,7 @@ CONFIGS = {
     "llama7b_ctx4096": config_llama7b_ctx4096,
     "llama7b_decode_fp8": config_llama7b_decode_fp8,
     "spec_verify": config_spec_verify,
+    "prefill": config_prefill,
 }
 
 
