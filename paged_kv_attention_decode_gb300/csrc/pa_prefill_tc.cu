@@ -49,6 +49,14 @@ constexpr int kTcTiles = 2;                                          // query ti
 constexpr int kTcMmaWarp = kTcTiles * kTcSoftmaxWarps;                // warp 8
 constexpr int kTcLoaders = 3;                                        // warps 9-11
 constexpr int kTcThreads = (kTcMmaWarp + 1 + kTcLoaders) * 32;      // 384
+// Registers per thread: 168 at launch (65536 / 384, in steps of 8); the MMA
+// and loader warpgroup gives up all but kTcOtherRegs, and the two softmax
+// warpgroups take them (a whole row of 128 fp32 scores stays in registers).
+constexpr int kTcLaunchRegs = 168;
+constexpr int kTcOtherRegs = 56;
+constexpr int kTcSoftmaxRegs = (kTcLaunchRegs * kTcThreads - kTcOtherRegs * (kTcThreads - 256)) / 256 / 8 * 8;   // 224
+static_assert(kTcSoftmaxRegs * 256 + kTcOtherRegs * (kTcThreads - 256) <= kTcLaunchRegs * kTcThreads,
+              "the warpgroups' registers must fit the launch pool");
 constexpr int kTcKeys = 128;                                         // keys per K/V tile
 constexpr int kTcBlocks = kTcKeys / 16;                               // cache blocks per tile
 constexpr uint32_t kTmemCols = 512;  // S_A | S_B (128 each) | O_A | O_B
@@ -68,6 +76,18 @@ struct TcShape {
     static constexpr int kKStages = kRingFit - kVStages > 4 ? 4 : kRingFit - kVStages;   // 3 at D = 128
     static constexpr int kSmem = kTcTiles * kQ + (kKStages + kVStages) * kKV + 1024;
 };
+
+// Per-warpgroup register budgets (every warp of the warpgroup executes the
+// same call).  An increase waits until the CTA's pool (its threads x the
+// registers per thread it was launched with) has the registers free.
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
 
 // Bounded mbarrier wait that also gives up when another thread of the CTA has
 // already recorded a failure.
@@ -245,20 +265,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = tmem_slot;
     volatile int* abort_v = &abort_flag;
 
-    // running counters (identical in every role): key tiles loaded so far (the
-    // ring position), tiles processed so far per query-tile slot, items so far
-    int kv0 = 0;
-    int t0[kTcTiles] = {0, 0};
-    int items = 0;
-    bool ok = true;
-    // MMA warp bookkeeping for the abort path
-    int s_issued[kTcTiles] = {0, 0}, pv_issued[kTcTiles] = {0, 0};
-    int k_total = 0, v_total = 0;   // loader: K and V tiles issued so far (ring order)
-
-    for (int w0 = blockIdx.x; ok && w0 < total_items; w0 += ctas) {
-        // ---- decode the work item -------------------------------------------
-        const int w = w0;
-        const int g = w % p.num_kv_heads;
+    // Work item w: (tile pair, kv head) of the plan; within a sequence the
+    // pairs nearest the end (the longest key ranges) come first.  Query
+    // tiles A (x = 0) and B (x = 1, absent past the chunk's last tile).
+    struct Item {
+        int g, row0, qlen, n, nkt, pos_pair, nblk_live;
+        int q0[kTcTiles], nkx[kTcTiles], pos_lo[kTcTiles], pos_hi[kTcTiles];
+        const int32_t* bt;
+    };
+    // false when the sequence is malformed: every role skips the item
+    auto decode_item = [&](int w, Item& it) -> bool {
+        it.g = w % p.num_kv_heads;
         const int l = w / p.num_kv_heads;
         int lo = 0, hi = p.num_seqs - 1;  // last b with plan[b] <= l
         while (lo < hi) {
@@ -266,221 +283,86 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (plan[mid] <= l) lo = mid; else hi = mid - 1;
         }
         const int b = lo;
-        const int row0 = p.cu_q_lens[b];
-        const int qlen = p.cu_q_lens[b + 1] - row0;
-        const int ntiles = (qlen + QT - 1) / QT;
+        it.row0 = p.cu_q_lens[b];
+        it.qlen = p.cu_q_lens[b + 1] - it.row0;
+        const int ntiles = (it.qlen + QT - 1) / QT;
         const int npairs = (ntiles + kTcTiles - 1) / kTcTiles;
         const int pr = npairs - 1 - (l - plan[b]);
-        const int n = p.seq_lens[b];
-        if (n < qlen || n > p.max_seq_len || n > p.max_blocks * 16) {
-            if (pr == npairs - 1 && g == 0 && tid == 0) record_error(p.err, PA_DEVERR_SEQ_LEN_);
-            continue;
+        it.n = p.seq_lens[b];
+        if (it.n < it.qlen || it.n > p.max_seq_len || it.n > p.max_blocks * 16) {
+            if (pr == npairs - 1 && it.g == 0 && tid == 0) record_error(p.err, PA_DEVERR_SEQ_LEN_);
+            return false;
         }
-        // query tiles A (x = 0) and B (x = 1, absent past the chunk's last tile)
-        int q0[kTcTiles], nkx[kTcTiles], pos_lo[kTcTiles], pos_hi[kTcTiles];
 #pragma unroll
         for (int x = 0; x < kTcTiles; ++x) {
             const int qt = pr * kTcTiles + x;
-            q0[x] = qt * QT;
+            it.q0[x] = qt * QT;
             if (qt < ntiles) {
-                const int q_last = min(qlen, q0[x] + QT) - 1;
-                pos_lo[x] = n - qlen + q0[x];
-                pos_hi[x] = n - qlen + q_last;
-                nkx[x] = (pos_hi[x] + kTcKeys) / kTcKeys;
+                const int q_last = min(it.qlen, it.q0[x] + QT) - 1;
+                it.pos_lo[x] = it.n - it.qlen + it.q0[x];
+                it.pos_hi[x] = it.n - it.qlen + q_last;
+                it.nkx[x] = (it.pos_hi[x] + kTcKeys) / kTcKeys;
             } else {
-                pos_lo[x] = pos_hi[x] = 0;
-                nkx[x] = 0;
+                it.pos_lo[x] = it.pos_hi[x] = 0;
+                it.nkx[x] = 0;
             }
         }
-        const int nkt = max(nkx[0], nkx[1]);                 // key tiles of the pair
-        const int pos_pair = nkx[1] ? pos_hi[1] : pos_hi[0];  // the pair's last query position
-        const int nblk_live = (pos_pair + 16) >> 4;
-        const int32_t* bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
+        it.nkt = max(it.nkx[0], it.nkx[1]);                          // key tiles of the pair
+        it.pos_pair = it.nkx[1] ? it.pos_hi[1] : it.pos_hi[0];      // the pair's last query position
+        it.nblk_live = (it.pos_pair + 16) >> 4;
+        it.bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
+        return true;
+    };
 
-        if (warp == kTcMmaWarp) {
-            // ============================ MMA issuer ============================
-            auto issue_s = [&](int x, int j) {
-                if (lane == 0) {
-                    const uint32_t qa = smem_addr(qs(x));
-                    const uint32_t ka = smem_addr(kst((kv0 + j) % NK));
-                    const uint32_t d_tm = tmem + static_cast<uint32_t>(x * kTcKeys);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t a = smem_desc_sw128(qa + (kk >> 2) * Sh::kQHalf + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd =
-                            smem_desc_sw128(ka + (kk >> 2) * Sh::kKeyHalf + (kk & 3) * 32, 16, 1024);
-                        tc_mma_f16(d_tm, a, bd, kIdescS, kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit(&s_full[x]);
-                }
-                __syncwarp();
-                ++s_issued[x];
-            };
-            // O_X += P_X(j) V(j): P is read from tensor memory, where the softmax
-            // stored it over the first 64 columns of S_X
-            auto issue_pv = [&](int x, int j) {
-                const int Tx = t0[x] + j;
-                if (lane == 0) {
-                    const uint32_t p_tm = tmem + static_cast<uint32_t>(x * kTcKeys);
-                    const uint32_t o_tm = tmem + static_cast<uint32_t>(kTcTiles * kTcKeys + x * D);
-                    const uint32_t va = smem_addr(vst((kv0 + j) % NV));
-#pragma unroll
-                    for (int kp = 0; kp < kTcKeys / 16; ++kp) {
-                        const uint64_t bd = smem_desc_sw128(va + kp * 2048, Sh::kKeyHalf, 1024);
-                        tc_mma_f16_ta(o_tm, p_tm + static_cast<uint32_t>(kp * 8), bd, kIdescPV,
-                                      (j > 0 || kp > 0) ? 1u : 0u);
-                    }
-                    tc_commit(&o_done[x][Tx & 1]);
-                }
-                __syncwarp();
-                ++pv_issued[x];
-            };
-            auto commit = [&](uint64_t* bar) {
-                if (lane == 0) tc_commit(bar);
-                __syncwarp();
-            };
-            auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-                return __all_sync(kFullMask, wait_or_abort(bar, parity, abort_v));
-            };
+    // running counters (identical in every role): key tiles loaded so far (the
+    // ring position), tiles processed so far per query-tile slot, items so far
+    int kv0 = 0;
+    int t0[kTcTiles] = {0, 0};
+    int items = 0;
+    bool ok = true;
+    auto next_item = [&](const Item& it) {
+        kv0 += it.nkt;
+        t0[0] += it.nkx[0];
+        t0[1] += it.nkx[1];
+        ++items;
+        if (*abort_v) ok = false;
+    };
 
-            // the previous item's MMAs must be complete: its S/P buffers and
-            // accumulators are reused
-            if (items > 0) ok = wait_all(&item_done, (items - 1) & 1);
-            if (ok) ok = wait_all(&q_full, items & 1) && wait_all(&k_full[kv0 % NK], (kv0 / NK) & 1);
-            if (ok) {
-                tc_fence_after_sync();
-#pragma unroll
-                for (int x = 0; x < kTcTiles; ++x)
-                    if (nkx[x]) issue_s(x, 0);
-                commit(&k_free[kv0 % NK]);
-            }
-            for (int j = 0; ok && j < nkt; ++j) {
-                const int J = kv0 + j;
-                ok = wait_all(&v_full[J % NV], (J / NV) & 1);
-                if (!ok) break;
-                bool k_next = false;   // K(j+1) seen landed
-                // per tile: P V(j) once its softmax stored P, then S(j+1) into
-                // the same columns once that P V has completed; the other
-                // tile's softmax runs meanwhile
-#pragma unroll
-                for (int x = 0; x < kTcTiles; ++x) {
-                    if (j >= nkx[x]) continue;
-                    const int Tx = t0[x] + j;
-                    if (!(ok = wait_all(&p_full[x], Tx & 1))) break;
-                    tc_fence_after_sync();
-                    issue_pv(x, j);
-                    if (j + 1 >= nkx[x]) continue;
-                    if (!k_next) {
-                        if (!(ok = wait_all(&k_full[(J + 1) % NK], ((J + 1) / NK) & 1))) break;
-                        k_next = true;
-                    }
-                    if (!(ok = wait_all(&o_done[x][Tx & 1], (Tx >> 1) & 1))) break;
-                    tc_fence_after_sync();
-                    issue_s(x, j + 1);
-                }
-                if (!ok) break;
-                commit(&v_free[J % NV]);                          // V(j)'s stage, once both P V are done
-                if (j + 1 < nkt) commit(&k_free[(J + 1) % NK]);   // K(j+1)'s, once both S are done
-            }
-            if (ok) commit(&item_done);
-            if (!ok && lane == 0) *abort_v = 1;
-        } else if (warp > kTcMmaWarp) {
-            // ============================== loaders =============================
-            // Loader li issues the boxes b = li, li + 3, ... of each K and V
-            // tile, box b = one 64-dim half (b % (D/64)) of one 16-token block
-            // (b / (D/64)); lane 0 issues, and arrives on the tile's barrier
-            // with its bytes.  Before a stage is refilled, the MMA warp's
-            // k_free / v_free for the stage's previous tile is awaited.
-            const int li = warp - kTcMmaWarp - 1;
-            constexpr int kHalves = D / 64;
-            constexpr int kBoxes = kTcBlocks * kHalves;
-            if (lane == 0) {
-                auto ids_of = [&](int j, int sk) {
-                    // this loader's blocks of tile j, recorded for the V issue
-#pragma unroll
-                    for (int blk = 0; blk < kTcBlocks; ++blk) {
-                        bool mine = false;
-#pragma unroll
-                        for (int h = 0; h < kHalves; ++h) mine |= (blk * kHalves + h) % kTcLoaders == li;
-                        int id = -1;
-                        if (mine && j * kTcBlocks + blk < nblk_live) {
-                            id = bt[j * kTcBlocks + blk];
-                            if (id < 0 || id >= p.num_blocks) {
-                                record_error(p.err, PA_DEVERR_BLOCK_ID_);
-                                id = -1;
-                            }
-                        }
-                        stage_blocks[li][sk][blk] = id;
-                    }
-                };
-                auto issue = [&](int j, bool v) {
-                    const int J = kv0 + j;
-                    const int N = v ? NV : NK;
-                    const int s = J % N;
-                    if (J >= N && !wait_or_abort(v ? &v_free[s] : &k_free[s], ((J - N) / N) & 1, abort_v))
-                        return false;
-                    // K(J) is issued before V(J), and K(J + NK) after it: the
-                    // K stage's record still holds tile J's ids for the V issue
-                    const int sk = J % NK;
-                    if (!v) ids_of(j, sk);
-                    uint32_t bytes = 0;
-                    for (int b = li; b < kBoxes; b += kTcLoaders)
-                        if (stage_blocks[li][sk][b / kHalves] >= 0) bytes += 2048;
-                    uint64_t* bar = v ? &v_full[s] : &k_full[s];
-                    mbar_arrive_expect_tx(bar, bytes);
-                    uint8_t* dst = v ? vst(s) : kst(s);
-                    const CUtensorMap* map = v ? &vmap : &kmap;
-                    for (int b = li; b < kBoxes; b += kTcLoaders) {
-                        const int blk = b / kHalves, h = b % kHalves;
-                        const int id = stage_blocks[li][sk][blk];
-                        if (id >= 0) tma_load_4d(dst + h * Sh::kKeyHalf + blk * 2048, map, bar, 0, h, g, id * 16);
-                    }
-                    if (v) ++v_total; else ++k_total;
-                    return true;
-                };
-                // the item's query tiles, once the previous item's MMAs are done
-                if (li == 0) {
-                    if (items > 0) ok = wait_or_abort(&item_done, (items - 1) & 1, abort_v);
-                    if (ok) {
-                        mbar_arrive_expect_tx(&q_full, static_cast<uint32_t>((nkx[1] ? 2 : 1) * Sh::kQ));
-#pragma unroll
-                        for (int x = 0; x < kTcTiles; ++x) {
-                            if (!nkx[x]) continue;
-#pragma unroll
-                            for (int h = 0; h < D / 64; ++h)
-                                tma_load_4d(qs(x) + h * Sh::kQHalf, &qmap, &q_full, 0, h, g * G, row0 + q0[x]);
-                        }
-                    }
-                }
-                for (int j = 0; ok && j < nkt; ++j) ok = issue(j, false) && issue(j, true);
-                if (!ok) *abort_v = 1;
-            }
-            __syncwarp();
-        } else {
-            // ========================== softmax rows ==========================
-            const int x = warp / kTcSoftmaxWarps;
-            const int wq = warp % kTcSoftmaxWarps;
-            const int r = wq * 32 + lane;                       // row = TMEM lane
-            const int nk = nkx[x];
+    if (warp < kTcMmaWarp) {
+        // ============================ softmax rows ============================
+        // (warpgroups 0 and 1: the registers of a whole 128-score row)
+        reg_alloc<kTcSoftmaxRegs>();
+        const int x = warp / kTcSoftmaxWarps;
+        const int wq = warp % kTcSoftmaxWarps;
+        const int r = wq * 32 + lane;                       // row = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t s_tm = tmem + lane_base + static_cast<uint32_t>(x * kTcKeys);
+        const uint32_t o_tm = tmem + lane_base + static_cast<uint32_t>(kTcTiles * kTcKeys + x * D);
+        const bool fold = p.scale_log2 > 0.f;   // scale folded into the exponent's FMA
+        for (int w0 = blockIdx.x; ok && w0 < total_items; w0 += ctas) {
+            Item it;
+            if (!decode_item(w0, it)) continue;
+            const int nk = x ? it.nkx[1] : it.nkx[0];
+            const int nk_a = it.nkx[0];
+            const int q0 = x ? it.q0[1] : it.q0[0];
+            const int pos_lo = x ? it.pos_lo[1] : it.pos_lo[0];
+            const int pos_hi = x ? it.pos_hi[1] : it.pos_hi[0];
+            const int tx0 = x ? t0[1] : t0[0];
             if (nk > 0) {
-                const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-                const uint32_t s_tm = tmem + lane_base + static_cast<uint32_t>(x * kTcKeys);
-                const uint32_t o_tm = tmem + lane_base + static_cast<uint32_t>(kTcTiles * kTcKeys + x * D);
-                const int qi_row = q0[x] + r / G;
-                const bool row_ok = r < QT * G && qi_row < qlen;
-                const int pos_row = row_ok ? n - qlen + qi_row : pos_hi[x];
+                const int qi_row = q0 + r / G;
+                const bool row_ok = r < QT * G && qi_row < it.qlen;
+                const int pos_row = row_ok ? it.n - it.qlen + qi_row : pos_hi;
                 // does the item's live table hold an id outside the pool?  (One
                 // scan per item keeps table loads off the per-tile path.)
                 bool any_bad = false;
-                for (int blk = lane; blk < nblk_live; blk += 32) {
-                    const int id = bt[blk];
+                for (int blk = lane; blk < it.nblk_live; blk += 32) {
+                    const int id = it.bt[blk];
                     any_bad |= id < 0 || id >= p.num_blocks;
                 }
                 any_bad = __any_sync(kFullMask, any_bad);
                 float m_ref = -INFINITY, l_run = 0.f;
-                const bool fold = p.scale_log2 > 0.f;   // scale folded into the exponent's FMA
                 for (int j = 0; j < nk; ++j) {
-                    const int Tx = t0[x] + j;
+                    const int Tx = tx0 + j;
                     const int J = kv0 + j;
                     // blocks of this tile outside the pool (their keys are masked
                     // and their V rows cleared), from the table as the producer saw it
@@ -489,8 +371,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                         for (int jb = 0; jb < kTcBlocks; ++jb) {
                             const int blk = j * kTcBlocks + jb;
-                            if (blk < nblk_live) {
-                                const int id = bt[blk];
+                            if (blk < it.nblk_live) {
+                                const int id = it.bt[blk];
                                 if (id < 0 || id >= p.num_blocks) bad |= 1u << jb;
                             }
                         }
@@ -501,46 +383,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc_fence_after_sync();
                     const int key0 = j * kTcKeys;
-                    // Scores of keys c0 .. c0 + 63 of the row: a positive scale
-                    // is applied after the row maximum (the maximum of the
-                    // scaled scores is the scaled maximum, as rounding is
-                    // monotonic), fused with the subtraction of the exponent.
-                    auto load64 = [&](int c0, float (&sv)[64]) {
-                        uint32_t r0[32], r1[32];
-                        tmem_ld32(s_tm + static_cast<uint32_t>(c0), r0);
-                        tmem_ld32(s_tm + static_cast<uint32_t>(c0 + 32), r1);
+                    // the row's 128 scores, all in flight before one wait
+                    float sv[kTcKeys];
+                    {
+                        uint32_t r0[32], r1[32], r2[32], r3[32];
+                        tmem_ld32(s_tm, r0);
+                        tmem_ld32(s_tm + 32, r1);
+                        tmem_ld32(s_tm + 64, r2);
+                        tmem_ld32(s_tm + 96, r3);
                         tmem_ld_wait();
 #pragma unroll
                         for (int c = 0; c < 32; ++c) {
                             sv[c] = __uint_as_float(r0[c]);
                             sv[32 + c] = __uint_as_float(r1[c]);
+                            sv[64 + c] = __uint_as_float(r2[c]);
+                            sv[96 + c] = __uint_as_float(r3[c]);
                         }
-                        if (!fold) {
+                    }
+                    // A positive scale is applied after the row maximum (the
+                    // maximum of the scaled scores is the scaled maximum, as
+                    // rounding is monotonic), fused with the subtraction of
+                    // the exponent.
+                    if (!fold) {
 #pragma unroll
-                            for (int c = 0; c < 64; c += 2) mul2(sv[c], sv[c + 1], p.scale_log2);
-                        }
-                        const bool need_mask = (key0 + c0 + 63 > pos_lo[x]) || ((bad >> (c0 >> 4)) & 0xfu);
-                        if (need_mask) {
+                        for (int c = 0; c < kTcKeys; c += 2) mul2(sv[c], sv[c + 1], p.scale_log2);
+                    }
+                    if ((key0 + kTcKeys - 1 > pos_lo) || bad) {
 #pragma unroll
-                            for (int c = 0; c < 64; ++c) {
-                                const bool dead = key0 + c0 + c > pos_row || ((bad >> ((c0 + c) >> 4)) & 1u);
-                                sv[c] = dead ? -INFINITY : sv[c];
-                            }
+                        for (int c = 0; c < kTcKeys; ++c) {
+                            const bool dead = key0 + c > pos_row || ((bad >> (c >> 4)) & 1u);
+                            sv[c] = dead ? -INFINITY : sv[c];
                         }
-                    };
-                    // pass 1: the row maximum (four chains of three-input maxima)
+                    }
+                    // the row maximum: four chains of three-input maxima
                     float mx;
                     {
                         float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-                        for (int hh = 0; hh < kTcKeys / 64; ++hh) {
-                            float sv[64];
-                            load64(hh * 64, sv);
 #pragma unroll
-                            for (int c = 0; c < 64; c += 8) {
+                        for (int c = 0; c < kTcKeys; c += 8) {
 #pragma unroll
-                                for (int u = 0; u < 4; ++u) mq[u] = fmax3(mq[u], sv[c + 2 * u], sv[c + 2 * u + 1]);
-                            }
+                            for (int u = 0; u < 4; ++u) mq[u] = fmax3(mq[u], sv[c + 2 * u], sv[c + 2 * u + 1]);
                         }
                         mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
                         if (fold) mx *= p.scale_log2;
@@ -567,43 +449,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         l_run *= alpha;
                         m_ref = new_ref;
                     }
-                    // pass 2: P = 2^(s - m_ref) and its sum; keys c0 .. c0 + 63
-                    // go to the 32 columns c0 / 2 .. c0 / 2 + 31 (two 16-bit
-                    // values per column, keys in order), which hold scores this
-                    // pass has already read
-                    const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-                    float sq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                    for (int hh = 0; hh < kTcKeys / 64; ++hh) {
-                        float sv[64];
-                        load64(hh * 64, sv);
+                    // P = 2^(s - m_ref) and its sum; P goes over the row's
+                    // first 64 columns (two 16-bit values per column, keys in
+                    // order)
+                    {
+                        const float ref = m_ref == -INFINITY ? 0.f : m_ref;
                         if (fold) {
 #pragma unroll
-                            for (int c = 0; c < 64; c += 2) fma2(sv[c], sv[c + 1], p.scale_log2, -ref);
+                            for (int c = 0; c < kTcKeys; c += 2) fma2(sv[c], sv[c + 1], p.scale_log2, -ref);
                         } else {
 #pragma unroll
-                            for (int c = 0; c < 64; c += 2) add2(sv[c], sv[c + 1], -ref, -ref);
+                            for (int c = 0; c < kTcKeys; c += 2) add2(sv[c], sv[c + 1], -ref, -ref);
                         }
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) sv[c] = fast_exp2(sv[c]);
+                        for (int c = 0; c < kTcKeys; ++c) sv[c] = fast_exp2(sv[c]);
+                        float sq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int c = 0; c < 64; c += 4) {
+                        for (int c = 0; c < kTcKeys; c += 4) {
                             add2(sq[0], sq[1], sv[c], sv[c + 1]);
                             add2(sq[2], sq[3], sv[c + 2], sv[c + 3]);
                         }
-                        uint32_t pw[32];
+                        l_run += (sq[0] + sq[1]) + (sq[2] + sq[3]);
+                        uint32_t pw0[32], pw1[32];
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) pw[c] = Elem<T>::pack(sv[2 * c], sv[2 * c + 1]);
-                        tmem_st32(s_tm + static_cast<uint32_t>(hh * 32), pw);
+                        for (int c = 0; c < 32; ++c) {
+                            pw0[c] = Elem<T>::pack(sv[2 * c], sv[2 * c + 1]);
+                            pw1[c] = Elem<T>::pack(sv[64 + 2 * c], sv[64 + 2 * c + 1]);
+                        }
+                        tmem_st32(s_tm, pw0);
+                        tmem_st32(s_tm + 32, pw1);
                     }
-                    l_run += (sq[0] + sq[1]) + (sq[2] + sq[3]);
                     // V rows that must contribute nothing (past the pair's last
                     // query position, or in a block outside the pool) may hold
                     // anything, NaN included: the first tile of the pair that
                     // reads this key tile clears them before its P V (the other
                     // tile's P V is issued after it)
-                    const bool clearer = x == 0 || j >= nkx[0];
-                    if (clearer && (j == nkt - 1 || bad)) {
+                    const bool clearer = x == 0 || j >= nk_a;
+                    if (clearer && (j == it.nkt - 1 || bad)) {
                         if (!__all_sync(kFullMask, wait_or_abort(&v_full[J % NV], (J / NV) & 1, abort_v))) {
                             ok = false;
                             break;
@@ -613,7 +495,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         for (int idx = r; idx < kTcKeys * CPR; idx += kTcSoftmaxWarps * 32) {
                             const int key = idx / CPR;
                             const int c = idx - key * CPR;
-                            if (key0 + key > pos_pair || ((bad >> (key >> 4)) & 1u))
+                            if (key0 + key > it.pos_pair || ((bad >> (key >> 4)) & 1u))
                                 *reinterpret_cast<uint4*>(vt + (c >> 3) * Sh::kKeyHalf + key * 128 +
                                                           (((c & 7) ^ (key & 7)) << 4)) = make_uint4(0, 0, 0, 0);
                         }
@@ -625,13 +507,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (lane == 0) mbar_arrive(&p_full[x]);
                 }
                 if (ok) {
-                    const int Tl = t0[x] + nk - 1;
+                    const int Tl = tx0 + nk - 1;
                     const bool got = wait_or_abort(&o_done[x][Tl & 1], (Tl >> 1) & 1, abort_v);
                     if (__all_sync(kFullMask, got)) {
                         tc_fence_after_sync();
                         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
                         const int64_t grow =
-                            static_cast<int64_t>(row0 + qi_row) * p.num_q_heads + g * G + (r % G);
+                            static_cast<int64_t>(it.row0 + qi_row) * p.num_q_heads + it.g * G + (r % G);
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + grow * D);
 #pragma unroll
                         for (int c0 = 0; c0 < D / 32; ++c0) {
@@ -661,17 +543,106 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             if (!ok) *abort_v = 1;
+            next_item(it);
         }
-        kv0 += nkt;
-        t0[0] += nkx[0];
-        t0[1] += nkx[1];
-        ++items;
-        if (*abort_v) ok = false;
-    }
-
-    if (!ok || *abort_v) {
-        if (tid == 0) record_error(p.err, PA_DEVERR_TIMEOUT_);
-        if (warp == kTcMmaWarp && lane == 0) {
+        if (!ok || *abort_v) {
+            if (tid == 0) record_error(p.err, PA_DEVERR_TIMEOUT_);
+        }
+    } else if (warp == kTcMmaWarp) {
+        // ============================== MMA issuer ==============================
+        reg_dealloc<kTcOtherRegs>();
+        int s_issued[kTcTiles] = {0, 0}, pv_issued[kTcTiles] = {0, 0};   // for the abort path
+        for (int w0 = blockIdx.x; ok && w0 < total_items; w0 += ctas) {
+            Item it;
+            if (!decode_item(w0, it)) continue;
+            // S_X(j) into S_X: eight MMAs of K=16 over the head dimension
+            auto mma_s = [&](int x, int j) {
+                if (lane == 0) {
+                    const uint32_t qa = smem_addr(qs(x));
+                    const uint32_t ka = smem_addr(kst((kv0 + j) % NK));
+                    const uint32_t d_tm = tmem + static_cast<uint32_t>(x * kTcKeys);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t a = smem_desc_sw128(qa + (kk >> 2) * Sh::kQHalf + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd =
+                            smem_desc_sw128(ka + (kk >> 2) * Sh::kKeyHalf + (kk & 3) * 32, 16, 1024);
+                        tc_mma_f16(d_tm, a, bd, kIdescS, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(&s_full[x]);
+                }
+                __syncwarp();
+                ++s_issued[x];
+            };
+            // O_X += P_X(j) V(j): P is read from tensor memory, where the softmax
+            // stored it over the first 64 columns of S_X
+            auto mma_pv = [&](int x, int j) {
+                const int Tx = t0[x] + j;
+                if (lane == 0) {
+                    const uint32_t p_tm = tmem + static_cast<uint32_t>(x * kTcKeys);
+                    const uint32_t o_tm = tmem + static_cast<uint32_t>(kTcTiles * kTcKeys + x * D);
+                    const uint32_t va = smem_addr(vst((kv0 + j) % NV));
+#pragma unroll
+                    for (int kp = 0; kp < kTcKeys / 16; ++kp) {
+                        const uint64_t bd = smem_desc_sw128(va + kp * 2048, Sh::kKeyHalf, 1024);
+                        tc_mma_f16_ta(o_tm, p_tm + static_cast<uint32_t>(kp * 8), bd, kIdescPV,
+                                      (j > 0 || kp > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&o_done[x][Tx & 1]);
+                }
+                __syncwarp();
+                ++pv_issued[x];
+            };
+            auto commit = [&](uint64_t* bar) {
+                if (lane == 0) tc_commit(bar);
+                __syncwarp();
+            };
+            auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+                return __all_sync(kFullMask, wait_or_abort(bar, parity, abort_v));
+            };
+            // the previous item's MMAs must be complete: its S/P buffers and
+            // accumulators are reused
+            if (items > 0) ok = wait_all(&item_done, (items - 1) & 1);
+            if (ok) ok = wait_all(&q_full, items & 1) && wait_all(&k_full[kv0 % NK], (kv0 / NK) & 1);
+            if (ok) {
+                tc_fence_after_sync();
+#pragma unroll
+                for (int x = 0; x < kTcTiles; ++x)
+                    if (it.nkx[x]) mma_s(x, 0);
+                commit(&k_free[kv0 % NK]);
+            }
+            for (int j = 0; ok && j < it.nkt; ++j) {
+                const int J = kv0 + j;
+                ok = wait_all(&v_full[J % NV], (J / NV) & 1);
+                if (!ok) break;
+                bool k_next = false;   // K(j+1) seen landed
+                // per tile: P V(j) once its softmax stored P, then S(j+1) into
+                // the same columns once that P V has completed; the other
+                // tile's softmax runs meanwhile
+#pragma unroll
+                for (int x = 0; x < kTcTiles; ++x) {
+                    if (j >= it.nkx[x]) continue;
+                    const int Tx = t0[x] + j;
+                    if (!(ok = wait_all(&p_full[x], Tx & 1))) break;
+                    tc_fence_after_sync();
+                    mma_pv(x, j);
+                    if (j + 1 >= it.nkx[x]) continue;
+                    if (!k_next) {
+                        if (!(ok = wait_all(&k_full[(J + 1) % NK], ((J + 1) / NK) & 1))) break;
+                        k_next = true;
+                    }
+                    if (!(ok = wait_all(&o_done[x][Tx & 1], (Tx >> 1) & 1))) break;
+                    tc_fence_after_sync();
+                    mma_s(x, j + 1);
+                }
+                if (!ok) break;
+                commit(&v_free[J % NV]);                              // V(j)'s stage, once both P V are done
+                if (j + 1 < it.nkt) commit(&k_free[(J + 1) % NK]);    // K(j+1)'s, once both S are done
+            }
+            if (ok) commit(&item_done);
+            if (!ok && lane == 0) *abort_v = 1;
+            next_item(it);
+        }
+        if ((!ok || *abort_v) && lane == 0) {
             // let MMAs still in flight finish before the CTA's memory is reused
 #pragma unroll
             for (int x = 0; x < kTcTiles; ++x) {
@@ -682,8 +653,88 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
         }
-        if (warp > kTcMmaWarp && lane == 0) {
-            // and this loader's copies: each stage's last issued phase
+    } else {
+        // ================================ loaders ===============================
+        // Loader li issues the boxes b = li, li + 3, ... of each K and V tile,
+        // box b = one 64-dim half (b % (D/64)) of one 16-token block
+        // (b / (D/64)); lane 0 issues, and arrives on the tile's barrier with
+        // its bytes.  Before a stage is refilled, the MMA warp's k_free /
+        // v_free for the stage's previous tile is awaited.
+        reg_dealloc<kTcOtherRegs>();
+        const int li = warp - kTcMmaWarp - 1;
+        constexpr int kHalves = D / 64;
+        constexpr int kBoxes = kTcBlocks * kHalves;
+        int k_total = 0, v_total = 0;   // K and V tiles issued so far (ring order), for the abort path
+        for (int w0 = blockIdx.x; ok && w0 < total_items; w0 += ctas) {
+            Item it;
+            if (!decode_item(w0, it)) continue;
+            if (lane == 0) {
+                auto ids_of = [&](int j, int sk) {
+                    // this loader's blocks of tile j, recorded for the V issue
+#pragma unroll
+                    for (int blk = 0; blk < kTcBlocks; ++blk) {
+                        bool mine = false;
+#pragma unroll
+                        for (int h = 0; h < kHalves; ++h) mine |= (blk * kHalves + h) % kTcLoaders == li;
+                        int id = -1;
+                        if (mine && j * kTcBlocks + blk < it.nblk_live) {
+                            id = it.bt[j * kTcBlocks + blk];
+                            if (id < 0 || id >= p.num_blocks) {
+                                record_error(p.err, PA_DEVERR_BLOCK_ID_);
+                                id = -1;
+                            }
+                        }
+                        stage_blocks[li][sk][blk] = id;
+                    }
+                };
+                auto issue = [&](int j, bool v) {
+                    const int J = kv0 + j;
+                    const int N = v ? NV : NK;
+                    const int s = J % N;
+                    if (J >= N && !wait_or_abort(v ? &v_free[s] : &k_free[s], ((J - N) / N) & 1, abort_v))
+                        return false;
+                    // K(J) is issued before V(J), and K(J + NK) after it: the
+                    // K stage's record still holds tile J's ids for the V issue
+                    const int sk = J % NK;
+                    if (!v) ids_of(j, sk);
+                    uint32_t bytes = 0;
+                    for (int b = li; b < kBoxes; b += kTcLoaders)
+                        if (stage_blocks[li][sk][b / kHalves] >= 0) bytes += 2048;
+                    uint64_t* bar = v ? &v_full[s] : &k_full[s];
+                    mbar_arrive_expect_tx(bar, bytes);
+                    uint8_t* dst = v ? vst(s) : kst(s);
+                    const CUtensorMap* map = v ? &vmap : &kmap;
+                    for (int b = li; b < kBoxes; b += kTcLoaders) {
+                        const int blk = b / kHalves, h = b % kHalves;
+                        const int id = stage_blocks[li][sk][blk];
+                        if (id >= 0) tma_load_4d(dst + h * Sh::kKeyHalf + blk * 2048, map, bar, 0, h, it.g, id * 16);
+                    }
+                    if (v) ++v_total; else ++k_total;
+                    return true;
+                };
+                // the item's query tiles, once the previous item's MMAs are done
+                if (li == 0) {
+                    if (items > 0) ok = wait_or_abort(&item_done, (items - 1) & 1, abort_v);
+                    if (ok) {
+                        mbar_arrive_expect_tx(&q_full, static_cast<uint32_t>((it.nkx[1] ? 2 : 1) * Sh::kQ));
+#pragma unroll
+                        for (int x = 0; x < kTcTiles; ++x) {
+                            if (!it.nkx[x]) continue;
+#pragma unroll
+                            for (int h = 0; h < D / 64; ++h)
+                                tma_load_4d(qs(x) + h * Sh::kQHalf, &qmap, &q_full, 0, h, it.g * G,
+                                            it.row0 + it.q0[x]);
+                        }
+                    }
+                }
+                for (int j = 0; ok && j < it.nkt; ++j) ok = issue(j, false) && issue(j, true);
+                if (!ok) *abort_v = 1;
+            }
+            ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+            next_item(it);
+        }
+        if ((!ok || *abort_v) && lane == 0) {
+            // this loader's copies still in flight: each stage's last issued phase
             for (int t = max(0, k_total - NK); t < k_total; ++t) (void)mbar_wait(&k_full[t % NK], (t / NK) & 1);
             for (int t = max(0, v_total - NV); t < v_total; ++t) (void)mbar_wait(&v_full[t % NV], (t / NV) & 1);
         }
@@ -704,6 +755,13 @@ cudaError_t launch_t(const PrefillParams& p, int32_t* plan, const CUtensorMap& k
     auto kern = prefill_tc_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // the softmax warpgroups' register increase is granted from the pool the
+    // CTA is launched with: refuse to launch if the build gave it fewer
+    static const int launch_regs = [&] {
+        cudaFuncAttributes fa{};
+        return cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : 0;
+    }();
+    if (launch_regs < kTcLaunchRegs) return cudaErrorInvalidConfiguration;
     prefill_plan_kernel<<<1, 1024, 0, s>>>(p.cu_q_lens, p.num_seqs, p.q_per_tile, plan);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
