@@ -552,6 +552,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
     // p.overlap the preceding kernel is a prefill kernel this one runs beside,
     // and the list was built before that kernel started
     if (!p.overlap) pdl_wait();
+    // a reduce launched with programmatic dependent launch may be scheduled
+    // now: its CTAs wait on chip for this grid to complete
+    pdl_trigger();
     const int total = *p.unit_count * H * C;
     if (total == 0) return;
     int* queue = claimed[warp];
@@ -877,6 +880,7 @@ __global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     float* sc = sc_all[warp];
+    pdl_wait();   // the decode kernel's partials (launched with programmatic dependent launch)
     const int P = p.partition_tokens;
     const int64_t pairs = static_cast<int64_t>(*p.row_count) * p.num_q_heads;
     for (int64_t w = static_cast<int64_t>(blockIdx.x) * kReduceWarps + warp; w < pairs;
@@ -1053,12 +1057,14 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, cons
             // persistent: a few waves of 8-warp CTAs, one warp per pair
             const int rgrid = static_cast<int>(std::max<long long>(
                 1, std::min<long long>((pairs + kReduceWarps - 1) / kReduceWarps, 8LL * sm_count())));
-            decode_reduce_kernel<T, D><<<rgrid, kReduceWarps * 32, 0, s>>>(p);
+            // scheduled while the decode grid drains (its CTAs wait on chip);
+            // the CTA-per-pair layout below has too many CTAs for that to pay
+            e = launch_pdl(decode_reduce_kernel<T, D>, dim3(rgrid), dim3(kReduceWarps * 32), 0, s, p);
         } else {
             dim3 rgrid(p.num_q_heads, std::min(p.max_rows, kReduceMaxRowsPerLaunch));
             decode_reduce_cta_kernel<T, D><<<rgrid, D, 0, s>>>(p);
+            e = cudaGetLastError();
         }
-        e = cudaGetLastError();
     }
     return e;
 }
