@@ -346,7 +346,8 @@ def run_ours(args):
     # slot mapping + KV write; the decode plan + decode kernels; the
     # log-sum-exp reduce when a sequence can span several partitions; the
     # prefill plan + prefill kernels when a chunk is longer than 8 queries
-    parts = -(-max_len // (args.partition or 512)) if decode else -(-max_len // 512)
+    partition = pa.decode_partition(max_len, args.partition if decode else 0)
+    parts = -(-max_len // partition)
     launches_per_step = 4 + (1 if parts > 1 else 0) + (2 if not decode and w.max_q_len > 8 else 0)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -450,7 +451,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": args.workload, "batch": B, "new_tokens_per_step": T, "ctx": ctx,
                    "heads": f"{w.num_q_heads}/{w.num_kv_heads}", "head_dim": w.head_dim, "block_size": 16,
-                   "partition": (args.partition or 512), "pool_blocks": w.num_blocks,
+                   "partition": partition, "pool_blocks": w.num_blocks,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {ab['kv_unique'] / 1e9:.2f} GB of KV read per step"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

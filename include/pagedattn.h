@@ -54,6 +54,11 @@ extern "C" {
 
 #define PA_BLOCK_SIZE 16
 #define PA_DEFAULT_PARTITION 512
+/* partition_size 0 means PA_DEFAULT_PARTITION tokens, doubled (up to
+ * PA_MAX_AUTO_PARTITION) while a sequence of max_seq_len tokens would have
+ * more than PA_AUTO_MAX_PARTS partitions (see pa_decode_partition). */
+#define PA_AUTO_MAX_PARTS 64
+#define PA_MAX_AUTO_PARTITION 8192
 #define PA_MAX_GROUP 8
 /* Chunks of at most this many queries (decode rows, speculative-verify rows)
  * run in the decode kernel inside pa_paged_attention_prefill. */
@@ -111,11 +116,22 @@ int pa_paged_kv_write(const void* key, const void* value, void* k_cache, void* v
                       int num_kv_heads, int head_dim, int block_size, int dtype, void* stream);
 
 /*
+ * The partition length (tokens) a decode call with these arguments uses:
+ * partition_size itself when nonzero; for 0, PA_DEFAULT_PARTITION doubled
+ * while ceil(max_seq_len / partition) > PA_AUTO_MAX_PARTS, at most
+ * PA_MAX_AUTO_PARTITION (long contexts merge fewer partials; shorter ones keep
+ * more, smaller work items for load balance).  Decode and verify rows of
+ * pa_paged_attention_prefill use the value for 0.  Returns -1 for a negative
+ * argument or a partition_size that is not a multiple of PA_BLOCK_SIZE.
+ */
+int pa_decode_partition(int max_seq_len, int partition_size);
+
+/*
  * Workspace for pa_paged_attention_decode: the kernel's work list (one entry
  * per sequence partition) and the split-context partials of num_seqs
  * sequences no longer than max_seq_len, cut into partitions of
- * partition_size tokens (0 = PA_DEFAULT_PARTITION).  Nonzero whenever
- * num_seqs > 0.
+ * partition_size tokens (0 = the automatic length of pa_decode_partition).
+ * Nonzero whenever num_seqs > 0.
  */
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len,
                                  int partition_size);
@@ -132,7 +148,7 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, in
  *   max_seq_len   host-side upper bound of seq_lens (sizes the grid).
  *   num_blocks    pool size in blocks (bounds every table entry).
  *   partition_size tokens per partition, a positive multiple of block_size,
- *                 or 0 for PA_DEFAULT_PARTITION.
+ *                 or 0 for the automatic length (pa_decode_partition).
  *   workspace     device scratch of at least pa_decode_workspace_bytes(...)
  *                 bytes, 256-byte aligned.
  * A sequence with seq_len == 0 gets an all-zero output row.
@@ -180,7 +196,7 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_p
  * num_tokens query rows: the chunk tile work list (num_seqs + 1 int32), the
  * decode kernel's work list, and the split-context partials of up to
  * min(num_tokens, PA_VERIFY_MAX_Q * num_seqs) query rows of decode and verify
- * chunks (partitions of PA_DEFAULT_PARTITION tokens).  Nonzero whenever
+ * chunks (partitions of pa_decode_partition(max_seq_len, 0) tokens).  Nonzero whenever
  * num_seqs > 0; 0 for a negative argument. */
 size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_q_heads, int head_dim,
                                   int max_seq_len);

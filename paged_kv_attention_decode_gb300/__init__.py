@@ -8,6 +8,7 @@ fails loudly if the library has not been built.
 from ._binding import (  # noqa: F401
     PagedAttnError,
     copy_blocks,
+    decode_partition,
     decode_workspace_bytes,
     library_path,
     load_library,

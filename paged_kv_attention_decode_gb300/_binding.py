@@ -45,6 +45,7 @@ _SIGNATURES = {
     "pa_paged_attention_decode_fp8": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _f32, _f32, _f32,
                                              _i32, _i32, _i32, _i32, _i32, _p, _sz, _i32, _p]),
     "pa_copy_blocks": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _p]),
+    "pa_decode_partition": (_i32, [_i32, _i32]),
     "pa_paged_kv_gather": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _p]),
 }
 
@@ -143,6 +144,13 @@ def paged_kv_write(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor
                                           v_cache.data_ptr(), slot_mapping.data_ptr(), T, NB, H, D,
                                           bs, _dt(key), _stream(stream))
     _check(rc, "pa_paged_kv_write")
+
+
+def decode_partition(max_seq_len: int, partition_size: int = 0) -> int:
+    """Partition length (tokens) a decode call uses; 0 selects the automatic one."""
+    n = int(load_library().pa_decode_partition(max_seq_len, partition_size))
+    _need(n > 0, "invalid max_seq_len or partition_size")
+    return n
 
 
 def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_seq_len: int,

@@ -148,6 +148,16 @@ int parts_for(int max_seq_len, int partition) {
     return max_seq_len > 0 ? (max_seq_len + partition - 1) / partition : 1;
 }
 
+// partition_size 0: PA_DEFAULT_PARTITION tokens, doubled (up to
+// PA_MAX_AUTO_PARTITION) while a sequence of max_seq_len tokens would have more
+// than PA_AUTO_MAX_PARTS partitions: long contexts then merge fewer partials
+int effective_partition(int max_seq_len, int partition_size) {
+    if (partition_size) return partition_size;
+    int part = PA_DEFAULT_PARTITION;
+    while (part < PA_MAX_AUTO_PARTITION && parts_for(max_seq_len, part) > PA_AUTO_MAX_PARTS) part *= 2;
+    return part;
+}
+
 size_t partials_bytes(int num_seqs, int num_q_heads, int head_dim, int parts) {
     const size_t n = static_cast<size_t>(num_seqs) * num_q_heads * parts;
     return 2 * align256(n * sizeof(float)) + align256(n * head_dim * sizeof(float));
@@ -247,10 +257,15 @@ int pa_paged_kv_write(const void* key, const void* value, void* k_cache, void* v
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+int pa_decode_partition(int max_seq_len, int partition_size) {
+    if (max_seq_len < 0 || partition_size < 0 || partition_size % PA_BLOCK_SIZE) return -1;
+    return effective_partition(max_seq_len, partition_size);
+}
+
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len,
                                  int partition_size) {
     if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len < 0 || partition_size < 0) return 0;
-    const int part = partition_size ? partition_size : PA_DEFAULT_PARTITION;
+    const int part = effective_partition(max_seq_len, partition_size);
     return decode_ws_bytes(num_seqs, num_seqs, num_q_heads, head_dim, parts_for(max_seq_len, part));
 }
 
@@ -268,7 +283,7 @@ static int decode_prepare(DecodeCall& c, void* out, const void* q, const void* k
                           int num_q_heads, int num_kv_heads, int head_dim, int partition_size, void* workspace,
                           size_t workspace_bytes, int dtype, int max_q, int max_rows, bool fp8 = false,
                           float k_scale = 1.f, float v_scale = 1.f) {
-    const int part = partition_size ? partition_size : PA_DEFAULT_PARTITION;
+    const int part = effective_partition(max_seq_len, partition_size);
     const int parts = parts_for(max_seq_len, part);
     if (parts > 65535) return PA_ERR_INVALID_ARG;   // partition index is a 16-bit field of the work list
     const size_t need = decode_ws_bytes(num_seqs, max_rows, num_q_heads, head_dim, parts);
@@ -402,7 +417,8 @@ int pa_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache,
 size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_q_heads, int head_dim, int max_seq_len) {
     if (num_seqs <= 0 || num_tokens < 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len < 0) return 0;
     return plan_bytes(num_seqs) + decode_ws_bytes(num_seqs, verify_rows_bound(num_seqs, num_tokens), num_q_heads,
-                                                  head_dim, parts_for(max_seq_len, PA_DEFAULT_PARTITION));
+                                                  head_dim,
+                                                  parts_for(max_seq_len, effective_partition(max_seq_len, 0)));
 }
 
 int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -63,20 +63,38 @@ def _partials(rows, heads, parts, dim=128):
     return 2 * _align(n * 4) + _align(n * dim * 4)
 
 
+def test_automatic_partition(lib):
+    # 512 tokens, doubled while a max_seq_len sequence would have more than 64 partitions
+    assert pa.decode_partition(0) == 512
+    assert pa.decode_partition(4096) == 512
+    assert pa.decode_partition(32768) == 512          # exactly 64 partitions
+    assert pa.decode_partition(32769) == 1024
+    assert pa.decode_partition(131072) == 2048
+    assert pa.decode_partition(131073) == 4096
+    assert pa.decode_partition(10 ** 8) == 8192       # capped
+    assert pa.decode_partition(131072, 256) == 256    # an explicit length is kept
+    for bad in ((-1, 0), (4096, 100), (4096, -16)):
+        with pytest.raises(pa.PagedAttnError):
+            pa.decode_partition(*bad)
+
+
 def test_workspace_sizes(lib):
     # [header 256 B][work list: B x partitions int32]
     # + when partitions > 1: [row_base: B int32][rows: R int32][partials of R rows]
     assert pa.decode_workspace_bytes(64, 32, 128, 512, 512) == 256 + _align(64 * 4)
     assert pa.decode_workspace_bytes(64, 32, 128, 4096, 512) == (256 + _align(64 * 8 * 4) + _align(64 * 4)
                                                                  + _align(64 * 4) + _partials(64, 32, 8))
-    assert pa.decode_workspace_bytes(8, 64, 128, 131072, 0) == (256 + _align(8 * 256 * 4) + 2 * _align(8 * 4)
-                                                                + _partials(8, 64, 256))
+    # 131072 tokens: the automatic partition is 2048 tokens (64 partitions)
+    assert pa.decode_workspace_bytes(8, 64, 128, 131072, 0) == (256 + _align(8 * 64 * 4) + 2 * _align(8 * 4)
+                                                                + _partials(8, 64, 64))
+    assert pa.decode_workspace_bytes(8, 64, 128, 131072, 512) == (256 + _align(8 * 256 * 4) + 2 * _align(8 * 4)
+                                                                  + _partials(8, 64, 256))
     # prefill: partials rows = min(num_tokens, 8 * num_seqs) (decode and verify chunks)
     assert pa.prefill_workspace_bytes(8, 8, 64, 128, 131072) == (_align(9 * 4)
                                                                  + pa.decode_workspace_bytes(8, 64, 128, 131072, 0))
-    assert pa.prefill_workspace_bytes(8, 6000, 64, 128, 131072) == (_align(9 * 4) + 256 + _align(8 * 256 * 4)
+    assert pa.prefill_workspace_bytes(8, 6000, 64, 128, 131072) == (_align(9 * 4) + 256 + _align(8 * 64 * 4)
                                                                     + _align(8 * 4) + _align(64 * 4)
-                                                                    + _partials(64, 64, 256))
+                                                                    + _partials(64, 64, 64))
     assert pa.prefill_workspace_bytes(4, 12, 32, 128, 1024) == (_align(5 * 4) + 256 + _align(4 * 2 * 4)
                                                                 + _align(4 * 4) + _align(12 * 4)
                                                                 + _partials(12, 32, 2))
