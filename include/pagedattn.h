@@ -221,7 +221,9 @@ size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_q_heads,
  *                 256-byte aligned.
  * Errors on the device set PA_DEVERR_SEQ_LEN: a decode/verify chunk longer
  * than its seq_len or than max_q_len gets zero rows; a longer chunk that
- * exceeds its seq_len is left unwritten.
+ * exceeds its seq_len is left unwritten; a chunk whose rows fall outside
+ * 0 .. num_tokens - 1 (cu_q_lens inconsistent with num_tokens) is neither
+ * read nor written.
  * The call only enqueues work on `stream` (the prefill and decode kernels may
  * run side by side inside it); work queued after it on the same stream sees
  * every output row.

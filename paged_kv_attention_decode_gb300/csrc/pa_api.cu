@@ -281,7 +281,7 @@ static int decode_prepare(DecodeCall& c, void* out, const void* q, const void* k
                           const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
                           const int32_t* cu_q_lens, int num_seqs, int max_seq_len, int num_blocks, float scale,
                           int num_q_heads, int num_kv_heads, int head_dim, int partition_size, void* workspace,
-                          size_t workspace_bytes, int dtype, int max_q, int max_rows, bool fp8 = false,
+                          size_t workspace_bytes, int dtype, int max_q, int max_rows, int num_rows, bool fp8 = false,
                           float k_scale = 1.f, float v_scale = 1.f) {
     const int part = effective_partition(max_seq_len, partition_size);
     const int parts = parts_for(max_seq_len, part);
@@ -316,6 +316,7 @@ static int decode_prepare(DecodeCall& c, void* out, const void* q, const void* k
     p.max_parts = parts;
     p.max_q = max_q;
     p.max_rows = max_rows;
+    p.num_rows = num_rows;
     // (query, head) columns per work item: 8, or 16 once a row can have more
     const int cols = max_q * p.group;
     const int chunk = cols > 8 ? 16 : 8;
@@ -344,8 +345,8 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
     DecodeCall c;
     const int rc = decode_prepare(c, out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens,
                                   num_seqs, max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim,
-                                  partition_size, workspace, workspace_bytes, dtype, max_q, max_rows, fp8, k_scale,
-                                  v_scale);
+                                  partition_size, workspace, workspace_bytes, dtype, max_q, max_rows, num_seqs, fp8,
+                                  k_scale, v_scale);
     return rc ? rc : decode_launch(c, stream);
 }
 
@@ -368,7 +369,13 @@ int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, con
 }
 
 // Prefill workspace: [tile work list: num_seqs + 1 int32, 256-aligned][decode-row partials].
-static size_t plan_bytes(int num_seqs) { return align256(static_cast<size_t>(num_seqs + 1) * sizeof(int32_t)); }
+// prefill plan: offsets (num_seqs + 1) and the cost-sorted pair list.  A pair
+// is two tiles of at least 16 queries (128 rows / at most 8 heads), so a chunk
+// of q queries has at most q / 32 + 1 pairs.
+static size_t plan_bytes(int num_seqs, int num_tokens) {
+    const size_t pairs = static_cast<size_t>(num_tokens) / 32 + static_cast<size_t>(num_seqs);
+    return align256((static_cast<size_t>(num_seqs) + 1 + pairs) * sizeof(int32_t));
+}
 
 int pa_paged_kv_write_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
                           const int64_t* slot_mapping, int num_tokens, int num_blocks, int num_kv_heads,
@@ -416,7 +423,7 @@ int pa_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache,
 
 size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_q_heads, int head_dim, int max_seq_len) {
     if (num_seqs <= 0 || num_tokens < 0 || num_q_heads <= 0 || head_dim <= 0 || max_seq_len < 0) return 0;
-    return plan_bytes(num_seqs) + decode_ws_bytes(num_seqs, verify_rows_bound(num_seqs, num_tokens), num_q_heads,
+    return plan_bytes(num_seqs, num_tokens) + decode_ws_bytes(num_seqs, verify_rows_bound(num_seqs, num_tokens), num_q_heads,
                                                   head_dim,
                                                   parts_for(max_seq_len, effective_partition(max_seq_len, 0)));
 }
@@ -437,7 +444,7 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
     if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_q_lens) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t pb = plan_bytes(num_seqs);
+    const size_t pb = plan_bytes(num_seqs, num_tokens);
     if (!workspace ||
         workspace_bytes < pa_prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, head_dim, max_seq_len))
         return PA_ERR_WORKSPACE_TOO_SMALL;
@@ -452,7 +459,7 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
     rc = decode_prepare(dc, out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens, num_seqs,
                         max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, 0,
                         static_cast<uint8_t*>(workspace) + pb, workspace_bytes - pb, dtype, max_q,
-                        verify_rows_bound(num_seqs, num_tokens));
+                        verify_rows_bound(num_seqs, num_tokens), num_tokens);
     if (rc) return rc;
     if (max_q_len <= PA_VERIFY_MAX_Q) return decode_launch(dc, s);
     unsigned int* err = error_word();

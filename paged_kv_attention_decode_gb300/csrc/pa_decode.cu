@@ -431,7 +431,14 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
     auto row_of = [&](int b, bool record, int& qlen) -> int {
         qlen = 1;
         if (p.cu_q_lens) {
-            qlen = p.cu_q_lens[b + 1] - p.cu_q_lens[b];
+            const int c0 = p.cu_q_lens[b], c1 = p.cu_q_lens[b + 1];
+            qlen = c1 - c0;
+            if (c0 < 0 || c1 > p.num_rows) {
+                // rows outside q / out: none of them is read or written
+                if (record && qlen >= 1 && qlen <= PA_VERIFY_MAX_Q_) record_error(p.err, PA_DEVERR_SEQ_LEN_);
+                qlen = 0;
+                return 0;
+            }
             if (qlen < 1 || qlen > PA_VERIFY_MAX_Q_) {
                 qlen = 0;
                 return 0;
@@ -576,7 +583,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
             it.qlen = p.cu_q_lens[it.b + 1] - it.qrow0;
         }
         int n = p.seq_lens[it.b];
-        if (n < it.qlen || n > p.max_seq_len || n > p.max_blocks * 16 || it.qlen < 1 || it.qlen > p.max_q) n = 0;
+        if (n < it.qlen || n > p.max_seq_len || n > p.max_blocks * 16 || it.qlen < 1 || it.qlen > p.max_q ||
+            it.qrow0 < 0 || it.qrow0 + it.qlen > p.num_rows)
+            n = 0;
         it.n = n;
         it.col0 = (w % C) * kChunkCols;
         it.ncols = min(kChunkCols, it.qlen * G - it.col0);

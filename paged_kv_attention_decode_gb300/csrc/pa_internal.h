@@ -67,6 +67,7 @@ struct DecodeParams {
     int max_parts;                // ceil(max_seq_len / partition_tokens)
     int max_q;                    // largest chunk handled here (1..PA_VERIFY_MAX_Q_)
     int max_rows;                 // partials rows available in the workspace
+    int num_rows;                 // rows of q and out (num_seqs without cu_q_lens)
     int col_chunks;               // chunks of 8 or 16 (query, head) columns per (unit, kv head)
     float scale_log2;             // scale * log2(e) (times the K dequantisation scale for FP8)
     float v_scale;                // V dequantisation scale (1 for 16-bit caches)

@@ -127,57 +127,131 @@ __device__ __forceinline__ void fma2(float& x, float& y, float s, float a) {
         : "f"(s), "f"(a));
 }
 
-// Work list of the chunked-prefill items: offsets[b] = number of query-tile
-// pairs (two 128-row tiles) of sequences 0..b-1 whose chunk is longer than
-// PA_VERIFY_MAX_Q_ tokens (shorter chunks are decode or speculative-verify
-// rows and belong to the decode kernel); offsets[B] = total.  One CTA.
-__global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __restrict__ cu_q_lens, int num_seqs,
-                                                            int q_per_tile, int32_t* __restrict__ offsets) {
-    __shared__ int warp_tot[32];
-    __shared__ int carry;
+// Key tiles a query-tile pair of a chunk reads: those of its last tile.
+// Pair pr of a chunk of ql queries on a sequence of n tokens (tiles of qt rows).
+__device__ __forceinline__ int pair_key_tiles(int n, int ql, int qt, int pr) {
+    const int ntiles = (ql + qt - 1) / qt;
+    const int last = min(2 * pr + 1, ntiles - 1);                 // the pair's last query tile
+    const int q_last = min(ql, (last + 1) * qt) - 1;
+    return (n - ql + q_last + kTcKeys) / kTcKeys;
+}
+
+// Exclusive prefix sum of one value per thread over a 1024-thread block, plus
+// the running total `carry` of earlier calls (updated).  Every thread calls.
+__device__ __forceinline__ int block_exclusive_scan_1024(int v, int* warp_tot, int* carry) {
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    if (tid == 0) carry = 0;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(kFullMask, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
-    for (int base = 0; base < num_seqs; base += 1024) {
-        const int b = base + tid;
-        int v = 0;
-        if (b < num_seqs) {
-            const int ql = cu_q_lens[b + 1] - cu_q_lens[b];
-            const int tiles = ql > PA_VERIFY_MAX_Q_ ? (ql + q_per_tile - 1) / q_per_tile : 0;
-            v = (tiles + kTcTiles - 1) / kTcTiles;
-        }
-        int incl = v;
+    if (warp == 0) {
+        int t = warp_tot[lane];
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(kFullMask, incl, off);
-            if (lane >= off) incl += y;
+            const int y = __shfl_up_sync(kFullMask, t, off);
+            if (lane >= off) t += y;
         }
-        if (lane == 31) warp_tot[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            int t = warp_tot[lane];
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int y = __shfl_up_sync(kFullMask, t, off);
-                if (lane >= off) t += y;
-            }
-            warp_tot[lane] = t;  // inclusive over warps
-        }
-        __syncthreads();
-        const int before = carry + (warp > 0 ? warp_tot[warp - 1] : 0);
-        if (b < num_seqs) offsets[b] = before + incl - v;
-        __syncthreads();
-        if (tid == 1023) carry = before + incl;
-        __syncthreads();
+        warp_tot[lane] = t;  // inclusive over warps
     }
-    if (tid == 0) offsets[num_seqs] = carry;
+    __syncthreads();
+    const int before = *carry + (warp > 0 ? warp_tot[warp - 1] : 0);
+    __syncthreads();
+    if (tid == 1023) *carry = before + incl;
+    __syncthreads();
+    return before + incl - v;
 }
 
-// Persistent: each CTA walks work items w = blockIdx.x, blockIdx.x + gridDim.x, ...
-// over (tile pair, kv head) of the plan; within a sequence the pairs nearest
-// the end (the longest key ranges) come first.
+// Cost classes of the plan's counting sort (key tiles of a pair, clamped).
+constexpr int kPlanBuckets = 2048;
+static_assert(kPlanBuckets == 2 * 1024, "the plan's class scan takes two classes per thread");
+
+// Work list of the chunked-prefill items.  offsets[b] = number of query-tile
+// pairs (two 128-row tiles) of sequences 0..b-1 whose chunk is longer than
+// PA_VERIFY_MAX_Q_ tokens (shorter chunks are decode or speculative-verify
+// rows and belong to the decode kernel); offsets[B] = total.  order[0 ..
+// total) = the global pair indices sorted by the number of key tiles they
+// read, longest first (a counting sort; the order within a cost class is
+// arbitrary and does not affect any result).  One CTA.
+__global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __restrict__ cu_q_lens,
+                                                            const int32_t* __restrict__ seq_lens, int num_seqs,
+                                                            int num_tokens, int q_per_tile,
+                                                            int32_t* __restrict__ offsets, unsigned int* err) {
+    __shared__ int warp_tot[32];
+    __shared__ int carry;
+    __shared__ int hist[kPlanBuckets];
+    int32_t* order = offsets + num_seqs + 1;
+    const int tid = threadIdx.x;
+    if (tid == 0) carry = 0;
+    for (int i = tid; i < kPlanBuckets; i += 1024) hist[i] = 0;
+    __syncthreads();
+    // the pairs of sequence b: count them (offsets) and their cost classes
+    // (a chunk outside the num_tokens query rows has none: its rows cannot be
+    // written, and the pair list stays within num_tokens / 32 + num_seqs)
+    auto pairs_of = [&](int b, int& ql, int& n) {
+        const int c0 = cu_q_lens[b], c1 = cu_q_lens[b + 1];
+        ql = c1 - c0;
+        n = seq_lens[b];
+        if (c0 < 0 || c1 < c0 || c1 > num_tokens) {
+            ql = 0;
+            return 0;
+        }
+        const int tiles = ql > PA_VERIFY_MAX_Q_ ? (ql + q_per_tile - 1) / q_per_tile : 0;
+        return (tiles + kTcTiles - 1) / kTcTiles;
+    };
+    auto bucket = [&](int n, int ql, int pr) {
+        // a malformed sequence (skipped by the kernel) goes to class 0
+        const int c = (n >= ql && ql > 0) ? pair_key_tiles(n, ql, q_per_tile, pr) : 0;
+        return kPlanBuckets - 1 - max(0, min(c, kPlanBuckets - 1));   // longest first
+    };
+    for (int base = 0; base < num_seqs; base += 1024) {
+        const int b = base + tid;
+        int v = 0, ql = 0, n = 0;
+        if (b < num_seqs) {
+            v = pairs_of(b, ql, n);
+            if (ql == 0 && cu_q_lens[b + 1] != cu_q_lens[b]) record_error(err, PA_DEVERR_SEQ_LEN_);
+            for (int pr = 0; pr < v; ++pr) atomicAdd(&hist[bucket(n, ql, pr)], 1);
+        }
+        const int start = block_exclusive_scan_1024(v, warp_tot, &carry);
+        if (b < num_seqs) offsets[b] = start;
+    }
+    if (tid == 0) offsets[num_seqs] = carry;
+    __syncthreads();
+    // bucket starts (exclusive scan of the histogram, two classes per thread)
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    {
+        const int h0 = hist[2 * tid], h1 = hist[2 * tid + 1];
+        const int start = block_exclusive_scan_1024(h0 + h1, warp_tot, &carry);
+        __syncthreads();
+        hist[2 * tid] = start;
+        hist[2 * tid + 1] = start + h0;
+    }
+    __syncthreads();
+    // scatter each pair's global index to its class
+    for (int b = tid; b < num_seqs; b += 1024) {
+        int ql = 0, n = 0;
+        const int v = pairs_of(b, ql, n);
+        const int first = offsets[b];
+        for (int pr = 0; pr < v; ++pr) {
+            // the kernel's pair index l within the sequence counts from the last pair
+            const int l = first + (v - 1 - pr);
+            order[atomicAdd(&hist[bucket(n, ql, pr)], 1)] = l;
+        }
+    }
+}
+
+// Persistent: work item w = (rank, kv head) is pair order[rank] of the plan
+// (pairs sorted by cost, longest first) for kv head w % num_kv_heads.  The
+// CTAs deal the items out like cards in a snake: round k gives CTA i item
+// k * C + i for even k and k * C + C - 1 - i for odd k, so the CTAs' total
+// costs stay even.  (Beside decode rows: pair w / num_kv_heads of the plan's
+// own order, round-robin.)
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const int32_t* __restrict__ plan,
@@ -225,7 +299,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // stay, so that it gets the other SMs
     pdl_trigger();
     int ctas = static_cast<int>(gridDim.x);
-    if (p.decode_units && *p.decode_units > 0) ctas = min(ctas, p.overlap_ctas);
+    // Alone on the GPU, the CTAs take the items in the cost-sorted snake order
+    // (even totals, the kernel ends together).  Beside decode rows, they take
+    // them round-robin in plan order: CTAs that finish early hand their SMs to
+    // the HBM-bound decode kernel sooner, which shortens the step more.
+    const bool snake = !(p.decode_units && *p.decode_units > 0);
+    if (!snake) ctas = min(ctas, p.overlap_ctas);
     const int total_items = plan[p.num_seqs] * p.num_kv_heads;
     if (static_cast<int>(blockIdx.x) >= total_items || static_cast<int>(blockIdx.x) >= ctas) return;
 
@@ -276,7 +355,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // false when the sequence is malformed: every role skips the item
     auto decode_item = [&](int w, Item& it) -> bool {
         it.g = w % p.num_kv_heads;
-        const int l = w / p.num_kv_heads;
+        const int l = snake ? plan[p.num_seqs + 1 + w / p.num_kv_heads] : w / p.num_kv_heads;
         int lo = 0, hi = p.num_seqs - 1;  // last b with plan[b] <= l
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -314,6 +393,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return true;
     };
 
+    // the CTA's k-th item: kNoMoreItems past the end, -1 when round k has
+    // none for this CTA (a partial last round)
+    constexpr int kNoMoreItems = -2;
+    auto item_at = [&](int k) -> int {
+        const long long base = static_cast<long long>(k) * ctas;
+        if (base >= total_items) return kNoMoreItems;
+        const int i = static_cast<int>(blockIdx.x);
+        const long long w = (snake && (k & 1)) ? base + ctas - 1 - i : base + i;
+        return w < total_items ? static_cast<int>(w) : -1;
+    };
+
     // running counters (identical in every role): key tiles loaded so far (the
     // ring position), tiles processed so far per query-tile slot, items so far
     int kv0 = 0;
@@ -339,9 +429,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t s_tm = tmem + lane_base + static_cast<uint32_t>(x * kTcKeys);
         const uint32_t o_tm = tmem + lane_base + static_cast<uint32_t>(kTcTiles * kTcKeys + x * D);
         const bool fold = p.scale_log2 > 0.f;   // scale folded into the exponent's FMA
-        for (int w0 = blockIdx.x; ok && w0 < total_items; w0 += ctas) {
+        for (int k = 0; ok; ++k) {
+            const int w0 = item_at(k);
+            if (w0 == kNoMoreItems) break;
             Item it;
-            if (!decode_item(w0, it)) continue;
+            if (w0 < 0 || !decode_item(w0, it)) continue;
             const int nk = x ? it.nkx[1] : it.nkx[0];
             const int nk_a = it.nkx[0];
             const int q0 = x ? it.q0[1] : it.q0[0];
@@ -552,9 +644,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ============================== MMA issuer ==============================
         reg_dealloc<kTcOtherRegs>();
         int s_issued[kTcTiles] = {0, 0}, pv_issued[kTcTiles] = {0, 0};   // for the abort path
-        for (int w0 = blockIdx.x; ok && w0 < total_items; w0 += ctas) {
+        for (int k = 0; ok; ++k) {
+            const int w0 = item_at(k);
+            if (w0 == kNoMoreItems) break;
             Item it;
-            if (!decode_item(w0, it)) continue;
+            if (w0 < 0 || !decode_item(w0, it)) continue;
             // S_X(j) into S_X: eight MMAs of K=16 over the head dimension
             auto mma_s = [&](int x, int j) {
                 if (lane == 0) {
@@ -665,9 +759,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         constexpr int kHalves = D / 64;
         constexpr int kBoxes = kTcBlocks * kHalves;
         int k_total = 0, v_total = 0;   // K and V tiles issued so far (ring order), for the abort path
-        for (int w0 = blockIdx.x; ok && w0 < total_items; w0 += ctas) {
+        for (int k = 0; ok; ++k) {
+            const int w0 = item_at(k);
+            if (w0 == kNoMoreItems) break;
             Item it;
-            if (!decode_item(w0, it)) continue;
+            if (w0 < 0 || !decode_item(w0, it)) continue;
             if (lane == 0) {
                 auto ids_of = [&](int j, int sk) {
                     // this loader's blocks of tile j, recorded for the V issue
@@ -762,7 +858,8 @@ cudaError_t launch_t(const PrefillParams& p, int32_t* plan, const CUtensorMap& k
         return cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : 0;
     }();
     if (launch_regs < kTcLaunchRegs) return cudaErrorInvalidConfiguration;
-    prefill_plan_kernel<<<1, 1024, 0, s>>>(p.cu_q_lens, p.num_seqs, p.q_per_tile, plan);
+    prefill_plan_kernel<<<1, 1024, 0, s>>>(p.cu_q_lens, p.seq_lens, p.num_seqs, num_tokens, p.q_per_tile, plan,
+                                           p.err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // upper bound on the work items: each listed chunk (length > 8) has at

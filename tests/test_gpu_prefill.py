@@ -53,6 +53,40 @@ def test_prefill_any_scale(scale):
     assert pa.device_error() == 0
 
 
+@pytest.mark.parametrize("last_q,past", [(100, 50), (3, 1)])
+def test_chunk_outside_the_rows_is_flagged(last_q, past):
+    """The last chunk's rows run past the call's num_tokens rows (cu_q_lens
+    inconsistent with q): no row of it is read or written, PA_DEVERR_SEQ_LEN
+    is set, and the other chunks are computed as usual.  A long last chunk
+    goes to the tensor-core kernel, a 3-query one to the decode kernel."""
+    q_lens = [40, 1, 5, last_q]
+    seq_lens = [90, 21, 35, last_q + 10]
+    w = W.build_workload(name="rows", seq_lens=seq_lens, q_lens=q_lens, num_q_heads=8, num_kv_heads=2,
+                         head_dim=128, dtype="bf16", seed=77, device=DEV)
+    seqs = np.arange(w.batch - 1)
+    snap = snapshot(w, seqs)
+    bt = torch.from_numpy(w.block_tables).to(DEV)
+    sl = torch.from_numpy(w.seq_lens).to(DEV)
+    cu = torch.from_numpy(w.cu_q_lens).to(DEV)
+    T = w.num_tokens
+    slots = pa.slot_mapping(bt, sl, cu, T, w.num_blocks)
+    pa.paged_kv_write(w.key, w.value, w.k_cache, w.v_cache, slots)
+    cu_bad = cu.clone()
+    cu_bad[-1] = T + past
+    sentinel = 3.0
+    out_full = torch.full((T + 64, 8, 128), sentinel, dtype=torch.bfloat16, device=DEV)
+    out = out_full[:T]
+    pa.device_error()
+    pa.paged_attention_prefill(w.q, w.k_cache, w.v_cache, bt, sl, cu_bad, w.scale, max(q_lens) + past,
+                               w.max_seq_len, out=out)
+    torch.cuda.synchronize()
+    assert pa.device_error() == 1 << 2          # PA_DEVERR_SEQ_LEN
+    assert bool((out_full[T:] == sentinel).all())          # nothing past the rows
+    assert bool((out[int(w.cu_q_lens[-2]):] == sentinel).all())   # the rejected chunk's rows untouched
+    rows, ref = oracle_rows(w, seqs, snap)
+    assert max_err(out[torch.from_numpy(rows).to(DEV)], ref) <= TOL["bf16"]
+
+
 def test_mixed_step_small():
     w = W.make("mixed", device=DEV, poison=True, n_prefill=3, chunk=150, n_decode=40, prefix_hi=700,
                dec_lo=1, dec_hi=900)
