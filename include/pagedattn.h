@@ -193,7 +193,8 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_p
                    int num_kv_heads, int head_dim, int elem_bytes, void* stream);
 
 /* Workspace for pa_paged_attention_prefill over num_seqs sequences and
- * num_tokens query rows: the chunk tile work list (num_seqs + 1 int32), the
+ * num_tokens query rows: the chunk tile work list (num_seqs + 1 int32 offsets
+ * and a cost-sorted list of num_tokens / 32 + num_seqs int32), the
  * decode kernel's work list, and the split-context partials of up to
  * min(num_tokens, PA_VERIFY_MAX_Q * num_seqs) query rows of decode and verify
  * chunks (partitions of pa_decode_partition(max_seq_len, 0) tokens).  Nonzero whenever

@@ -89,16 +89,19 @@ def test_workspace_sizes(lib):
                                                                 + _partials(8, 64, 64))
     assert pa.decode_workspace_bytes(8, 64, 128, 131072, 512) == (256 + _align(8 * 256 * 4) + 2 * _align(8 * 4)
                                                                   + _partials(8, 64, 256))
-    # prefill: partials rows = min(num_tokens, 8 * num_seqs) (decode and verify chunks)
-    assert pa.prefill_workspace_bytes(8, 8, 64, 128, 131072) == (_align(9 * 4)
+    # prefill: [plan: offsets (B + 1) + cost-sorted pair list (T / 32 + B) int32]
+    # + the decode part, partials rows = min(num_tokens, 8 * num_seqs) (decode and verify chunks)
+    def _plan(B, T):
+        return _align((B + 1 + T // 32 + B) * 4)
+    assert pa.prefill_workspace_bytes(8, 8, 64, 128, 131072) == (_plan(8, 8)
                                                                  + pa.decode_workspace_bytes(8, 64, 128, 131072, 0))
-    assert pa.prefill_workspace_bytes(8, 6000, 64, 128, 131072) == (_align(9 * 4) + 256 + _align(8 * 64 * 4)
+    assert pa.prefill_workspace_bytes(8, 6000, 64, 128, 131072) == (_plan(8, 6000) + 256 + _align(8 * 64 * 4)
                                                                     + _align(8 * 4) + _align(64 * 4)
                                                                     + _partials(64, 64, 64))
-    assert pa.prefill_workspace_bytes(4, 12, 32, 128, 1024) == (_align(5 * 4) + 256 + _align(4 * 2 * 4)
+    assert pa.prefill_workspace_bytes(4, 12, 32, 128, 1024) == (_plan(4, 12) + 256 + _align(4 * 2 * 4)
                                                                 + _align(4 * 4) + _align(12 * 4)
                                                                 + _partials(12, 32, 2))
-    assert pa.prefill_workspace_bytes(2052, 8192, 32, 128, 300) == _align(2053 * 4) + 256 + _align(2052 * 4)
+    assert pa.prefill_workspace_bytes(2052, 8192, 32, 128, 300) == _plan(2052, 8192) + 256 + _align(2052 * 4)
     assert pa.prefill_workspace_bytes(0, 0, 32, 128, 300) == 0
     assert pa.prefill_workspace_bytes(4, -1, 32, 128, 300) == 0
     assert pa.decode_workspace_bytes(0, 32, 128, 300, 0) == 0
