@@ -301,6 +301,17 @@ int pa_paged_attention_decode_noalloc(void* out, const void* q, const void* k_ca
                                       int block_size, int partition_size, int dtype, void* stream);
 
 /*
+ * Failure-path self-test.  Enqueues a one-thread kernel that waits on an
+ * mbarrier phase nothing ever completes, through the same bounded wait the
+ * attention kernels use for their TMA copies and pipeline stages.  The wait
+ * gives up after about one second of polling and records PA_DEVERR_TIMEOUT
+ * in the device error word (read it with pa_get_device_error); the kernel
+ * then returns normally, so the context stays usable.  Returns PA_OK once
+ * enqueued.
+ */
+int pa_selftest_wait_timeout(void* stream);
+
+/*
  * Read the device error word (PA_DEVERR_* bits) of the current device after
  * the work queued on `stream` has finished; `clear` != 0 resets it to 0.
  * This call synchronises the stream.

@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     paged_kv_write,
     paged_kv_write_fp8,
     prefill_workspace_bytes,
+    selftest_wait_timeout,
     slot_mapping,
     device_error,
 )

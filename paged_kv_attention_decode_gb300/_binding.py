@@ -46,6 +46,7 @@ _SIGNATURES = {
                                              _i32, _i32, _i32, _i32, _i32, _p, _sz, _i32, _p]),
     "pa_copy_blocks": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _p]),
     "pa_decode_partition": (_i32, [_i32, _i32]),
+    "pa_selftest_wait_timeout": (_i32, [_p]),
     "pa_paged_kv_gather": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _p]),
 }
 
@@ -144,6 +145,12 @@ def paged_kv_write(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor
                                           v_cache.data_ptr(), slot_mapping.data_ptr(), T, NB, H, D,
                                           bs, _dt(key), _stream(stream))
     _check(rc, "pa_paged_kv_write")
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Enqueue the failure-path self-test (a bounded wait that runs out after
+    about a second and records PA_DEVERR_TIMEOUT)."""
+    _check(load_library().pa_selftest_wait_timeout(_stream(stream)), "pa_selftest_wait_timeout")
 
 
 def decode_partition(max_seq_len: int, partition_size: int = 0) -> int:

@@ -548,6 +548,12 @@ int pa_paged_kv_gather(void* k_out, void* v_out, const void* k_cache, const void
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+int pa_selftest_wait_timeout(void* stream) {
+    unsigned int* err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    return pa::launch_wait_selftest(err, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 int pa_get_device_error(int* code, int clear, void* stream) {
     if (!code) return PA_ERR_INVALID_ARG;
     unsigned int* err = error_word();

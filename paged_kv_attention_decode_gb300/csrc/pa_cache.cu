@@ -272,4 +272,22 @@ cudaError_t launch_kv_gather(void* k_out, void* v_out, const void* k_cache, cons
     return cudaGetLastError();
 }
 
+// Failure-path self-test: one thread waits on an mbarrier phase that nothing
+// ever completes, through the same bounded wait as the attention kernels.
+// The wait gives up (about a second) and the kernel records the timeout and
+// returns normally.
+__global__ void wait_selftest_kernel(unsigned int* err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+        if (!mbar_wait(&bar, 0)) record_error(err, PA_DEVERR_TIMEOUT_);
+    }
+}
+
+cudaError_t launch_wait_selftest(unsigned int* err, cudaStream_t s) {
+    wait_selftest_kernel<<<1, 32, 0, s>>>(err);
+    return cudaGetLastError();
+}
+
 }  // namespace pa

@@ -81,13 +81,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase.  Returns false after kMaxWaitIters
-// unsuccessful polls (each poll may suspend the thread for a short,
-// hardware-chosen time); the caller records PA_DEVERR_TIMEOUT and leaves.
-constexpr uint32_t kMaxWaitIters = 1u << 20;
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase.  Gives up after kWaitLimitNs of polling
+// (checked every 256 polls; each poll may suspend the thread for a short,
+// hardware-chosen time) or kMaxWaitIters polls, whichever comes first, and
+// returns false; the caller records PA_DEVERR_TIMEOUT and leaves.  A phase
+// that completes is seen on the first poll after it.
+constexpr uint32_t kMaxWaitIters = 1u << 26;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // one second
+__device__ __forceinline__ bool wait_timed_out(uint32_t i, uint64_t& t0) {
+    if ((i & 255u) != 255u) return false;
+    const uint64_t t = global_ns();
+    if (i == 255u) t0 = t;   // the clock starts after the first polls (a phase about to complete costs nothing)
+    return t - t0 > kWaitLimitNs;
+}
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kMaxWaitIters; ++i)
+    uint64_t t0 = 0;
+    for (uint32_t i = 0; i < kMaxWaitIters; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (wait_timed_out(i, t0)) return false;
+    }
     return false;
 }
 

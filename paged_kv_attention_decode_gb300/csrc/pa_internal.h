@@ -126,6 +126,8 @@ cudaError_t launch_kv_gather(void* k_out, void* v_out, const void* k_cache, cons
                              const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
                              const int32_t* cu_seq_lens, int num_seqs, int num_blocks, int64_t row_bytes,
                              int max_seq_len, unsigned int* err, cudaStream_t s);
+// One-thread kernel whose bounded mbarrier wait runs out (records a timeout).
+cudaError_t launch_wait_selftest(unsigned int* err, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            int head_dim, int dtype, int max_q_len, cudaStream_t s);
 // tcgen05 prefill: groups of 1, 2, 4 or 8 q heads per kv head; q_per_tile = 128 / group.

@@ -92,8 +92,10 @@ __device__ __forceinline__ void reg_dealloc() {
 // Bounded mbarrier wait that also gives up when another thread of the CTA has
 // already recorded a failure.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    uint64_t t0 = 0;
     for (uint32_t i = 0; i < kMaxWaitIters; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (wait_timed_out(i, t0)) return false;
         if ((i & 1023u) == 1023u && *abort_flag) return false;
     }
     return false;
