@@ -12,8 +12,10 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 # (q_len, cached prefix) per sequence: chunks shorter and longer than a tile,
-# ragged block and tile tails, empty and long prefixes, decode rows mixed in.
-CASES = [(2, 0), (17, 0), (64, 0), (65, 3), (100, 200), (1, 50), (130, 1000), (33, 15), (1, 1), (300, 17)]
+# ragged block and tile tails, empty and long prefixes, decode rows mixed in,
+# and a sequence with no new rows this step (q_len 0).
+CASES = [(2, 0), (17, 0), (64, 0), (65, 3), (100, 200), (1, 50), (0, 40), (130, 1000), (33, 15), (1, 1),
+         (300, 17)]
 
 
 @pytest.mark.parametrize("Hq,Hkv,D,dtype", [
