@@ -529,8 +529,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const float new_ref = fmaxf(m_ref, mx);
                         const float alpha = new_ref == -INFINITY ? 1.f : fast_exp2(m_ref - new_ref);
                         if (j > 0) {
-#pragma unroll
-                            for (int c0 = 0; c0 < D / 32; ++c0) {
+#pragma unroll 1
+                            for (int c0 = 0; c0 < D / 32; ++c0) {   // (rare: kept rolled)
                                 uint32_t rr[32];
                                 tmem_ld32(o_tm + static_cast<uint32_t>(c0 * 32), rr);
                                 tmem_ld_wait();
@@ -548,13 +548,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // order)
                     {
                         const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-                        if (fold) {
+                        // s * 1 + (-ref) rounds once, like s - ref: one loop for both
+                        const float mul = fold ? p.scale_log2 : 1.f;
 #pragma unroll
-                            for (int c = 0; c < kTcKeys; c += 2) fma2(sv[c], sv[c + 1], p.scale_log2, -ref);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < kTcKeys; c += 2) add2(sv[c], sv[c + 1], -ref, -ref);
-                        }
+                        for (int c = 0; c < kTcKeys; c += 2) fma2(sv[c], sv[c + 1], mul, -ref);
 #pragma unroll
                         for (int c = 0; c < kTcKeys; ++c) sv[c] = fast_exp2(sv[c]);
                         float sq[4] = {0.f, 0.f, 0.f, 0.f};
@@ -609,8 +606,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const int64_t grow =
                             static_cast<int64_t>(it.row0 + qi_row) * p.num_q_heads + it.g * G + (r % G);
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + grow * D);
-#pragma unroll
-                        for (int c0 = 0; c0 < D / 32; ++c0) {
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D / 32; ++c0) {   // (once per item: kept rolled)
                             uint32_t rr[32];
                             tmem_ld32(o_tm + static_cast<uint32_t>(c0 * 32), rr);
                             tmem_ld_wait();
