@@ -8,20 +8,24 @@
 // One persistent CTA per SM.  A work item is a pair of adjacent 128-row query
 // tiles, A and B (rows = (query, q head) pairs of one kv group; TMEM lane r =
 // row r), that share one stream of 128-key K/V tiles: every K/V byte loaded
-// feeds two tiles of MMAs.  Warp roles:
+// feeds two tiles of MMAs.  A plan kernel sorts the pairs by cost and the
+// CTAs deal them out in a snake (even totals); beside decode rows they take
+// them round-robin instead.  One role per warpgroup for the whole kernel:
 //   * warps 0-3: softmax of tile A, warps 4-7: softmax of tile B (thread r of
-//     a group = row r);
+//     a group = row r), with 224 registers each (setmaxnreg) so that a row's
+//     128 scores stay in registers;
 //   * warp 8, lane 0: every tcgen05.mma;
 //   * warps 9-11: the TMA loads (Q tiles; K and V tiles gathered block by
 //     block through the block table into a ring of K stages and a ring of V
 //     stages).  TMA issue is costly per issuing thread, so the boxes of a
-//     tile are split over three warps.
+//     tile are split over three warps.  Warps 8-11 keep 56 registers.
 // Tensor memory (512 columns): S_A | S_B (128 columns each) | O_A | O_B.
 // Per key tile j and query tile X:
 //   S_X(j) = Q_X K(j)^T   M=128 N=128, eight MMAs of K=16;
-//   softmax_X(j)          tcgen05.ld of the S row (two passes: maximum, then
-//                          exponentials), running reference m_ref and sum l;
-//                          P (bf16/fp16) is stored over the row's S;
+//   softmax_X(j)          one tcgen05.ld wait for the S row, its maximum, the
+//                          running reference m_ref and sum l, exponentials
+//                          with paired fp32 instructions; P (bf16/fp16) is
+//                          stored over the row's S;
 //   O_X += P_X(j) V(j)    M=128 N=D, eight MMAs of K=16, A read from tensor
 //                          memory.
 // A tcgen05.mma instruction of M=128 costs the tensor pipe about the same time
