@@ -84,8 +84,8 @@ bool make_kv_map_block(CUtensorMap* map, const void* base, int num_blocks, int n
 
 // Tensor map over the query rows [T, Hq, D] viewed as 4-D (64-element row
 // piece, D/64 pieces, q head, token); one box = one 64-dim half of the `group`
-// heads of `q_per_tile` consecutive tokens, i.e. 128 rows of 128 bytes whose
-// row index is token * group + head.
+// heads of `q_per_tile` consecutive tokens, i.e. q_per_tile * group <= 128
+// rows of 128 bytes whose row index is token * group + head.
 bool make_q_map(CUtensorMap* map, const void* q, int num_tokens, int num_q_heads, int head_dim, int group,
                 int q_per_tile, int dtype) {
     auto fn = encode_fn();
@@ -451,7 +451,6 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
     if (!aligned256(workspace)) return PA_ERR_INVALID_ARG;
     int32_t* plan = static_cast<int32_t*>(workspace);
     const int group = num_q_heads / num_kv_heads;
-    const bool tc = group == 1 || group == 2 || group == 4 || group == 8;
     // decode rows (q_len == 1) and speculative-verify rows (q_len <= PA_VERIFY_MAX_Q)
     // through the decode kernel
     const int max_q = std::max(1, std::min(max_q_len, PA_VERIFY_MAX_Q));
@@ -479,34 +478,23 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
     p.group = group;
     p.scale_log2 = scale_log2(scale);
     CUtensorMap kmap, vmap;
-    cudaError_t e;
-    if (tc) {
-        // 128-row tiles on the tcgen05 tensor cores, running beside the decode
-        // rows: the decode plan and the prefill kernel go first; the decode
-        // kernel then starts on the SMs the prefill kernel leaves free
-        if (!make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) ||
-            !make_kv_map(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype))
-            return PA_ERR_CUDA;
-        p.q_per_tile = 128 / group;
-        CUtensorMap qmap;
-        if (!make_q_map(&qmap, q, num_tokens, num_q_heads, head_dim, group, p.q_per_tile, dtype)) return PA_ERR_CUDA;
-        if (pa::launch_decode_plan(dc.p, s) != cudaSuccess) return PA_ERR_CUDA;
-        p.decode_units = dc.p.unit_count;
-        p.overlap_ctas = std::max(1, pa::sm_count() * kOverlapPrefillNum / kOverlapPrefillDen);
-        e = pa::launch_prefill_tc(p, plan, kmap, vmap, qmap, head_dim, dtype, max_q_len, num_tokens, s);
-        if (e != cudaSuccess) return PA_ERR_CUDA;
-        dc.p.overlap = 1;
-        return decode_launch(dc, s);
-    }
-    // other groupings: 64-row mma.sync tiles after the decode rows
-    rc = decode_launch(dc, s);
-    if (rc) return rc;
+    // tiles of 128 / group queries (every supported grouping) on the tcgen05
+    // tensor cores, running beside the decode rows: the decode plan and the
+    // prefill kernel go first; the decode kernel then starts on the SMs the
+    // prefill kernel leaves free
     if (!make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) ||
         !make_kv_map(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype))
         return PA_ERR_CUDA;
-    p.q_per_tile = 64 / group;
-    e = pa::launch_prefill(p, kmap, vmap, head_dim, dtype, max_q_len, s);
-    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    p.q_per_tile = 128 / group;
+    CUtensorMap qmap;
+    if (!make_q_map(&qmap, q, num_tokens, num_q_heads, head_dim, group, p.q_per_tile, dtype)) return PA_ERR_CUDA;
+    if (pa::launch_decode_plan(dc.p, s) != cudaSuccess) return PA_ERR_CUDA;
+    p.decode_units = dc.p.unit_count;
+    p.overlap_ctas = std::max(1, pa::sm_count() * kOverlapPrefillNum / kOverlapPrefillDen);
+    if (pa::launch_prefill_tc(p, plan, kmap, vmap, qmap, head_dim, dtype, max_q_len, num_tokens, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    dc.p.overlap = 1;
+    return decode_launch(dc, s);
 }
 
 int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs, int num_blocks,

@@ -92,7 +92,7 @@ struct PrefillParams {
     int num_q_heads;
     int num_kv_heads;
     int group;
-    int q_per_tile;               // queries per tile: rows = q_per_tile * group (128 tcgen05, 64 mma.sync)
+    int q_per_tile;               // queries per tile: rows = q_per_tile * group <= 128
     float scale_log2;
     // when *decode_units > 0 (decode rows will run next to this kernel), only
     // the first overlap_ctas CTAs take prefill work; the others leave their SMs
@@ -128,9 +128,7 @@ cudaError_t launch_kv_gather(void* k_out, void* v_out, const void* k_cache, cons
                              int max_seq_len, unsigned int* err, cudaStream_t s);
 // One-thread kernel whose bounded mbarrier wait runs out (records a timeout).
 cudaError_t launch_wait_selftest(unsigned int* err, cudaStream_t s);
-cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           int head_dim, int dtype, int max_q_len, cudaStream_t s);
-// tcgen05 prefill: groups of 1, 2, 4 or 8 q heads per kv head; q_per_tile = 128 / group.
+// tcgen05 prefill: groups of 1 to 8 q heads per kv head; q_per_tile = 128 / group.
 // `plan` is device scratch of num_seqs + 1 int32 (the work list of query-tile pairs).
 cudaError_t launch_prefill_tc(const PrefillParams& p, int32_t* plan, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, const CUtensorMap& qmap, int head_dim, int dtype,

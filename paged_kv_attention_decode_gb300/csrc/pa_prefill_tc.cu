@@ -1,9 +1,9 @@
 // Chunked-prefill attention on the 5th-generation tensor cores (tcgen05).
 //
-// Same operation as prefill_kernel in pa_prefill.cu ("vLLM-Ascend 原理",
+// Causal attention of query chunks on their cached prefix ("vLLM-Ascend 原理",
 // section 2.3 "因果自注意力": query at position i sees positions 0..i; section
 // 2.4: a later chunk reads the KV earlier chunks wrote), for query groups of
-// 1, 2, 4 or 8 heads per kv head.
+// 1 to 8 heads per kv head (a tile holds 128 / G queries of G heads).
 //
 // One persistent CTA per SM.  A work item is a pair of adjacent 128-row query
 // tiles, A and B (rows = (query, q head) pairs of one kv group; TMEM lane r =
@@ -320,6 +320,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     auto kst = [&](int s) { return smem + kTcTiles * Sh::kQ + s * Sh::kKV; };
     auto vst = [&](int s) { return smem + kTcTiles * Sh::kQ + (NK + s) * Sh::kKV; };
 
+    // A tile holds q_per_tile queries x G heads <= 128 rows (fewer when G does
+    // not divide 128).  The rows past them are never loaded: zero them once,
+    // so their scores stay finite and quiet.
+    const int q_rows = QT * G;
+    const int q_tile_bytes = q_rows * 128 * (D / 64);
+    if (q_rows < 128) {
+        const int n16 = (128 - q_rows) * 8;   // 16-byte chunks past the loaded rows, per 64-dim half
+        for (int i = tid; i < kTcTiles * (D / 64) * n16; i += kTcThreads) {
+            const int half = i / n16;         // (tile, half) = smem + half * kQHalf
+            reinterpret_cast<uint4*>(smem + half * Sh::kQHalf + q_rows * 128)[i - half * n16] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
     if (warp == 0) {
         tmem_alloc(&tmem_slot, kTmemCols);
         tmem_relinquish();
@@ -815,7 +828,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (li == 0) {
                     if (items > 0) ok = wait_or_abort(&item_done, (items - 1) & 1, abort_v);
                     if (ok) {
-                        mbar_arrive_expect_tx(&q_full, static_cast<uint32_t>((it.nkx[1] ? 2 : 1) * Sh::kQ));
+                        mbar_arrive_expect_tx(&q_full, static_cast<uint32_t>((it.nkx[1] ? 2 : 1) * q_tile_bytes));
 #pragma unroll
                         for (int x = 0; x < kTcTiles; ++x) {
                             if (!it.nkx[x]) continue;
