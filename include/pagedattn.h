@@ -24,7 +24,8 @@
  *   key, value        [num_tokens, num_kv_heads, head_dim] (new tokens).
  *
  * Supported: block_size == 16, head_dim in {64, 128}, dtype fp16 or bf16,
- * num_q_heads % num_kv_heads == 0 with num_q_heads / num_kv_heads <= 8;
+ * num_q_heads % num_kv_heads == 0 with num_q_heads / num_kv_heads <= PA_MAX_GROUP
+ * (64: grouped-query and multi-query attention);
  * q head h reads kv head h / (num_q_heads / num_kv_heads).
  *
  * Ownership: the caller owns every buffer.  The library allocates no device
@@ -59,7 +60,7 @@ extern "C" {
  * more than PA_AUTO_MAX_PARTS partitions (see pa_decode_partition). */
 #define PA_AUTO_MAX_PARTS 64
 #define PA_MAX_AUTO_PARTITION 8192
-#define PA_MAX_GROUP 8
+#define PA_MAX_GROUP 64
 /* Chunks of at most this many queries (decode rows, speculative-verify rows)
  * run in the decode kernel inside pa_paged_attention_prefill. */
 #define PA_VERIFY_MAX_Q 8
@@ -194,7 +195,7 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_p
 
 /* Workspace for pa_paged_attention_prefill over num_seqs sequences and
  * num_tokens query rows: the chunk tile work list (num_seqs + 1 int32 offsets
- * and a cost-sorted list of num_tokens / 32 + num_seqs int32), the
+ * and a cost-sorted list of num_tokens / 4 + num_seqs int32), the
  * decode kernel's work list, and the split-context partials of up to
  * min(num_tokens, PA_VERIFY_MAX_Q * num_seqs) query rows of decode and verify
  * chunks (partitions of pa_decode_partition(max_seq_len, 0) tokens).  Nonzero whenever

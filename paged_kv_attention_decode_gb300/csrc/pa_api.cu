@@ -318,8 +318,9 @@ static int decode_prepare(DecodeCall& c, void* out, const void* q, const void* k
     p.max_rows = max_rows;
     p.num_rows = num_rows;
     // (query, head) columns per work item: 8, or 16 once a row can have more
+    // (the FP8 kernels take 8 per item)
     const int cols = max_q * p.group;
-    const int chunk = cols > 8 ? 16 : 8;
+    const int chunk = (cols > 8 && !fp8) ? 16 : 8;
     p.col_chunks = (cols + chunk - 1) / chunk;
     p.scale_log2 = scale_log2(scale) * k_scale;
     p.v_scale = v_scale;
@@ -370,10 +371,11 @@ int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, con
 
 // Prefill workspace: [tile work list: num_seqs + 1 int32, 256-aligned][decode-row partials].
 // prefill plan: offsets (num_seqs + 1) and the cost-sorted pair list.  A pair
-// is two tiles of at least 16 queries (128 rows / at most 8 heads), so a chunk
-// of q queries has at most q / 32 + 1 pairs.
+// is two tiles of at least 2 queries (128 rows / at most PA_MAX_GROUP = 64
+// heads), so a chunk of q queries has at most q / 4 + 1 pairs.
+static_assert(PA_MAX_GROUP <= 64, "the plan's pair bound assumes tiles of at least 2 queries");
 static size_t plan_bytes(int num_seqs, int num_tokens) {
-    const size_t pairs = static_cast<size_t>(num_tokens) / 32 + static_cast<size_t>(num_seqs);
+    const size_t pairs = static_cast<size_t>(num_tokens) / 4 + static_cast<size_t>(num_seqs);
     return align256((static_cast<size_t>(num_seqs) + 1 + pairs) * sizeof(int32_t));
 }
 

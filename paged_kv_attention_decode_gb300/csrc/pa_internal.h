@@ -128,7 +128,7 @@ cudaError_t launch_kv_gather(void* k_out, void* v_out, const void* k_cache, cons
                              int max_seq_len, unsigned int* err, cudaStream_t s);
 // One-thread kernel whose bounded mbarrier wait runs out (records a timeout).
 cudaError_t launch_wait_selftest(unsigned int* err, cudaStream_t s);
-// tcgen05 prefill: groups of 1 to 8 q heads per kv head; q_per_tile = 128 / group.
+// tcgen05 prefill: groups of 1 to PA_MAX_GROUP q heads per kv head; q_per_tile = 128 / group.
 // `plan` is device scratch of num_seqs + 1 int32 (the work list of query-tile pairs).
 cudaError_t launch_prefill_tc(const PrefillParams& p, int32_t* plan, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, const CUtensorMap& qmap, int head_dim, int dtype,

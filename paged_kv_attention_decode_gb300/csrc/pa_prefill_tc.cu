@@ -3,7 +3,7 @@
 // Causal attention of query chunks on their cached prefix ("vLLM-Ascend 原理",
 // section 2.3 "因果自注意力": query at position i sees positions 0..i; section
 // 2.4: a later chunk reads the KV earlier chunks wrote), for query groups of
-// 1 to 8 heads per kv head (a tile holds 128 / G queries of G heads).
+// 1 to 64 heads per kv head (a tile holds 128 / G queries of G heads).
 //
 // One persistent CTA per SM.  A work item is a pair of adjacent 128-row query
 // tiles, A and B (rows = (query, q head) pairs of one kv group; TMEM lane r =
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
     __syncthreads();
     // the pairs of sequence b: count them (offsets) and their cost classes
     // (a chunk outside the num_tokens query rows has none: its rows cannot be
-    // written, and the pair list stays within num_tokens / 32 + num_seqs)
+    // written, and the pair list stays within num_tokens / 4 + num_seqs)
     auto pairs_of = [&](int b, int& ql, int& n) {
         const int c0 = cu_q_lens[b], c1 = cu_q_lens[b + 1];
         ql = c1 - c0;

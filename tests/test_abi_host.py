@@ -89,10 +89,10 @@ def test_workspace_sizes(lib):
                                                                 + _partials(8, 64, 64))
     assert pa.decode_workspace_bytes(8, 64, 128, 131072, 512) == (256 + _align(8 * 256 * 4) + 2 * _align(8 * 4)
                                                                   + _partials(8, 64, 256))
-    # prefill: [plan: offsets (B + 1) + cost-sorted pair list (T / 32 + B) int32]
+    # prefill: [plan: offsets (B + 1) + cost-sorted pair list (T / 4 + B) int32]
     # + the decode part, partials rows = min(num_tokens, 8 * num_seqs) (decode and verify chunks)
     def _plan(B, T):
-        return _align((B + 1 + T // 32 + B) * 4)
+        return _align((B + 1 + T // 4 + B) * 4)
     assert pa.prefill_workspace_bytes(8, 8, 64, 128, 131072) == (_plan(8, 8)
                                                                  + pa.decode_workspace_bytes(8, 64, 128, 131072, 0))
     assert pa.prefill_workspace_bytes(8, 6000, 64, 128, 131072) == (_plan(8, 6000) + 256 + _align(8 * 64 * 4)
@@ -121,7 +121,7 @@ def _decode(lib, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(dt=7), 2), (dict(d=96), 2), (dict(bs=32), 2), (dict(hq=5, hkv=2), 1),
-    (dict(hq=32, hkv=2), 2), (dict(part=17), 1), (dict(part=-16), 1), (dict(q=None), 1),
+    (dict(hq=65, hkv=1), 2), (dict(hq=64, hkv=1), 3), (dict(part=17), 1), (dict(part=-16), 1), (dict(q=None), 1),
     (dict(out=FAKE + 2), 1), (dict(B=-1), 1), (dict(nb=0), 1), (dict(scale=float("nan")), 1),
     (dict(maxlen=4096, part=512), 3), (dict(maxlen=4096, ws=FAKE, wsb=10), 3), (dict(maxlen=16), 3),
     (dict(maxlen=1 << 24, part=16), 1),

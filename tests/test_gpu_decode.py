@@ -37,6 +37,8 @@ def test_tiny_workload():
     (4, 4, 64, "f16"), (8, 8, 128, "f16"), (8, 8, 128, "bf16"), (8, 4, 128, "bf16"),
     (16, 4, 128, "bf16"), (16, 2, 64, "f16"), (24, 3, 128, "bf16"), (8, 1, 128, "f16"),
     (12, 4, 64, "bf16"), (7, 7, 128, "f16"),
+    # large groups: 16 and 32 (multi-query) heads per kv head, and the limit
+    (32, 2, 128, "bf16"), (32, 1, 128, "f16"), (64, 1, 64, "bf16"),
 ])
 @pytest.mark.parametrize("partition", [0, 16, 48, 4096])
 def test_decode_parity(Hq, Hkv, D, dtype, partition):

@@ -39,7 +39,7 @@ def test_fp8_write_is_bit_exact(src):
 
 
 @pytest.mark.parametrize("Hq,Hkv,dtype", [(8, 8, "f16"), (8, 8, "bf16"), (16, 4, "bf16"), (16, 2, "f16"),
-                                          (12, 4, "bf16")])
+                                          (12, 4, "bf16"), (32, 2, "bf16"), (32, 1, "f16")])
 @pytest.mark.parametrize("partition", [0, 48])
 def test_fp8_decode_step_parity(Hq, Hkv, dtype, partition):
     w = W.build_workload(name="f8", seq_lens=LENS, q_lens=1, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128,

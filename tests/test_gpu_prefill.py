@@ -23,6 +23,8 @@ CASES = [(2, 0), (17, 0), (64, 0), (65, 3), (100, 200), (1, 50), (0, 40), (130, 
     (16, 2, 128, "f16"),
     # groupings that do not divide 128 rows: tiles of 42, 25, 21 and 18 queries
     (28, 4, 128, "bf16"), (10, 2, 64, "f16"), (12, 2, 128, "bf16"), (7, 1, 128, "f16"),
+    # 16, 32 and 64 heads per kv head: tiles of 8, 4 and 2 queries
+    (32, 2, 128, "bf16"), (32, 1, 128, "f16"), (64, 1, 64, "bf16"),
 ])
 def test_prefill_parity(Hq, Hkv, D, dtype):
     q_lens = [c[0] for c in CASES]

@@ -25,6 +25,7 @@ CASES = [(1, 0), (2, 0), (8, 0), (3, 13), (4, 16), (5, 509), (8, 505), (6, 511),
 @pytest.mark.parametrize("Hq,Hkv,D,dtype", [
     (32, 8, 128, "bf16"), (8, 8, 128, "f16"), (16, 2, 128, "f16"), (6, 2, 64, "bf16"), (8, 4, 64, "f16"),
     (14, 2, 128, "bf16"), (12, 2, 64, "f16"),
+    (32, 2, 128, "bf16"), (32, 1, 64, "f16"),      # 16 and 32 heads per kv head
 ])
 def test_verify_rows_parity(Hq, Hkv, D, dtype):
     q_lens = [c[0] for c in CASES]
