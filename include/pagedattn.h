@@ -169,8 +169,11 @@ int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, con
  * copy); it exists to check the index translation byte for byte.
  *   k_out, v_out  [cu_seq_lens[num_seqs], num_kv_heads, head_dim], device
  *   cu_seq_lens   device int32 [num_seqs + 1], exclusive prefix sum of seq_lens
- *   elem_bytes    2 (fp16/bf16 pools) or 1 (FP8 pools)
- * Row b, t receives cache[table[b][t / 16], t % 16] for t < seq_lens[b].  A
+ *   elem_bytes    2 (fp16/bf16 pools, [num_blocks, 16, num_kv_heads, head_dim])
+ *                 or 1 (FP8 pools, head-major [num_blocks, num_kv_heads, 16,
+ *                 head_dim]); the output rows are token-major either way
+ * Row b, t receives cache[table[b][t / 16], t % 16] for t < seq_lens[b]
+ * (for FP8 pools, cache[table[b][t / 16], h, t % 16] for each head h).  A
  * table entry outside [0, num_blocks) zero-fills its rows and sets
  * PA_DEVERR_BLOCK_ID; a length that disagrees with cu_seq_lens or exceeds the
  * table sets PA_DEVERR_SEQ_LEN and skips the sequence.
@@ -242,9 +245,15 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
  * FP8 (E4M3) KV cache ("vLLM-Ascend 原理", section 4 "量化": k and v are
  * quantised to 8 bits as they are written and dequantised after they are read
  * through the block table; the cache takes half the HBM and half the bytes
- * per decode step).  Codes are OCP E4M3 ("FN"), one byte per element, same
- * [num_blocks, block_size, num_kv_heads, head_dim] layout; one fp32 scale per
- * pool: value = code * scale.  head_dim must be 128.
+ * per decode step).  Codes are OCP E4M3 ("FN"), one byte per element; one
+ * fp32 scale per pool: value = code * scale.  head_dim must be 128.
+ *
+ * FP8 pools are head-major: [num_blocks, num_kv_heads, block_size, head_dim],
+ * so the 16 rows of one (block, kv head) tile are one contiguous 2 KB run
+ * (a 128-byte row per token would otherwise sit num_kv_heads * 128 bytes
+ * from the next).  Slot s = block * 16 + offset holds head h's codes at
+ * cache[s / 16][h][s % 16][:].  pa_copy_blocks moves whole blocks and works
+ * on either layout; pa_paged_kv_gather reads FP8 pools in this order.
  *
  * pa_paged_kv_write_fp8 stores code = e4m3(float(x) * (1.0f / scale)) for each
  * new element x (fp16/bf16 `src_dtype`): one fp32 multiply, round to nearest

@@ -174,13 +174,15 @@ def encode_e4m3(values) -> np.ndarray:
 
 def kv_write_fp8(key_bits, value_bits, k_cache_codes, v_cache_codes, slots, src_dtype: str,
                  k_scale: float, v_scale: float) -> None:
-    """In place: cache[slot] = e4m3(float(x) * float32(1 / scale)) for every slot >= 0."""
+    """In place, for every slot >= 0 and head h:
+    cache[slot // bs, h, slot % bs] = e4m3(float(x) * float32(1 / scale)).
+    The E4M3 pools are head-major [NB, Hkv, bs, D]."""
     key_bits = _c(key_bits, np.uint16)
     value_bits = _c(value_bits, np.uint16)
     slots = _c(slots, np.int64)
     assert k_cache_codes.dtype == np.uint8 and k_cache_codes.flags.c_contiguous
     assert v_cache_codes.dtype == np.uint8 and v_cache_codes.flags.c_contiguous
-    NB, bs, H, D = k_cache_codes.shape
+    NB, H, bs, D = k_cache_codes.shape
     k_inv = float(np.float32(1.0) / np.float32(k_scale))
     v_inv = float(np.float32(1.0) / np.float32(v_scale))
     _check(_load().oracle_kv_write_fp8(_ptr(key_bits), _ptr(value_bits), _ptr(k_cache_codes),
@@ -191,10 +193,11 @@ def kv_write_fp8(key_bits, value_bits, k_cache_codes, v_cache_codes, slots, src_
 def paged_attention_decode_fp8(q_bits, k_cache_codes, v_cache_codes, block_tables, seq_lens, scale: float,
                                q_dtype: str, k_scale: float, v_scale: float, select=None,
                                threads: int = 0) -> np.ndarray:
-    """fp64 decode attention over an E4M3 cache (values = code * scale)."""
+    """fp64 decode attention over a head-major E4M3 cache [NB, Hkv, bs, D]
+    (values = code * scale)."""
     q_bits = _c(q_bits, np.uint16)
     B, Hq, D = q_bits.shape
-    NB, bs, Hkv, D2 = k_cache_codes.shape
+    NB, Hkv, bs, D2 = k_cache_codes.shape
     assert D2 == D
     kc = _c(k_cache_codes, np.uint8)
     vc = _c(v_cache_codes, np.uint8)

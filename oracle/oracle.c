@@ -215,8 +215,9 @@ int oracle_encode_e4m3(const float* in, uint8_t* out, int64_t n) {
 /* Quantising cache write ("vLLM-Ascend 原理", section 4 "量化": the k and v of
  * a decode step are quantised as they are written into the cache).  Each new
  * element is decoded from its fp16/bf16 pattern, multiplied in fp32 by the
- * fp32 reciprocal scale, and stored as its E4M3 code:
- *   cache[slot / bs][slot % bs][h][d] = e4m3(float(x) * inv_scale). */
+ * fp32 reciprocal scale, and stored as its E4M3 code.  E4M3 pools are
+ * head-major ([block][head][offset][d], the library's FP8 layout):
+ *   cache[slot / bs][h][slot % bs][d] = e4m3(float(x) * inv_scale). */
 int oracle_kv_write_fp8(const uint16_t* key, const uint16_t* value, uint8_t* k_cache, uint8_t* v_cache,
                         const int64_t* slots, int64_t T, int num_blocks, int num_kv_heads, int head_dim,
                         int block_size, int src_dtype, float k_inv_scale, float v_inv_scale) {
@@ -229,7 +230,8 @@ int oracle_kv_write_fp8(const uint16_t* key, const uint16_t* value, uint8_t* k_c
         if (slot >= num_slots) return OR_ERR_SLOT;
         for (int h = 0; h < num_kv_heads; ++h) {
             for (int d = 0; d < head_dim; ++d) {
-                int64_t dst = (slot * num_kv_heads + h) * head_dim + d;
+                int64_t blk = slot / block_size, off = slot % block_size;
+                int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * head_dim + d;
                 int64_t src = (t * num_kv_heads + h) * head_dim + d;
                 float kx = (float)tab[key[src]];     /* exact: fp16/bf16 values are floats */
                 float vx = (float)tab[value[src]];
@@ -285,7 +287,7 @@ static int attend_one(const job_t* J, int64_t r, int h, double* s, double* qd, d
         const int64_t koff = ((phys * bs + off) * J->Hkv + g) * D;
         double dot = 0.0;
         if (J->k8) {
-            const uint8_t* kp = J->k8 + koff;
+            const uint8_t* kp = J->k8 + ((phys * J->Hkv + g) * bs + off) * D;   /* head-major */
             for (int d = 0; d < D; ++d) dot += qd[d] * (J->tab8[kp[d]] * J->k_scale);
         } else {
             const uint16_t* kp = J->k_cache + koff;
@@ -303,7 +305,7 @@ static int attend_one(const job_t* J, int64_t r, int h, double* s, double* qd, d
         double w = exp(s[t] - M);
         L += w;
         if (J->v8) {
-            const uint8_t* vp = J->v8 + voff;
+            const uint8_t* vp = J->v8 + ((phys * J->Hkv + g) * bs + off) * D;   /* head-major */
             for (int d = 0; d < D; ++d) acc[d] += w * (J->tab8[vp[d]] * J->v_scale);
         } else {
             const uint16_t* vp = J->v_cache + voff;
@@ -448,7 +450,8 @@ int oracle_paged_attention_prefill(double* out, const uint16_t* q, const uint16_
     return rc;
 }
 
-/* Decode attention over an E4M3 cache: k_t = e4m3(code) * k_scale and
+/* Decode attention over a head-major E4M3 cache ([block][head][offset][d]):
+ * k_t = e4m3(code) * k_scale and
  * v_t = e4m3(code) * v_scale ("vLLM-Ascend 原理", section 4 "量化": blocks
  * are dequantised after being read through the block table), then the same
  * two-pass softmax as oracle_paged_attention_decode, in fp64. */

@@ -250,11 +250,15 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, pairs: torch.Tenso
 def paged_kv_gather(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                     seq_lens: torch.Tensor, max_seq_len: int, stream=None):
     """Test support: every sequence's live K/V rows, gathered through its block
-    table into contiguous [sum(seq_lens), Hkv, D] tensors."""
+    table into contiguous [sum(seq_lens), Hkv, D] tensors.  16-bit pools are
+    [NB, 16, Hkv, D]; one-byte (FP8) pools are head-major [NB, Hkv, 16, D]."""
     _cuda(k_cache, v_cache, block_tables, seq_lens)
     _need(block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32, "int32 tables")
     _need(v_cache.shape == k_cache.shape and v_cache.dtype == k_cache.dtype, "cache shape/dtype")
-    NB, bs, H, D = k_cache.shape
+    if k_cache.element_size() == 1:
+        NB, H, bs, D = k_cache.shape
+    else:
+        NB, bs, H, D = k_cache.shape
     B = seq_lens.shape[0]
     cu = torch.zeros(B + 1, dtype=torch.int32, device=seq_lens.device)
     torch.cumsum(seq_lens, 0, out=cu[1:])
@@ -288,11 +292,12 @@ def _u8(t: torch.Tensor) -> torch.Tensor:
 
 def paged_kv_write_fp8(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                        slot_mapping: torch.Tensor, k_scale: float, v_scale: float, stream=None) -> None:
-    """In place: E4M3 codes of key/value * (1 / scale) into the FP8 pools (slot < 0: skipped)."""
+    """In place: E4M3 codes of key/value * (1 / scale) into the head-major FP8
+    pools [NB, Hkv, 16, D] (slot < 0: skipped)."""
     _cuda(key, value, k_cache, v_cache, slot_mapping)
     _u8(k_cache), _u8(v_cache)
     _need(slot_mapping.dtype == torch.int64, "slot_mapping must be int64")
-    NB, bs, H, D = k_cache.shape
+    NB, H, bs, D = k_cache.shape
     T = key.shape[0]
     _need(tuple(key.shape) == (T, H, D) and value.shape == key.shape and v_cache.shape == k_cache.shape,
           "key/value/cache shapes")
@@ -307,11 +312,12 @@ def paged_attention_decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
                                v_scale: float, max_seq_len: int | None = None, out: torch.Tensor | None = None,
                                partition_size: int = 0, workspace: torch.Tensor | None = None,
                                stream=None) -> torch.Tensor:
-    """Decode attention over FP8 (E4M3) pools: q [B, Hq, 128] -> out [B, Hq, 128]."""
+    """Decode attention over head-major FP8 (E4M3) pools [NB, Hkv, 16, 128]:
+    q [B, Hq, 128] -> out [B, Hq, 128]."""
     _cuda(q, k_cache, v_cache, block_tables, seq_lens, out, workspace)
     _u8(k_cache), _u8(v_cache)
     B, Hq, D = q.shape
-    NB, bs, Hkv, D2 = k_cache.shape
+    NB, Hkv, bs, D2 = k_cache.shape
     _need(D2 == D and v_cache.shape == k_cache.shape, "cache shape")
     if max_seq_len is None:
         max_seq_len = int(seq_lens.max().item()) if B else 0

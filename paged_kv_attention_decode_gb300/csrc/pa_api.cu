@@ -102,16 +102,17 @@ bool make_q_map(CUtensorMap* map, const void* q, int num_tokens, int num_q_heads
     return r == CUDA_SUCCESS;
 }
 
-// Tensor map over an FP8 pool [num_blocks * 16 token rows, Hkv, 128 codes]:
-// one box = the 16 rows of one (block, head), 128 bytes each, 128-byte swizzled.
+// Tensor map over a head-major FP8 pool [num_blocks, Hkv, 16 token rows, 128
+// codes]: one box = the 16 rows of one (block, head), a contiguous 2 KB run,
+// landing as 16 rows of 128 bytes, 128-byte swizzled.
 bool make_kv_map_fp8(CUtensorMap* map, const void* base, int num_blocks, int num_kv_heads) {
     auto fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(num_blocks) * 16};
-    const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(num_kv_heads) * 128};
-    const cuuint32_t box[3] = {128, 1, 16};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+    const cuuint64_t dims[4] = {128, 16, static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[3] = {128, 16 * 128, static_cast<cuuint64_t>(num_kv_heads) * 16 * 128};
+    const cuuint32_t box[4] = {128, 16, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -525,6 +526,9 @@ int pa_paged_kv_gather(void* k_out, void* v_out, const void* k_cache, const void
     if (elem_bytes != 1 && elem_bytes != 2) return PA_ERR_UNSUPPORTED;
     const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * elem_bytes;
     if (row_bytes % 16) return PA_ERR_UNSUPPORTED;
+    // FP8 pools are head-major: each head's row of head_dim codes is moved in 16-byte chunks
+    const int64_t head_major_row_bytes = elem_bytes == 1 ? head_dim : 0;
+    if (head_major_row_bytes % 16) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PA_OK;
     if (!k_out || !v_out || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_seq_lens)
         return PA_ERR_INVALID_ARG;
@@ -533,7 +537,8 @@ int pa_paged_kv_gather(void* k_out, void* v_out, const void* k_cache, const void
     unsigned int* err = error_word();
     if (!err) return PA_ERR_CUDA;
     cudaError_t e = pa::launch_kv_gather(k_out, v_out, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
-                                         cu_seq_lens, num_seqs, num_blocks, row_bytes, max_seq_len, err,
+                                         cu_seq_lens, num_seqs, num_blocks, row_bytes, head_major_row_bytes,
+                                         max_seq_len, err,
                                          static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -82,7 +82,9 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__
 // Quantising write into an FP8 (E4M3) cache ("vLLM-Ascend 原理", section 4
 // "量化": k and v are quantised as they are written).  Each thread turns 16
 // source values (fp16/bf16) into 16 codes: code = e4m3(float(x) * inv_scale),
-// one fp32 multiply, round to nearest even, saturating at +-448.
+// one fp32 multiply, round to nearest even, saturating at +-448.  The pools
+// are head-major, [block][head][offset][128 codes]: the eight threads of one
+// (token, head) row still store one whole 128-byte line.
 template <typename T>
 __global__ void __launch_bounds__(256) kv_write_fp8_kernel(const uint4* __restrict__ key,
                                                            const uint4* __restrict__ value,
@@ -124,7 +126,8 @@ __global__ void __launch_bounds__(256) kv_write_fp8_kernel(const uint4* __restri
             }
             out[kv] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
         }
-        const int64_t dst = slot * row_chunks + within;
+        const int64_t h = within / CPR;
+        const int64_t dst = (((slot >> 4) * num_kv_heads + h) * 16 + (slot & 15)) * CPR + (within - h * CPR);
         k_cache[dst] = out[0];
         v_cache[dst] = out[1];
     }
@@ -229,13 +232,16 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pair
 // ("vLLM 在 CANN 上的推理优化", read_kv: logical index -> block, offset).  One
 // CTA row (blockIdx.y) per sequence; each warp moves whole token rows with
 // 16-byte loads.  A table entry outside the pool zero-fills its rows.
+// head_chunks > 0 reads a head-major pool ([block][head][offset][...], the
+// FP8 layout) whose (token, head) rows are head_chunks 16-byte chunks long;
+// 0 reads the token-major layout.
 __global__ void __launch_bounds__(256) kv_gather_kernel(uint4* __restrict__ k_out, uint4* __restrict__ v_out,
                                                         const uint4* __restrict__ k_cache,
                                                         const uint4* __restrict__ v_cache,
                                                         const int32_t* __restrict__ block_tables, int max_blocks,
                                                         const int32_t* __restrict__ seq_lens,
                                                         const int32_t* __restrict__ cu_seq_lens, int num_blocks,
-                                                        int row_chunks, unsigned int* err) {
+                                                        int row_chunks, int head_chunks, unsigned int* err) {
     const int b = blockIdx.y;
     int n = seq_lens[b];
     const int64_t base = cu_seq_lens[b];
@@ -249,11 +255,18 @@ __global__ void __launch_bounds__(256) kv_gather_kernel(uint4* __restrict__ k_ou
         const int phys = block_tables[static_cast<int64_t>(b) * max_blocks + (t >> 4)];
         const bool ok = phys >= 0 && phys < num_blocks;
         if (!ok && lane == 0) record_error(err, PA_DEVERR_BLOCK_ID_);
-        const int64_t src = (static_cast<int64_t>(phys) * 16 + (t & 15)) * row_chunks;
         const int64_t dst = (base + t) * row_chunks;
         for (int c = lane; c < row_chunks; c += 32) {
-            k_out[dst + c] = ok ? k_cache[src + c] : make_uint4(0, 0, 0, 0);
-            v_out[dst + c] = ok ? v_cache[src + c] : make_uint4(0, 0, 0, 0);
+            int64_t src;
+            if (head_chunks > 0) {
+                const int h = c / head_chunks;
+                src = ((static_cast<int64_t>(phys) * (row_chunks / head_chunks) + h) * 16 + (t & 15)) * head_chunks +
+                      (c - h * head_chunks);
+            } else {
+                src = (static_cast<int64_t>(phys) * 16 + (t & 15)) * row_chunks + c;
+            }
+            k_out[dst + c] = ok ? k_cache[src] : make_uint4(0, 0, 0, 0);
+            v_out[dst + c] = ok ? v_cache[src] : make_uint4(0, 0, 0, 0);
         }
     }
 }
@@ -261,14 +274,14 @@ __global__ void __launch_bounds__(256) kv_gather_kernel(uint4* __restrict__ k_ou
 cudaError_t launch_kv_gather(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
                              const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
                              const int32_t* cu_seq_lens, int num_seqs, int num_blocks, int64_t row_bytes,
-                             int max_seq_len, unsigned int* err, cudaStream_t s) {
+                             int64_t head_major_row_bytes, int max_seq_len, unsigned int* err, cudaStream_t s) {
     if (num_seqs == 0) return cudaSuccess;
     const int threads = 256;
     const int gx = std::max(1, std::min((max_seq_len + 7) / 8, 64));   // 8 token rows per CTA pass
     kv_gather_kernel<<<dim3(gx, num_seqs), threads, 0, s>>>(
         static_cast<uint4*>(k_out), static_cast<uint4*>(v_out), static_cast<const uint4*>(k_cache),
         static_cast<const uint4*>(v_cache), block_tables, max_blocks, seq_lens, cu_seq_lens, num_blocks,
-        static_cast<int>(row_bytes / 16), err);
+        static_cast<int>(row_bytes / 16), static_cast<int>(head_major_row_bytes / 16), err);
     return cudaGetLastError();
 }
 

@@ -24,6 +24,9 @@
 //  * GQA (group 2..8): the query group x K-block product is a dense
 //    contraction: S^T[16 tokens x 8 heads] = K Q^T and O^T += V^T P^T with
 //    mma.sync m16n8k16 (fp32 accumulate); M = 16 tokens matches the block.
+//  * FP8 (E4M3) pools are head-major, so a (block, kv head) tile is one
+//    contiguous 2 KB box; MHA converts codes in registers, GQA converts the
+//    tile to 16-bit in shared memory for the MMA.
 //  * a warp writes its item's output row, or the partition's (m, l, acc)
 //    for the log-sum-exp reduction kernel.
 #include <algorithm>
@@ -74,8 +77,9 @@ __device__ __forceinline__ void issue_tile(const WarpRing& ring, int slot, int p
     uint8_t* dst = ring.base + slot * Shape::kStageBytes;
     mbar_arrive_expect_tx(&ring.bars[slot], Shape::kStageBytes);
     if constexpr (kFp8) {
-        tma_load_3d(dst, kmap, &ring.bars[slot], 0, kv_head, phys * 16);
-        tma_load_3d(dst + Shape::kTileBytes, vmap, &ring.bars[slot], 0, kv_head, phys * 16);
+        // head-major FP8 pool: the (block, head) tile is one contiguous 2 KB box
+        tma_load_4d(dst, kmap, &ring.bars[slot], 0, 0, kv_head, phys);
+        tma_load_4d(dst + Shape::kTileBytes, vmap, &ring.bars[slot], 0, 0, kv_head, phys);
     } else {
         // one box per tile: both 64-dim halves of the 16 rows (block tensor map)
         tma_load_4d(dst, kmap, &ring.bars[slot], 0, phys * 16, 0, kv_head);
@@ -1050,14 +1054,21 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, cons
         e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, s, p);
         if (e != cudaSuccess) return e;
     }
-    // persistent: as many CTAs as fit on every SM (shared memory bound), fewer
-    // when there cannot be that many items
-    constexpr int kCtasPerSm = (228 * 1024) / (smem + 2048);
+    // persistent: as many CTAs as are resident on every SM at once (shared
+    // memory and registers), fewer when there cannot be that many items; a
+    // CTA beyond that would only start once the work is nearly gone
+    static int ctas_per_sm = 0;
+    if (!ctas_per_sm) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kDecodeWarps * 32, smem) != cudaSuccess || n < 1)
+            n = 1;
+        ctas_per_sm = n;
+    }
     const long long max_items =
         static_cast<long long>(p.num_seqs) * p.max_parts * p.num_kv_heads * p.col_chunks;
     const long long want = (max_items + kDecodeWarps - 1) / kDecodeWarps;
     const int grid = static_cast<int>(
-        std::max<long long>(1, std::min<long long>(want, static_cast<long long>(kCtasPerSm) * sm_count())));
+        std::max<long long>(1, std::min<long long>(want, static_cast<long long>(ctas_per_sm) * sm_count())));
     e = launch_pdl(kern, dim3(grid), dim3(kDecodeWarps * 32), smem, s, p, kmap, vmap);
     if (e != cudaSuccess) return e;
     if (p.max_parts > 1) {

@@ -125,7 +125,7 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pair
 cudaError_t launch_kv_gather(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
                              const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
                              const int32_t* cu_seq_lens, int num_seqs, int num_blocks, int64_t row_bytes,
-                             int max_seq_len, unsigned int* err, cudaStream_t s);
+                             int64_t head_major_row_bytes, int max_seq_len, unsigned int* err, cudaStream_t s);
 // One-thread kernel whose bounded mbarrier wait runs out (records a timeout).
 cudaError_t launch_wait_selftest(unsigned int* err, cudaStream_t s);
 // tcgen05 prefill: groups of 1 to PA_MAX_GROUP q heads per kv head; q_per_tile = 128 / group.

@@ -186,7 +186,8 @@ def build_workload(
 
     materialize: False builds the integer tables only (tensors are None).
 
-    cache_dtype: "same" (the pools hold ``dtype``) or "fp8": the pools hold
+    cache_dtype: "same" (the pools hold ``dtype``) or "fp8": the pools are
+    head-major [NB, Hkv, bs, D] and hold
     E4M3 codes (uint8) of N(0, 1) / kv_scale values drawn in fp32 and
     converted by torch, so that code * kv_scale is about N(0, 1); the new
     key/value rows stay in ``dtype`` (they are quantised by the write).
@@ -263,8 +264,10 @@ def build_workload(
     value = torch.empty((T, num_kv_heads, head_dim), dtype=tdt, device=dev)
     fp8 = cache_dtype == "fp8"
     cdt = torch.float8_e4m3fn if fp8 else tdt
-    k_cache = torch.empty((num_blocks, bs, num_kv_heads, head_dim), dtype=cdt, device=dev)
-    v_cache = torch.empty((num_blocks, bs, num_kv_heads, head_dim), dtype=cdt, device=dev)
+    # FP8 pools are head-major [NB, Hkv, bs, D]; 16-bit pools [NB, bs, Hkv, D]
+    shape = (num_blocks, num_kv_heads, bs, head_dim) if fp8 else (num_blocks, bs, num_kv_heads, head_dim)
+    k_cache = torch.empty(shape, dtype=cdt, device=dev)
+    v_cache = torch.empty(shape, dtype=cdt, device=dev)
     for t in (q, key, value):
         if t.numel():
             _fill_normal(t, gen)
@@ -285,8 +288,9 @@ def build_workload(
                 live[tables[b, j], :n_ok] = True
         dead = torch.from_numpy(~live).to(dev)
         nan = torch.tensor(0x7F if fp8 else float("nan"), dtype=k_cache.dtype, device=dev)
-        k_cache.masked_fill_(dead[:, :, None, None], nan)
-        v_cache.masked_fill_(dead[:, :, None, None], nan)
+        mask = dead[:, None, :, None] if fp8 else dead[:, :, None, None]
+        k_cache.masked_fill_(mask, nan)
+        v_cache.masked_fill_(mask, nan)
     if fp8:
         meta["kv_scale"] = float(kv_scale)
         meta["cache_dtype"] = "fp8"

@@ -94,8 +94,11 @@ def test_gather_matches_numpy_fancy_index(name, fp8):
     idx = np.concatenate(rows)
     H, D = w.num_kv_heads, w.head_dim
     view = torch.uint8 if fp8 else torch.int16
-    kc = w.k_cache.view(view).cpu().numpy().reshape(-1, H, D)
-    vc = w.v_cache.view(view).cpu().numpy().reshape(-1, H, D)
+    kc = w.k_cache.view(view).cpu().numpy()
+    vc = w.v_cache.view(view).cpu().numpy()
+    if fp8:   # head-major [NB, H, 16, D] -> token-major rows
+        kc, vc = kc.transpose(0, 2, 1, 3), vc.transpose(0, 2, 1, 3)
+    kc, vc = kc.reshape(-1, H, D), vc.reshape(-1, H, D)
     assert np.array_equal(k.view(view).cpu().numpy(), kc[idx])
     assert np.array_equal(v.view(view).cpu().numpy(), vc[idx])
 

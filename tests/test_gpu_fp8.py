@@ -26,7 +26,7 @@ def test_fp8_write_is_bit_exact(src):
     key = (torch.randn(T, H, D, device=DEV, generator=g) * 5).to(W.torch_dtype(src))
     val = (torch.randn(T, H, D, device=DEV, generator=g) * 700).to(W.torch_dtype(src))  # saturates
     key[0, 0, :4] = float("nan")
-    kc = torch.randint(0, 256, (NB, 16, H, D), device=DEV, dtype=torch.uint8, generator=g)
+    kc = torch.randint(0, 256, (NB, H, 16, D), device=DEV, dtype=torch.uint8, generator=g)   # head-major
     vc = kc.clone()
     rng = np.random.default_rng(6)
     slots = rng.permutation(NB * 16)[:T].astype(np.int64)

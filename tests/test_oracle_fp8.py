@@ -58,7 +58,7 @@ def test_fp8_write_matches_torch_quantisation(src):
     g = torch.Generator().manual_seed(4)
     key = (torch.randn(T, H, D, generator=g) * 3).to(W.torch_dtype(src))
     val = (torch.randn(T, H, D, generator=g) * 200).to(W.torch_dtype(src))
-    kc = rng.integers(0, 256, size=(NB, bs, H, D), dtype=np.uint8)
+    kc = rng.integers(0, 256, size=(NB, H, bs, D), dtype=np.uint8)   # head-major E4M3 pools
     vc = kc.copy()
     slots = rng.permutation(NB * bs)[:T].astype(np.int64)
     slots[::5] = -1
@@ -71,8 +71,10 @@ def test_fp8_write_matches_torch_quantisation(src):
         y = (x.to(torch.float32) * torch.tensor(inv)).clamp(-448, 448)
         return y.to(F8).view(torch.uint8).numpy()
 
-    kref.reshape(NB * bs, H, D)[slots[keep]] = quant(key, k_scale)[keep]
-    vref.reshape(NB * bs, H, D)[slots[keep]] = quant(val, v_scale)[keep]
+    # slot s, head h lives at [s // bs, h, s % bs]: index the pools block by block
+    blk, off = slots[keep] // bs, slots[keep] % bs
+    kref.transpose(0, 2, 1, 3)[blk, off] = quant(key, k_scale)[keep]
+    vref.transpose(0, 2, 1, 3)[blk, off] = quant(val, v_scale)[keep]
     oracle.kv_write_fp8(bits(key), bits(val), kc, vc, slots, src, k_scale, v_scale)
     assert np.array_equal(kc, kref) and np.array_equal(vc, vref)
 
@@ -86,11 +88,11 @@ def test_fp8_decode_equals_sdpa_on_dequantised_values():
     q = torch.randn(len(lens), Hq, D, generator=g).to(torch.bfloat16)
     Kc = [(torch.randn(int(n), Hkv, D, generator=g) * 8).to(F8) for n in lens]
     Vc = [(torch.randn(int(n), Hkv, D, generator=g) * 8).to(F8) for n in lens]
-    kpool = np.zeros((w.num_blocks, 16, Hkv, D), np.uint8)
+    kpool = np.zeros((w.num_blocks, Hkv, 16, D), np.uint8)     # head-major E4M3 pools
     vpool = np.zeros_like(kpool)
     slots = oracle.slot_mapping(w.block_tables, lens, lens, 16, w.num_blocks)
-    kpool.reshape(-1, Hkv, D)[slots] = torch.cat(Kc).view(torch.uint8).numpy()
-    vpool.reshape(-1, Hkv, D)[slots] = torch.cat(Vc).view(torch.uint8).numpy()
+    kpool.transpose(0, 2, 1, 3)[slots // 16, slots % 16] = torch.cat(Kc).view(torch.uint8).numpy()
+    vpool.transpose(0, 2, 1, 3)[slots // 16, slots % 16] = torch.cat(Vc).view(torch.uint8).numpy()
     k_scale, v_scale, scale = 1 / 8, 1 / 4, 1 / math.sqrt(D)
     out = oracle.paged_attention_decode_fp8(bits(q), kpool, vpool, w.block_tables, lens, scale, "bf16",
                                             k_scale, v_scale)
