@@ -38,7 +38,7 @@ def test_fp8_write_is_bit_exact(src):
     assert np.array_equal(u8(kc), k_ref) and np.array_equal(u8(vc), v_ref)
 
 
-@pytest.mark.parametrize("Hq,Hkv,dtype", [(8, 8, "f16"), (8, 8, "bf16"), (16, 4, "bf16"), (16, 2, "f16"),
+@pytest.mark.parametrize("Hq,Hkv,dtype", [(8, 8, "f16"), (8, 8, "bf16"), (5, 5, "bf16"), (16, 4, "bf16"), (16, 2, "f16"),
                                           (12, 4, "bf16"), (32, 2, "bf16"), (32, 1, "f16")])
 @pytest.mark.parametrize("partition", [0, 48])
 def test_fp8_decode_step_parity(Hq, Hkv, dtype, partition):
