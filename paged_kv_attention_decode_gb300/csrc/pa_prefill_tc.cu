@@ -31,8 +31,9 @@
 // A tcgen05.mma instruction of M=128 costs the tensor pipe about the same time
 // for any N up to 128, so 128-key tiles (N=128 for S) do twice the work per
 // instruction of 64-key ones.  S_X is single-buffered: S_X(j+1) is issued
-// once P_X(j) V(j) has completed (it overwrites P_X(j)), so while one tile's
-// softmax runs, the tensor pipe works on the other tile (ping-pong).  K(j)'s
+// right behind P_X(j) V(j), which reads P_X(j) from the same columns (the
+// MMAs of one thread execute in issue order), so while one tile's softmax
+// runs, the tensor pipe works on the other tile (ping-pong).  K(j)'s
 // stage is refilled once both S(j) are done, V(j)'s once both P V are
 // (k_free / v_free, committed by the MMA warp).
 // A row rescales O and l only when its maximum exceeds m_ref by more than 2^8
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ uint64_t q_full;                   // the item's query tiles landed
     __shared__ uint64_t item_done;                // every MMA of an item complete
     // S_X(j) complete (one phase per tile of X).  S_X(j+1) is issued only
-    // after P_X(j) V(j) completed, which needs the softmax of tile j, so the
+    // after P_X(j) was stored, which needs the softmax of tile j, so the
     // barrier never runs more than one phase ahead of a waiter.
     __shared__ uint64_t s_full[kTcTiles];
     // P_X(j) stored: one arrival per softmax warp.  A warp reaches tile j+1
@@ -287,9 +288,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ uint64_t p_full[kTcTiles];
     // P_X(j) V(j) complete, by tile parity.  A parity wait is only sound when
     // the barrier's previous phase is known complete: waiting for P V(T)
-    // needs P V(T-2) done, which every waiter has (S(T) is issued only after
-    // P V(T-1) completed).  A completed phase also means every earlier MMA
-    // completed (tcgen05.commit tracks all of them).
+    // needs P V(T-2) done.  The waits (the softmax epilogue after its last
+    // tile T, the abort path) come after S(T) completed, and S(T) was issued
+    // after P V(T-1): a completed commit means every earlier MMA completed
+    // (tcgen05.commit tracks all of them), so both earlier P V are done.
     __shared__ uint64_t o_done[kTcTiles][2];
     __shared__ int32_t stage_blocks[kTcLoaders][NK][kTcBlocks];   // each loader's block ids per K stage
     __shared__ uint32_t tmem_slot;
@@ -726,8 +728,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!ok) break;
                 bool k_next = false;   // K(j+1) seen landed
                 // per tile: P V(j) once its softmax stored P, then S(j+1) into
-                // the same columns once that P V has completed; the other
-                // tile's softmax runs meanwhile
+                // the same columns right behind it (tcgen05.mma operations of
+                // one thread execute in issue order, so P V(j) has read P
+                // before S(j+1) overwrites it); the other tile's softmax runs
+                // meanwhile
 #pragma unroll
                 for (int x = 0; x < kTcTiles; ++x) {
                     if (j >= it.nkx[x]) continue;
@@ -740,8 +744,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if (!(ok = wait_all(&k_full[(J + 1) % NK], ((J + 1) / NK) & 1))) break;
                         k_next = true;
                     }
-                    if (!(ok = wait_all(&o_done[x][Tx & 1], (Tx >> 1) & 1))) break;
-                    tc_fence_after_sync();
                     mma_s(x, j + 1);
                 }
                 if (!ok) break;
