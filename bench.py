@@ -12,6 +12,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -107,10 +108,15 @@ def _prefill_flops(w) -> float:
 
 
 def _source_hash() -> str:
+    """Hash of the decode kernel's source with comments and blank space
+    removed, so that an edit to comments alone keeps a traffic record valid."""
     h = hashlib.sha256()
     for f in ("pa_decode.cu", "pa_device.cuh"):
-        with open(os.path.join(ROOT, "paged_kv_attention_decode_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_kv_attention_decode_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)   # block comments
+        text = re.sub(r"//[^\n]*", "", text)                  # line comments
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
@@ -496,7 +502,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="llama7b_decode")
+    from paged_kv_attention_decode_gb300.workloads import CONFIGS
+    ap.add_argument("--workload", default="llama7b_decode", choices=sorted(CONFIGS),
+                    help="synthetic workload (default: the B=64 LLaMA-2-7B-shaped decode step)")
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -158,7 +158,8 @@ __device__ __forceinline__ uint32_t tile_off(int tok, int dim) {
 }
 
 // FP8 (E4M3) tiles: one token row of 128 codes (head_dim 128) per 128-byte
-// swizzle row, fetched with a single 3-D TMA per tile.
+// swizzle row, fetched with a single TMA box per tile (the 2 KB run of one
+// (block, kv head) in the head-major pool).
 __device__ __forceinline__ uint32_t fp8_off(int tok, int byte) {
     return static_cast<uint32_t>(tok * 128 + ((((byte >> 4) ^ (tok & 7))) << 4) + (byte & 15));
 }
