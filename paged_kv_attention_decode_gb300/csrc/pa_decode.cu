@@ -118,14 +118,41 @@ __device__ __forceinline__ void convert_fp8_tile(const uint8_t* src, uint8_t* ds
     }
 }
 
+// q . k for two 16-bit pairs of type T: s + q0 k0 + q1 k1, each a fused
+// multiply-add in fp32 of two 16-bit operands (exact products, one rounding
+// per step, as fmaf on the converted values).
+template <typename T>
+__device__ __forceinline__ float dot2_mixed(float s, uint32_t q01, uint32_t k01) {
+    if constexpr (std::is_same<T, __half>::value) {
+        asm("{\n\t.reg .f16 q0, q1, k0, k1;\n\tmov.b32 {q0, q1}, %1;\n\tmov.b32 {k0, k1}, %2;\n\t"
+            "fma.rn.f32.f16 %0, q0, k0, %0;\n\tfma.rn.f32.f16 %0, q1, k1, %0;\n\t}"
+            : "+f"(s)
+            : "r"(q01), "r"(k01));
+    } else {
+        asm("{\n\t.reg .b16 q0, q1, k0, k1;\n\tmov.b32 {q0, q1}, %1;\n\tmov.b32 {k0, k1}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, q0, k0, %0;\n\tfma.rn.f32.bf16 %0, q1, k1, %0;\n\t}"
+            : "+f"(s)
+            : "r"(q01), "r"(k01));
+    }
+    return s;
+}
+
 // ---------------------------------------------------------------------------
 // MHA block step: fp32 dot products on the ALU.
 // Lane l owns head dims [l*DPL, (l+1)*DPL).
+// The scores (kMixedK: 16-bit caches, and FP8 caches with fp16 queries)
+// multiply the query's and the key's 16-bit pairs in fp32 directly
+// (mixed-precision FMA; E4M3 codes as fp16 pairs straight from their
+// conversion), and the score scale is applied once to each finished dot
+// product.  FP8 caches with bf16 queries convert the codes to fp32 first.
 // ---------------------------------------------------------------------------
 template <typename T, int D, bool kFp8 = false>
 struct AluState {
     static constexpr int DPL = D / 32;
-    float q[DPL];
+    static constexpr bool kMixedK = !kFp8 || std::is_same<T, __half>::value;
+    float q[DPL];        // scaled fp32 query dims (all but kMixedK)
+    uint32_t qh[DPL / 2];  // 16-bit query pairs (kMixedK)
+    float qscale;        // score scale applied after the dot product (kMixedK)
     float acc[DPL];
     float m;
     float l;  // this lane's share (even lanes only)
@@ -152,11 +179,29 @@ struct AluState {
         float part[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-            float k[DPL];
-            load_dims(kt, t, lane, k);
             float s = 0.f;
+            if constexpr (kMixedK) {
+                uint32_t kw[DPL / 2];
+                if constexpr (kFp8) {
+                    static_assert(DPL == 4, "FP8 tiles hold head_dim 128");
+                    const uint32_t raw = *reinterpret_cast<const uint32_t*>(kt + fp8_off(t, lane * 4));
+                    kw[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(raw & 0xffffu));
+                    kw[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(raw >> 16));
+                } else if constexpr (DPL == 4) {
+                    const uint2 raw = *reinterpret_cast<const uint2*>(kt + tile_off<D>(t, lane * 4));
+                    kw[0] = raw.x;
+                    kw[1] = raw.y;
+                } else {
+                    kw[0] = *reinterpret_cast<const uint32_t*>(kt + tile_off<D>(t, lane * 2));
+                }
 #pragma unroll
-            for (int j = 0; j < DPL; ++j) s = fmaf(q[j], k[j], s);
+                for (int j = 0; j < DPL / 2; ++j) s = dot2_mixed<T>(s, qh[j], kw[j]);
+            } else {
+                float k[DPL];
+                load_dims(kt, t, lane, k);
+#pragma unroll
+                for (int j = 0; j < DPL; ++j) s = fmaf(q[j], k[j], s);
+            }
             part[t] = s;
         }
         // transpose-reduce: after the five exchange rounds lane l holds the full
@@ -195,6 +240,7 @@ struct AluState {
             part[0] = keep + __shfl_xor_sync(kFull, send, 2);
         }
         float s = part[0] + __shfl_xor_sync(kFull, part[0], 1);
+        if constexpr (kMixedK) s *= qscale;
         const int tok = lane >> 1;
         s = tok < nvalid ? s : -INFINITY;
         float mb = s;
@@ -716,12 +762,17 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
         AluState<T, D, kFp8> alu;
 #pragma unroll
         for (int j = 0; j < kQWords; ++j) {
-            const float2 f = Elem<T>::to_float2(qw[j]);
-            alu.q[2 * j] = f.x * p.scale_log2;
-            alu.q[2 * j + 1] = f.y * p.scale_log2;
+            if constexpr (AluState<T, D, kFp8>::kMixedK) {
+                alu.qh[j] = qw[j];
+            } else {
+                const float2 f = Elem<T>::to_float2(qw[j]);
+                alu.q[2 * j] = f.x * p.scale_log2;
+                alu.q[2 * j + 1] = f.y * p.scale_log2;
+            }
             alu.acc[2 * j] = 0.f;
             alu.acc[2 * j + 1] = 0.f;
         }
+        if constexpr (AluState<T, D, kFp8>::kMixedK) alu.qscale = p.scale_log2;
         alu.m = -INFINITY;
         alu.l = 0.f;
         if (!for_each_block(it, [&](uint8_t* kt, uint8_t* vt, int, int nvalid) { alu.step(kt, vt, nvalid, lane); }))
