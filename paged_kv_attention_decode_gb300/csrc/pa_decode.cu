@@ -30,6 +30,7 @@
 //  * a warp writes its item's output row, or the partition's (m, l, acc)
 //    for the log-sum-exp reduction kernel.
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "pa_device.cuh"
@@ -1108,13 +1109,12 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, cons
     // persistent: as many CTAs as are resident on every SM at once (shared
     // memory and registers), fewer when there cannot be that many items; a
     // CTA beyond that would only start once the work is nearly gone
-    static int ctas_per_sm = 0;
-    if (!ctas_per_sm) {
+    static const int ctas_per_sm = [&] {   // once per kernel variant (thread-safe)
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kDecodeWarps * 32, smem) != cudaSuccess || n < 1)
             n = 1;
-        ctas_per_sm = n;
-    }
+        return n;
+    }();
     const long long max_items =
         static_cast<long long>(p.num_seqs) * p.max_parts * p.num_kv_heads * p.col_chunks;
     const long long want = (max_items + kDecodeWarps - 1) / kDecodeWarps;
@@ -1143,15 +1143,15 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& kmap, cons
 }  // namespace
 
 int sm_count() {
-    static int count[64] = {};
+    static std::atomic<int> count[64];   // per device, 0 until first asked
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (!count[dev]) {
-        int c = 0;
+    int c = count[dev].load(std::memory_order_relaxed);
+    if (!c) {
         if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 148;
-        count[dev] = c;
+        count[dev].store(c, std::memory_order_relaxed);
     }
-    return count[dev];
+    return c;
 }
 
 cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t s) {
