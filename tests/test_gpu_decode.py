@@ -52,6 +52,21 @@ def test_prefix_sharing_gqa():
     _check(W.make("gqa_prefix", batch=48, device=DEV, poison=True))
 
 
+# Prefix sharing (sequences whose leading block ids are the same physical
+# blocks): share groups of several sizes over an odd batch, shared prefixes
+# shorter than a partition, and partition lengths that put the shared blocks
+# in one or many partitions.
+@pytest.mark.parametrize("Hq,Hkv,dtype", [(16, 4, "bf16"), (16, 8, "f16"), (8, 4, "f16")])
+@pytest.mark.parametrize("share_groups,share_tokens", [(2, 1024), (3, 512), (5, 1536), (16, 48)])
+@pytest.mark.parametrize("partition", [0, 16, 64])
+def test_shared_prefix_groups(Hq, Hkv, dtype, share_groups, share_tokens, partition):
+    lens = np.random.default_rng(share_groups * 31 + share_tokens).integers(1, 3000, size=23)
+    w = W.build_workload(name="share", seq_lens=lens, q_lens=1, num_q_heads=Hq, num_kv_heads=Hkv,
+                         head_dim=128, dtype=dtype, seed=Hq + share_groups, device=DEV, poison=True,
+                         pool_slack=0.3, share_groups=share_groups, share_tokens=share_tokens)
+    _check(w, partition)
+
+
 def test_output_is_independent_of_physical_placement():
     w = W.build_workload(name="perm", seq_lens=LENS, q_lens=1, num_q_heads=16, num_kv_heads=4,
                          head_dim=128, dtype="bf16", seed=3, device=DEV)
