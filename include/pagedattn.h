@@ -96,7 +96,11 @@ const char* pa_status_string(int status);
  *   cu_q_lens     int32 [num_seqs + 1], or NULL meaning one new token per
  *                 sequence (decode; num_tokens must equal num_seqs).
  * Rows of a sequence whose table entry is out of range get slot -1 and set
- * PA_DEVERR_BLOCK_ID.
+ * PA_DEVERR_BLOCK_ID; rows of a sequence whose seq_len is below its new-token
+ * count (or above the table's capacity) get slot -1 and set
+ * PA_DEVERR_SEQ_LEN.  A decode row (cu_q_lens NULL) with seq_len 0 is a
+ * padding row (a batch padded to a fixed size, e.g. a captured graph's
+ * bucket): slot -1, nothing flagged; decode attention gives it a zero row.
  */
 int pa_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables, int max_blocks_per_seq,
                     const int32_t* seq_lens, const int32_t* cu_q_lens, int num_seqs,

@@ -34,7 +34,10 @@ __global__ void __launch_bounds__(128) slot_mapping_kernel(int64_t* __restrict__
     }
     if (ql <= 0) return;
     const bool seq_ok = n >= ql && n <= max_blocks * 16;
-    if (!seq_ok && lane == 0) record_error(err, PA_DEVERR_SEQ_LEN_);
+    // a decode row of length 0 pads a batch (to a captured bucket size): it
+    // has no token to place, so its slot is -1 and nothing is flagged
+    const bool padding = !cu_q_lens && n == 0;
+    if (!seq_ok && !padding && lane == 0) record_error(err, PA_DEVERR_SEQ_LEN_);
     for (int i = lane; i < ql; i += 32) {
         int64_t slot = -1;
         if (seq_ok) {

@@ -74,6 +74,57 @@ def test_captured_decode_step_replays_with_new_inputs():
     assert pa.device_error() == 0
 
 
+def test_captured_decode_bucket_with_padding_rows():
+    """A batch smaller than the captured bucket: the unused rows are padding
+    (seq_len 0).  They place no token, read nothing and come out as zero rows;
+    the real rows match eager calls and the oracle, and nothing is flagged."""
+    max_len, nb, B = 1024, 600, 6
+    w0 = _step_inputs(11, [300, 1024, 17, 512, 64, 900], nb)
+    q, key, value = w0.q.clone(), w0.key.clone(), w0.value.clone()
+    kc, vc = w0.k_cache.clone(), w0.v_cache.clone()
+    bt = torch.zeros(B, max_len // 16, dtype=torch.int32, device=DEV)
+    sl = torch.zeros(B, dtype=torch.int32, device=DEV)
+    slots = torch.empty(B, dtype=torch.int64, device=DEV)
+    out = torch.empty_like(q)
+    ws = torch.empty(pa.decode_workspace_bytes(B, 8, 128, max_len, 0), dtype=torch.uint8, device=DEV)
+
+    def step():
+        pa.slot_mapping(bt, sl, None, B, nb, out=slots)
+        pa.paged_kv_write(key, value, kc, vc, slots)
+        pa.paged_attention_decode(q, kc, vc, bt, sl, w0.scale, max_len, out=out, workspace=ws)
+
+    bt[:, : w0.block_tables.shape[1]].copy_(torch.from_numpy(w0.block_tables))
+    sl.copy_(torch.from_numpy(w0.seq_lens))
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+
+    real = [0, 2, 3]                     # rows 1, 4 and 5 are padding in this step
+    w = _step_inputs(12, [700, 1, 1000, 250, 1, 1], nb)
+    lens = w.seq_lens.copy()
+    lens[[1, 4, 5]] = 0
+    kc.copy_(w.k_cache); vc.copy_(w.v_cache)
+    q.copy_(w.q); key.copy_(w.key); value.copy_(w.value)
+    bt.zero_(); bt[:, : w.block_tables.shape[1]].copy_(torch.from_numpy(w.block_tables))
+    sl.copy_(torch.from_numpy(lens))
+    pa.device_error()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert pa.device_error() == 0
+    assert torch.all(slots[[1, 4, 5]] == -1)
+    assert torch.count_nonzero(out[[1, 4, 5]]) == 0
+    replayed = out.clone()
+    okc, ovc = bits(w.k_cache), bits(w.v_cache)
+    sel = np.array(real)
+    oracle.kv_write(bits(w.key[real]), bits(w.value[real]), okc, ovc,
+                    oracle.slot_mapping(w.block_tables[sel], lens[sel], np.ones(len(real), np.int32), 16, nb))
+    ref = oracle.paged_attention_decode(bits(w.q[real]), okc, ovc, w.block_tables[sel], lens[sel], w.scale, "bf16")
+    err = float(np.max(np.abs(replayed[real].double().cpu().numpy() - ref)))
+    assert err <= TOL["bf16"], err
+
+
 def test_captured_mixed_step_replays_with_new_inputs():
     """A continuous-batching step (a prefill chunk, a speculative-verify chunk
     and decodes in one varlen call) captured once and replayed with other
