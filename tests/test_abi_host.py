@@ -170,3 +170,61 @@ def test_copy_blocks_rejects_bad_arguments_on_the_host(lib):
     assert f(FAKE, FAKE, None, 1, 8, 8, 128, 2, None) == 1          # no pair list
     assert f(FAKE + 8, FAKE, FAKE, 1, 8, 8, 128, 2, None) == 1      # misaligned pool
     assert f(None, None, None, 0, 8, 8, 128, 2, None) == 0          # nothing to copy
+
+
+def test_fp8_entry_points_reject_bad_arguments_on_the_host(lib):
+    w = lib.pa_paged_kv_write_fp8
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 128, 16, 0, 1.0, 1.0, None]
+
+    def write(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return w(*a)
+
+    assert write(a8=64) == 2                 # head_dim must be 128
+    assert write(a9=32) == 2                 # block size
+    assert write(a10=5) == 2                 # source dtype
+    assert write(a11=0.0) == 1 and write(a12=-1.0) == 1 and write(a11=float("inf")) == 1
+    assert write(a4=None) == 1               # slot mapping
+    assert write(a5=0) == 0                  # nothing to write
+    d = lib.pa_paged_attention_decode_fp8
+    dargs = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 2, 64, 8, 0.1, 1.0, 1.0, 4, 2, 128, 16, 0, None, 0, 0, None]
+
+    def decode(**kw):
+        a = list(dargs)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return d(*a)
+
+    assert decode(a15=64) == 2               # FP8 pools hold head_dim 128 only
+    assert decode(a11=float("nan")) == 1
+    assert decode(a13=5) == 1                # q heads not a multiple of kv heads
+    assert decode(a1=None) == 1
+    assert decode(a7=0) == 0
+
+
+def test_gather_rejects_bad_arguments_on_the_host(lib):
+    g = lib.pa_paged_kv_gather
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 64, 8, 2, 128, 2, None]
+
+    def gather(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return g(*a)
+
+    assert gather(a13=4) == 2                # element size
+    assert gather(a12=8, a13=1) == 2         # a head-major FP8 row must be whole 16-byte chunks
+    assert gather(a5=0) == 1 and gather(a0=None) == 1
+    assert gather(a8=0) == 0
+
+
+def test_noalloc_rejects_before_touching_the_device(lib):
+    """The allocation-free decode checks its sizes against its fixed scratch
+    before anything else, so these run without a GPU."""
+    n = lib.pa_paged_attention_decode_noalloc
+    # 64 heads x 1024 partitions of 16 tokens x (128 + 2) floats = 34 MB > 32 MiB
+    assert n(FAKE, FAKE, FAKE, FAKE, FAKE, 1024, FAKE, 1, 16 * 1024, 8, 0.1, 64, 8, 128, 16, 16, 1, None) == 3
+    assert n(FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, -1, 64, 8, 0.1, 4, 2, 128, 16, 0, 1, None) == 1
+    assert n(FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 1, -5, 8, 0.1, 4, 2, 128, 16, 0, 1, None) == 1
