@@ -30,7 +30,7 @@ def _rank(rank, world, port, out):
 
 
 def test_two_gloo_replicas_agree_on_the_slowest_rank():
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()   # no fork of this multi-threaded process
     out = mgr.dict()
     mp.spawn(_rank, args=(2, _free_port(), out), nprocs=2, join=True)
     want = 2 * 64 * 1000 / 0.150
