@@ -57,9 +57,10 @@ struct DecodeShape {
     // The 16-bit tensor-core kernels are bound by instruction latency per
     // warp: the single-tile one (group heads of decode rows) runs best with
     // 2-stage rings and 3 CTAs (12 warps) per SM; the two-tile one (verify
-    // rows, 16 columns) with 3-stage rings and 2 CTAs per SM.
+    // rows, 16 columns) with 3-stage rings and 2 CTAs per SM.  The FP8 MHA
+    // kernel keeps 5 CTAs (20 warps) per SM: registers capped at 96.
     static constexpr int kStages = kFp8 ? (kMma ? 4 : 2) : (kMma ? (kMaxNT > 1 ? 3 : 2) : 3);
-    static constexpr int kMinCtasPerSm = (kMma && !kFp8) ? (kMaxNT > 1 ? 2 : 3) : 1;
+    static constexpr int kMinCtasPerSm = (kMma && !kFp8) ? (kMaxNT > 1 ? 2 : 3) : (kFp8 && !kMma ? 5 : 1);
     static constexpr int kConvBytes = (kFp8 && kMma) ? 2 * 16 * D * 2 : 0;
     static constexpr int kWarpBytes = kStages * kStageBytes + kConvBytes;
     static constexpr int kSmemBytes = kDecodeWarps * kWarpBytes + 1024;  // + alignment slack
@@ -146,11 +147,17 @@ __device__ __forceinline__ float dot2_mixed(float s, uint32_t q01, uint32_t k01)
 // (mixed-precision FMA; E4M3 codes as fp16 pairs straight from their
 // conversion), and the score scale is applied once to each finished dot
 // product.  FP8 caches with bf16 queries convert the codes to fp32 first.
+// With an FP8 cache and fp16 queries (kTokenK) the scores are computed token
+// by token instead: lanes 2t and 2t+1 each take half of token t's 128 dims
+// (four 16-byte loads of codes, no transpose-reduction), which leaves the
+// scores in the same lanes as the reduction does.
 // ---------------------------------------------------------------------------
 template <typename T, int D, bool kFp8 = false>
 struct AluState {
     static constexpr int DPL = D / 32;
     static constexpr bool kMixedK = !kFp8 || std::is_same<T, __half>::value;
+    static constexpr bool kTokenK = kFp8 && std::is_same<T, __half>::value;
+    uint32_t qk[kTokenK ? 32 : 1];   // this lane's 64 query dims as fp16 pairs (kTokenK)
     float q[DPL];        // scaled fp32 query dims (all but kMixedK)
     uint32_t qh[DPL / 2];  // 16-bit query pairs (kMixedK)
     float qscale;        // score scale applied after the dot product (kMixedK)
@@ -177,6 +184,27 @@ struct AluState {
     }
 
     __device__ __forceinline__ void step(const uint8_t* kt, const uint8_t* vt, int nvalid, int lane) {
+      float s;
+      if constexpr (kTokenK) {
+        // lanes 2t and 2t+1 each take one half of token t's 128 dims
+        const int t = lane >> 1, h = lane & 1;
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(kt + fp8_off(t, h * 64 + k * 16));
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t k01 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] & 0xffffu));
+                const uint32_t k23 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] >> 16));
+                s0 = dot2_mixed<T>(s0, qk[8 * k + 2 * j], k01);
+                s1 = dot2_mixed<T>(s1, qk[8 * k + 2 * j + 1], k23);
+            }
+        }
+        s = s0 + s1;
+        s += __shfl_xor_sync(kFull, s, 1);
+        s *= qscale;
+      } else {
         float part[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
@@ -240,8 +268,9 @@ struct AluState {
             const float keep = hi ? part[1] : part[0];
             part[0] = keep + __shfl_xor_sync(kFull, send, 2);
         }
-        float s = part[0] + __shfl_xor_sync(kFull, part[0], 1);
+        s = part[0] + __shfl_xor_sync(kFull, part[0], 1);
         if constexpr (kMixedK) s *= qscale;
+      }
         const int tok = lane >> 1;
         s = tok < nvalid ? s : -INFINITY;
         float mb = s;
@@ -774,6 +803,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
             alu.acc[2 * j + 1] = 0.f;
         }
         if constexpr (AluState<T, D, kFp8>::kMixedK) alu.qscale = p.scale_log2;
+        if constexpr (AluState<T, D, kFp8>::kTokenK) {
+            const uint4* qq = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                             (static_cast<int64_t>(it.qrow0) * p.num_q_heads + it.g) * D +
+                                                             (lane & 1) * 64);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint4 v = qq[i];
+                alu.qk[4 * i] = v.x; alu.qk[4 * i + 1] = v.y; alu.qk[4 * i + 2] = v.z; alu.qk[4 * i + 3] = v.w;
+            }
+        }
         alu.m = -INFINITY;
         alu.l = 0.f;
         if (!for_each_block(it, [&](uint8_t* kt, uint8_t* vt, int, int nvalid) { alu.step(kt, vt, nvalid, lane); }))
