@@ -234,6 +234,13 @@ def _workload_kw(args) -> dict:
     return {"batch": args.batch}
 
 
+def _ctx(workload: str, w) -> str:
+    """The context-length description of a workload for the JSON line."""
+    if workload == "llama7b_decode":
+        return f"U[512,4096] (mean {int(w.seq_lens.mean())})"
+    return f"mean {int(w.seq_lens.mean())}, max {w.max_seq_len}"
+
+
 def run_reference(args):
     """--impl reference: the oracle on the host cores, one whole sequence per step."""
     import oracle
@@ -276,7 +283,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "batch": w.batch, "ctx": "U[512,4096]",
+        "config": {"workload": args.workload, "batch": w.batch, "ctx": _ctx(args.workload, w),
                    "heads": f"{w.num_q_heads}/{w.num_kv_heads}", "head_dim": w.head_dim, "block_size": 16,
                    "step": "one whole sequence per step (rotating through the batch)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(0), "kind": "oracle",
@@ -447,8 +454,7 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     ab = _algorithmic_bytes(w)
     achieved = ab["total"] / (attn_ms / 1e3) / 1e9
-    ctx = (f"U[512,4096] (mean {int(w.seq_lens.mean())})" if args.workload == "llama7b_decode"
-           else f"mean {int(w.seq_lens.mean())}, max {w.max_seq_len}")
+    ctx = _ctx(args.workload, w)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
