@@ -184,93 +184,93 @@ struct AluState {
     }
 
     __device__ __forceinline__ void step(const uint8_t* kt, const uint8_t* vt, int nvalid, int lane) {
-      float s;
-      if constexpr (kTokenK) {
-        // lanes 2t and 2t+1 each take one half of token t's 128 dims
-        const int t = lane >> 1, h = lane & 1;
-        float s0 = 0.f, s1 = 0.f;
+        float s;
+        if constexpr (kTokenK) {
+            // lanes 2t and 2t+1 each take one half of token t's 128 dims
+            const int t = lane >> 1, h = lane & 1;
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(kt + fp8_off(t, h * 64 + k * 16));
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            for (int k = 0; k < 4; ++k) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(kt + fp8_off(t, h * 64 + k * 16));
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t k01 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] & 0xffffu));
-                const uint32_t k23 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] >> 16));
-                s0 = dot2_mixed<T>(s0, qk[8 * k + 2 * j], k01);
-                s1 = dot2_mixed<T>(s1, qk[8 * k + 2 * j + 1], k23);
-            }
-        }
-        s = s0 + s1;
-        s += __shfl_xor_sync(kFull, s, 1);
-        s *= qscale;
-      } else {
-        float part[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            float s = 0.f;
-            if constexpr (kMixedK) {
-                uint32_t kw[DPL / 2];
-                if constexpr (kFp8) {
-                    static_assert(DPL == 4, "FP8 tiles hold head_dim 128");
-                    const uint32_t raw = *reinterpret_cast<const uint32_t*>(kt + fp8_off(t, lane * 4));
-                    kw[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(raw & 0xffffu));
-                    kw[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(raw >> 16));
-                } else if constexpr (DPL == 4) {
-                    const uint2 raw = *reinterpret_cast<const uint2*>(kt + tile_off<D>(t, lane * 4));
-                    kw[0] = raw.x;
-                    kw[1] = raw.y;
-                } else {
-                    kw[0] = *reinterpret_cast<const uint32_t*>(kt + tile_off<D>(t, lane * 2));
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t k01 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] & 0xffffu));
+                    const uint32_t k23 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] >> 16));
+                    s0 = dot2_mixed<T>(s0, qk[8 * k + 2 * j], k01);
+                    s1 = dot2_mixed<T>(s1, qk[8 * k + 2 * j + 1], k23);
                 }
-#pragma unroll
-                for (int j = 0; j < DPL / 2; ++j) s = dot2_mixed<T>(s, qh[j], kw[j]);
-            } else {
-                float k[DPL];
-                load_dims(kt, t, lane, k);
-#pragma unroll
-                for (int j = 0; j < DPL; ++j) s = fmaf(q[j], k[j], s);
             }
-            part[t] = s;
-        }
-        // transpose-reduce: after the five exchange rounds lane l holds the full
-        // dot product of token l >> 1 (lanes 2t and 2t+1 hold the same value).
-        {
-            const bool hi = lane & 16;
+            s = s0 + s1;
+            s += __shfl_xor_sync(kFull, s, 1);
+            s *= qscale;
+        } else {
+            float part[16];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float send = hi ? part[j] : part[j + 8];
-                const float keep = hi ? part[j + 8] : part[j];
-                part[j] = keep + __shfl_xor_sync(kFull, send, 16);
-            }
-        }
-        {
-            const bool hi = lane & 8;
+            for (int t = 0; t < 16; ++t) {
+                float s = 0.f;
+                if constexpr (kMixedK) {
+                    uint32_t kw[DPL / 2];
+                    if constexpr (kFp8) {
+                        static_assert(DPL == 4, "FP8 tiles hold head_dim 128");
+                        const uint32_t raw = *reinterpret_cast<const uint32_t*>(kt + fp8_off(t, lane * 4));
+                        kw[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(raw & 0xffffu));
+                        kw[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(raw >> 16));
+                    } else if constexpr (DPL == 4) {
+                        const uint2 raw = *reinterpret_cast<const uint2*>(kt + tile_off<D>(t, lane * 4));
+                        kw[0] = raw.x;
+                        kw[1] = raw.y;
+                    } else {
+                        kw[0] = *reinterpret_cast<const uint32_t*>(kt + tile_off<D>(t, lane * 2));
+                    }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float send = hi ? part[j] : part[j + 4];
-                const float keep = hi ? part[j + 4] : part[j];
-                part[j] = keep + __shfl_xor_sync(kFull, send, 8);
-            }
-        }
-        {
-            const bool hi = lane & 4;
+                    for (int j = 0; j < DPL / 2; ++j) s = dot2_mixed<T>(s, qh[j], kw[j]);
+                } else {
+                    float k[DPL];
+                    load_dims(kt, t, lane, k);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float send = hi ? part[j] : part[j + 2];
-                const float keep = hi ? part[j + 2] : part[j];
-                part[j] = keep + __shfl_xor_sync(kFull, send, 4);
+                    for (int j = 0; j < DPL; ++j) s = fmaf(q[j], k[j], s);
+                }
+                part[t] = s;
             }
+            // transpose-reduce: after the five exchange rounds lane l holds the full
+            // dot product of token l >> 1 (lanes 2t and 2t+1 hold the same value).
+            {
+                const bool hi = lane & 16;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float send = hi ? part[j] : part[j + 8];
+                    const float keep = hi ? part[j + 8] : part[j];
+                    part[j] = keep + __shfl_xor_sync(kFull, send, 16);
+                }
+            }
+            {
+                const bool hi = lane & 8;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float send = hi ? part[j] : part[j + 4];
+                    const float keep = hi ? part[j + 4] : part[j];
+                    part[j] = keep + __shfl_xor_sync(kFull, send, 8);
+                }
+            }
+            {
+                const bool hi = lane & 4;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float send = hi ? part[j] : part[j + 2];
+                    const float keep = hi ? part[j + 2] : part[j];
+                    part[j] = keep + __shfl_xor_sync(kFull, send, 4);
+                }
+            }
+            {
+                const bool hi = lane & 2;
+                const float send = hi ? part[0] : part[1];
+                const float keep = hi ? part[1] : part[0];
+                part[0] = keep + __shfl_xor_sync(kFull, send, 2);
+            }
+            s = part[0] + __shfl_xor_sync(kFull, part[0], 1);
+            if constexpr (kMixedK) s *= qscale;
         }
-        {
-            const bool hi = lane & 2;
-            const float send = hi ? part[0] : part[1];
-            const float keep = hi ? part[1] : part[0];
-            part[0] = keep + __shfl_xor_sync(kFull, send, 2);
-        }
-        s = part[0] + __shfl_xor_sync(kFull, part[0], 1);
-        if constexpr (kMixedK) s *= qscale;
-      }
         const int tok = lane >> 1;
         s = tok < nvalid ? s : -INFINITY;
         float mb = s;
