@@ -804,9 +804,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
         }
         if constexpr (AluState<T, D, kFp8>::kMixedK) alu.qscale = p.scale_log2;
         if constexpr (AluState<T, D, kFp8>::kTokenK) {
-            const uint4* qq = reinterpret_cast<const uint4*>(
-                static_cast<const uint16_t*>(p.q) + (static_cast<int64_t>(it.qrow0) * p.num_q_heads + it.g) * D +
-                (lane & 1) * 64);
+            const uint4* qq = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                             (static_cast<int64_t>(it.qrow0) * p.num_q_heads + it.g) * D +
+                                                             (lane & 1) * 64);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const uint4 v = qq[i];
