@@ -102,3 +102,43 @@ def test_fp8_decode_equals_sdpa_on_dequantised_values():
         ref = F.scaled_dot_product_attention(q[b].to(torch.float64)[:, None][None], k[None], v[None],
                                              scale=scale)[0, :, 0]
         np.testing.assert_allclose(out[b], ref.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_fp8_decode_against_pure_python_brute_force():
+    """A third implementation on a tiny case: E4M3 codes decoded from their
+    bit fields (sign, 4-bit exponent with bias 7, 3-bit mantissa, subnormals
+    below exponent 1; no infinities), the head-major pool walked token by
+    token, and the softmax with math.exp."""
+    def e4m3(code):
+        sgn = -1.0 if code & 0x80 else 1.0
+        e, m = (code >> 3) & 0xF, code & 0x7
+        if e == 0xF and m == 0x7:
+            return math.nan
+        return sgn * (m / 8.0) * 2.0 ** -6 if e == 0 else sgn * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+    Hq, Hkv, D = 4, 2, 128
+    lens = np.array([1, 19, 40], dtype=np.int32)
+    w = W.build_workload(name="f8bf", seq_lens=lens, q_lens=1, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                         dtype="f16", seed=21, pool_slack=0.5, materialize=False)
+    rng = np.random.default_rng(22)
+    kpool = rng.integers(0, 256, size=(w.num_blocks, Hkv, 16, D), dtype=np.uint8)
+    kpool[(kpool & 0x7F) == 0x7F] = 0x3C          # no NaN codes
+    vpool = rng.integers(0, 256, size=(w.num_blocks, Hkv, 16, D), dtype=np.uint8)
+    vpool[(vpool & 0x7F) == 0x7F] = 0x2A
+    q = (torch.randn(len(lens), Hq, D, generator=torch.Generator().manual_seed(23)) * 0.1).to(torch.float16)
+    k_scale, v_scale, scale = 1 / 64, 1 / 32, 1 / math.sqrt(D)
+    out = oracle.paged_attention_decode_fp8(bits(q), kpool, vpool, w.block_tables, lens, scale, "f16",
+                                            k_scale, v_scale)
+    qf = q.to(torch.float64).tolist()
+    for b, n in enumerate(lens):
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            rows = [(int(w.block_tables[b][t // 16]), t % 16) for t in range(n)]
+            s = [scale * sum(qf[b][h][d] * e4m3(int(kpool[blk, g, off, d])) * k_scale for d in range(D))
+                 for blk, off in rows]
+            mx = max(s)
+            e = [math.exp(x - mx) for x in s]
+            tot = sum(e)
+            for d in range(0, D, 7):
+                ref = sum(e[t] * e4m3(int(vpool[blk, g, off, d])) * v_scale for t, (blk, off) in enumerate(rows)) / tot
+                assert out[b, h, d] == pytest.approx(ref, rel=1e-11, abs=1e-12)
