@@ -534,6 +534,14 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
         return n;
     };
     int chunk_total = 0;
+    // Only inputs are read before the wait: the first 1024 rows' lengths.
+    // Every global write comes after it, because the preceding kernel of the
+    // stream may still be running -- a previous decode call's kernel allows
+    // dependent launch as soon as it starts, and it reads the work list, the
+    // counter and the output rows that this plan is about to rewrite.
+    int qlen0 = 0;
+    const int n0 = tid < p.num_seqs ? row_of(tid, true, qlen0) : 0;
+    pdl_wait();
     // pass 1: full partitions, partials rows (and the zero rows of empty sequences)
     if (tid == 0) {
         carry_u = 0;
@@ -544,7 +552,9 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
         const int b = base + tid;
         int v = 0, vr = 0, qlen = 0;
         if (b < p.num_seqs) {
-            const int n = row_of(b, true, qlen);
+            int n = n0;
+            qlen = qlen0;
+            if (base > 0) n = row_of(b, true, qlen);
             if (n > 0) {
                 v = n / P;
                 vr = n > P ? qlen : 0;
@@ -570,7 +580,8 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
         const int b = base + tid;
         int v = 0, last = 0, qlen = 0;
         if (b < p.num_seqs) {
-            const int n = row_of(b, false, qlen);
+            int n = n0;
+            if (base > 0) n = row_of(b, false, qlen);
             if (n > 0 && n % P) {
                 v = 1;
                 last = n / P;
@@ -584,11 +595,9 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
         *p.work_counter = 0;
         if (p.row_count) *p.row_count = carry_r;
     }
-    // Only the lengths and tables (inputs) were read above, so this grid may
-    // have overlapped the previous kernel of the stream (the KV write).  It
-    // completes only after that kernel, so the decode kernel's wait on this
-    // grid also covers the write.
-    pdl_wait();
+    // this grid completed only after the previous kernel of the stream (the
+    // wait above), so the decode kernel's wait on this grid covers that
+    // kernel too (the KV write of the step)
 }
 
 // ---------------------------------------------------------------------------
@@ -637,13 +646,17 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
     prefetch_tensormap(&vmap);
     // the work list (and, through it, the KV write) is complete; with
     // p.overlap the preceding kernel is a prefill kernel this one runs beside,
-    // and the list was built before that kernel started
+    // and the list was built before that kernel started, so the wait moves to
+    // the kernel's exit (below)
     if (!p.overlap) pdl_wait();
     // a reduce launched with programmatic dependent launch may be scheduled
     // now: its CTAs wait on chip for this grid to complete
     pdl_trigger();
     const int total = *p.unit_count * H * C;
-    if (total == 0) return;
+    if (total == 0) {
+        if (p.overlap) pdl_wait();
+        return;
+    }
     int* queue = claimed[warp];
 
     struct Item {
@@ -966,6 +979,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
         // let copies still in flight land before the CTA's memory is reused
         for (uint32_t k = kc; k < kf; ++k) (void)mbar_wait(&ring.bars[k % kDecodeStages], (k / kDecodeStages) & 1u);
     }
+    // Beside a prefill kernel (p.overlap) this grid must not complete before
+    // that kernel does: whatever the stream runs next (the reduce, the next
+    // call) is ordered after this grid only, and may rewrite the output rows
+    // or cache blocks the prefill kernel is still using.
+    if (p.overlap) pdl_wait();
 }
 
 // Merge the partitions of each (query row, q head):

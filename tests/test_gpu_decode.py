@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_attention_decode_gb300 as pa
 from paged_kv_attention_decode_gb300 import workloads as W
 from tests._gpu_util import TOL, bits, gpu_step, max_err, oracle_rows, snapshot
@@ -131,3 +132,52 @@ def test_unsupported_shapes_are_rejected_before_launch():
     sl = torch.ones(2, device=DEV, dtype=torch.int32)
     with pytest.raises(pa.PagedAttnError):
         pa.paged_attention_decode(q, kc, kc, bt, sl, 0.1, max_seq_len=1)
+
+
+@pytest.mark.parametrize("empty_row", [False, True])
+def test_calls_back_to_back_on_one_workspace(empty_row):
+    """Decode calls queued with no other kernel between them, on one workspace,
+    each of one partition (so no reduce kernel separates them).  A call's
+    plan rewrites the work list, the work counter and the zero rows of empty
+    sequences; it must not do so while the previous call's kernel still
+    claims items.  The second call has fewer sequences, and optionally an
+    empty one whose zero row lands on a row the first call writes."""
+    rng = np.random.default_rng(21)
+    wa = W.build_workload(name="b2b_a", seq_lens=rng.integers(300, 513, 120), q_lens=1, num_q_heads=32,
+                          num_kv_heads=32, head_dim=128, dtype="f16", seed=31, device=DEV)
+    wb = W.build_workload(name="b2b_b", seq_lens=rng.integers(1, 513, 13), q_lens=1, num_q_heads=32,
+                          num_kv_heads=8, head_dim=128, dtype="f16", seed=32, device=DEV)
+    bta, sla = (torch.from_numpy(x).to(DEV) for x in (wa.block_tables, wa.seq_lens))
+    btb = torch.from_numpy(wb.block_tables).to(DEV)
+    lens_b = wb.seq_lens.copy()
+    if empty_row:
+        lens_b[4] = 0
+    slb = torch.from_numpy(lens_b).to(DEV)
+    assert pa.decode_partition(512) == 512
+    need = max(pa.decode_workspace_bytes(wa.batch, 32, 128, 512), pa.decode_workspace_bytes(wb.batch, 32, 128, 512))
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    snap_a = snapshot(wa, np.arange(wa.batch))
+    snap_b = snapshot(wb, np.arange(wb.batch))
+    out_a = torch.full_like(wa.q, float("nan"))
+    out_b = torch.full_like(wb.q, float("nan"))
+    # the second call writes into the first call's output rows as well
+    shared_out = out_a[: wb.batch]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        pa.paged_attention_decode(wa.q, wa.k_cache, wa.v_cache, bta, sla, wa.scale, max_seq_len=512, out=out_a,
+                                  workspace=ws)
+        pa.paged_attention_decode(wb.q, wb.k_cache, wb.v_cache, btb, slb, wb.scale, max_seq_len=512, out=out_b,
+                                  workspace=ws)
+    pa.paged_attention_decode(wb.q, wb.k_cache, wb.v_cache, btb, slb, wb.scale, max_seq_len=512,
+                              out=shared_out, workspace=ws)
+    torch.cuda.synchronize()
+    kc, vc, tables = snap_a
+    ref_a = oracle.paged_attention_decode(bits(wa.q), kc, vc, tables, wa.seq_lens, wa.scale, "f16")
+    kc, vc, tables = snap_b
+    ref_b = oracle.paged_attention_decode(bits(wb.q), kc, vc, tables, lens_b, wb.scale, "f16")
+    assert max_err(out_a[wb.batch:], ref_a[wb.batch:]) <= TOL["f16"]
+    assert max_err(out_b, ref_b) <= TOL["f16"]
+    assert torch.equal(shared_out.view(torch.int16), out_b.view(torch.int16))
+    if empty_row:
+        assert torch.count_nonzero(out_b[4]) == 0
+    assert pa.device_error() == 0
