@@ -36,6 +36,12 @@
  * = the legacy default stream) and returns without synchronising, except
  * pa_get_device_error, which waits for the stream.
  *
+ * Device state: the library looks up, once per device, the addresses of its
+ * own device variables (the error word, the scratch array of
+ * pa_paged_attention_decode_noalloc) and keeps them for the life of the
+ * process.  They do not survive cudaDeviceReset: after a reset, do not call
+ * the library again in that process.
+ *
  * Errors: arguments are validated on the host before anything is launched;
  * a rejected call returns a nonzero pa_status and enqueues nothing.  A
  * launch failure returns PA_ERR_CUDA.  The kernels also check every block
@@ -291,15 +297,22 @@ int pa_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache,
  * forbids device allocation by extensions.  This entry point takes the same
  * arguments as pa_paged_attention_decode minus the workspace and keeps the
  * split-context partials in a fixed scratch array of PA_NOALLOC_SCRATCH_BYTES
- * that the library holds on every GPU where it is loaded, until the process
- * exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ * that the library holds on each GPU, once reserved there (below), until the
+ * process exits.  It calls no cudaMalloc, cudaFree or other allocating
+ * routine.
  *
  *  - Sizes whose partials need more than PA_NOALLOC_SCRATCH_BYTES
  *    (pa_decode_workspace_bytes(...) > PA_NOALLOC_SCRATCH_BYTES) are rejected
  *    with PA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  *  - The first call on a device looks up that device's scratch address
  *    (once per device, with the device current); make that first call before
- *    any stream capture.
+ *    any stream capture.  Under CUDA's lazy module loading (the default) that
+ *    first call is also what reserves the PA_NOALLOC_SCRATCH_BYTES on the
+ *    device, so a runtime that later gives all free HBM to its KV pool must
+ *    make it before taking the memory.  A call with num_seqs == 0 does this
+ *    set-up and nothing else (the other arguments are not read).  With
+ *    eager loading the array is reserved when the library's code is loaded
+ *    into the device's context.
  *  - Every call on a device shares the one scratch array and it keeps the
  *    last call's contents.  Nothing in it needs to start at zero (each call
  *    writes every partial before reading it), but calls whose work overlaps

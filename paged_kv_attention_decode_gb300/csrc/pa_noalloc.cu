@@ -22,6 +22,8 @@ void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_noalloc_scratch on the current device, looked up once
 // per device (the first call on a device does it, with that device current).
+// Under lazy module loading (the CUDA default) this lookup is also what loads
+// this file's module on the device, and so what reserves the array there.
 void* scratch_address() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -45,11 +47,11 @@ extern "C" int pa_paged_attention_decode_noalloc(void* out, const void* q, const
     if (num_seqs < 0 || max_seq_len < 0 || partition_size < 0) return PA_ERR_INVALID_ARG;
     const size_t need = pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len, partition_size);
     if (need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE_TOO_SMALL;
-    void* ws = nullptr;
-    if (need > 0) {
-        ws = scratch_address();
-        if (!ws) return PA_ERR_CUDA;
-    }
+    // set-up first, even for a call with no sequences: such a call reserves
+    // the array on this device and does nothing else
+    void* ws = scratch_address();
+    if (!ws) return PA_ERR_CUDA;
+    if (num_seqs == 0) return PA_OK;
     return pa_paged_attention_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens,
                                      num_seqs, max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads,
                                      head_dim, block_size, partition_size, ws, need, dtype, stream);

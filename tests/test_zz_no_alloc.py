@@ -4,11 +4,15 @@ Some callers cannot allocate device memory when they run a decode step: an
 inference runtime that gave all remaining HBM to its KV block pool, or a
 plugin whose host framework forbids device allocation by extensions.  For
 them pa_paged_attention_decode_noalloc keeps the split-context partials in a
-fixed scratch array inside the library instead of a caller workspace.  These
-tests call it through the C ABI and hold its output to the ordinary decode
-entry point's, within the decode tolerance, on two calls in a row with
-different inputs (the scratch array is shared by every call and keeps the
-previous call's contents).  This file is collected last on purpose.
+fixed scratch array inside the library instead of a caller workspace.
+
+These tests call it through the C ABI.  Its outputs must be bit-identical to
+the ordinary decode entry point's (the same kernels with the same
+partitioning) and within the decode tolerance of the fp64 oracle on a sample
+of sequences.  The calls come in a row with different inputs and no other
+kernel between them: the scratch array is shared by every call and keeps the
+previous call's contents, and a call's work list must not be rewritten by the
+next call while it still runs.  This file is collected last on purpose.
 """
 import ctypes
 
@@ -16,43 +20,87 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_attention_decode_gb300 as pa
 from paged_kv_attention_decode_gb300 import _binding
 from paged_kv_attention_decode_gb300 import workloads as W
+from tests._gpu_util import TOL, bits, max_err, snapshot
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-TOL = {"f16": 2e-3, "bf16": 1.6e-2}
 SCRATCH = 32 << 20   # PA_NOALLOC_SCRATCH_BYTES
 
 
-def _noalloc(lib, out, w, bt, sl, max_len, partition=0):
+def _noalloc(lib, out, w, bt, sl, max_len, partition=0, num_seqs=None):
     stream = torch.cuda.current_stream().cuda_stream
     return lib.pa_paged_attention_decode_noalloc(
         out.data_ptr(), w.q.data_ptr(), w.k_cache.data_ptr(), w.v_cache.data_ptr(), bt.data_ptr(),
-        bt.shape[1], sl.data_ptr(), w.batch, max_len, w.num_blocks, ctypes.c_float(w.scale),
-        w.num_q_heads, w.num_kv_heads, w.head_dim, 16, partition, 0 if w.dtype == "f16" else 1, stream)
+        bt.shape[1], sl.data_ptr(), w.batch if num_seqs is None else num_seqs, max_len, w.num_blocks,
+        ctypes.c_float(w.scale), w.num_q_heads, w.num_kv_heads, w.head_dim, 16, partition,
+        0 if w.dtype == "f16" else 1, stream)
 
 
-def test_noalloc_matches_the_workspace_entry_point_on_two_calls():
+def _oracle_sample(w, count, seed):
+    seqs = np.sort(np.random.default_rng(seed).choice(w.batch, min(count, w.batch), replace=False))
+    kc, vc, tables = snapshot(w, seqs)
+    q = bits(w.q[torch.from_numpy(seqs).to(DEV)])
+    ref = oracle.paged_attention_decode(q, kc, vc, tables, w.seq_lens[seqs], w.scale, w.dtype)
+    return seqs, ref
+
+
+def test_noalloc_matches_the_workspace_entry_point_and_the_oracle_on_calls_in_a_row():
     lib = _binding.load_library()
-    cases = [W.make("llama7b_decode", device=DEV),
-             W.build_workload(name="second", seq_lens=np.arange(1, 40) * 97, q_lens=1, num_q_heads=32,
-                              num_kv_heads=8, head_dim=128, dtype="bf16", seed=77, device=DEV)]
+    rng = np.random.default_rng(5)
+    cases = [
+        # several partitions per sequence (split context + reduce), fp16 MHA
+        W.make("llama7b_decode", device=DEV),
+        # one partition each (no reduce between this call and the next), bf16 GQA 4:1
+        W.build_workload(name="one_part_a", seq_lens=rng.integers(200, 513, 96), q_lens=1, num_q_heads=32,
+                         num_kv_heads=8, head_dim=128, dtype="bf16", seed=77, device=DEV),
+        # one partition each, fewer sequences, fp16 GQA 2:1 at head_dim 64
+        W.build_workload(name="one_part_b", seq_lens=rng.integers(1, 400, 11), q_lens=1, num_q_heads=16,
+                         num_kv_heads=8, head_dim=64, dtype="f16", seed=78, device=DEV),
+    ]
+    args = []
     for w in cases:
         bt = torch.from_numpy(w.block_tables).to(DEV)
         sl = torch.from_numpy(w.seq_lens).to(DEV)
         need = pa.decode_workspace_bytes(w.batch, w.num_q_heads, w.head_dim, w.max_seq_len, 0)
         assert 0 < need <= SCRATCH
         ref = pa.paged_attention_decode(w.q, w.k_cache, w.v_cache, bt, sl, w.scale, w.max_seq_len)
-        out = torch.full_like(w.q, float("nan"))
-        assert _noalloc(lib, out, w, bt, sl, w.max_seq_len) == 0
+        args.append((w, bt, sl, ref))
+    # the oracle's view of a sample of each case, before anything else runs
+    samples = [_oracle_sample(w, 6, 40 + i) for i, w in enumerate(cases)]
+    outs = [torch.full_like(w.q, float("nan")) for w in cases]
+    torch.cuda.synchronize()
+    # three calls queued back to back, then the last two again in reverse order
+    for order in ([0, 1, 2], [2, 1]):
+        for i in order:
+            w, bt, sl, _ = args[i]
+            assert _noalloc(lib, outs[i], w, bt, sl, w.max_seq_len) == 0
         torch.cuda.synchronize()
-        assert torch.isfinite(out.float()).all()
-        err = float((out.float() - ref.float()).abs().max())
-        assert err <= TOL[w.dtype], err
-        del w
+        for i in order:
+            w, _, _, ref = args[i]
+            assert torch.equal(outs[i].view(torch.int16), ref.view(torch.int16)), w.name
+            seqs, oref = samples[i]
+            err = max_err(outs[i][torch.from_numpy(seqs).to(DEV)], oref)
+            assert err <= TOL[w.dtype], (w.name, err)
+            outs[i].fill_(float("nan"))
+        torch.cuda.synchronize()
     assert pa.device_error() == 0
+
+
+def test_noalloc_with_no_sequences_only_sets_up():
+    lib = _binding.load_library()
+    w = W.build_workload(name="empty", seq_lens=[16], q_lens=1, num_q_heads=8, num_kv_heads=8,
+                         head_dim=128, dtype="f16", seed=2, device=DEV)
+    bt = torch.from_numpy(w.block_tables).to(DEV)
+    sl = torch.from_numpy(w.seq_lens).to(DEV)
+    out = torch.zeros_like(w.q)
+    torch.cuda.synchronize()
+    assert _noalloc(lib, out, w, bt, sl, 16, num_seqs=0) == 0
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
