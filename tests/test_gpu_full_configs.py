@@ -25,7 +25,7 @@ def _check_cache(w, slots):
 
 
 @pytest.mark.parametrize("name,sample", [
-    ("llama7b_decode", None), ("llama7b_ctx4096", 16), ("gqa_prefix", 48), ("long_context", 2),
+    ("llama7b_decode", None), ("llama7b_ctx4096", 16), ("gqa_prefix", 48), ("long_context", None),
 ])
 def test_full_decode_config(name, sample):
     w = W.make(name, device=DEV)
