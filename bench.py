@@ -3,8 +3,12 @@ decode attention) on the LLaMA-2-7B-shaped workload: B=64 sequences, context
 lengths uniform in [512, 4096], 32 q heads = 32 kv heads, head_dim 128, fp16,
 16-token blocks scattered over a pool 10% larger than needed.
 
-Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on the
-host cores instead (the only baseline that exists for this path).
+Prints one JSON line.  After the headline (single GPU), every other workload
+is timed for about a second on its own and summarised under "configs":
+attention ms per launch, its roofline (HBM, or the tensor pipe for a call of
+prefill chunks only) and the median SM clock of its timed region.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (the
+only baseline that exists for this path).
 N > 1 (torchrun) runs independent replicas, one per GPU: the path has no
 exchange step.
 """
@@ -135,14 +139,19 @@ def _traffic_per_launch(workload: str):
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 200 ms) of the SM clock and the throttle
+    reasons; `stop` summarises all of them, `window` those taken between two
+    host times (time.time()) of the run."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
         self.path = None
+        self.rows = []
 
     def start(self):
         try:
@@ -155,6 +164,40 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    @staticmethod
+    def _when(stamp: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def _read(self):
+        self.rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 10:
+                    self.rows.append(parts)
+        os.unlink(self.path)
+
+    @classmethod
+    def summarise(cls, rows) -> dict | None:
+        if not rows:
+            return None
+        try:
+            sm = [float(r[2]) for r in rows]
+            mx = max(float(r[3]) for r in rows)
+        except ValueError:
+            return None
+        reasons = set()
+        for r in rows:
+            for name, val in zip(cls.REASONS, r[6:10]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
     def stop(self) -> dict | None:
         if self.proc is None:
             return None
@@ -163,28 +206,13 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
-        os.unlink(self.path)
-        if not rows:
-            return None
-        try:
-            sm = [float(r[1]) for r in rows]
-            mx = max(float(r[2]) for r in rows)
-        except ValueError:
-            return None
-        reasons = set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for r in rows:
-            for name, val in zip(names, r[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(rows)}
+        self._read()
+        return self.summarise(self.rows)
+
+    def window(self, t0: float, t1: float) -> dict | None:
+        """Summary of the samples taken between host times t0 and t1 (after stop)."""
+        inside = [r for r in self.rows if (lambda t: t is not None and t0 <= t <= t1)(self._when(r[0]))]
+        return self.summarise(inside)
 
 
 def cpu_baseline(w, seconds: float = 10.0) -> dict:
@@ -295,6 +323,161 @@ def run_reference(args):
     return 0
 
 
+# Workloads timed after the headline, one at a time (each freed before the
+# next), each for about SWEEP_SECONDS: every other configuration's attention
+# call with its roofline and the SM clock seen during its own timed region.
+SWEEP = ("llama7b_ctx4096", "gqa_prefix", "long_context", "mixed", "llama7b_decode_fp8", "prefill",
+         "spec_verify")
+SWEEP_SECONDS = 1.0
+
+
+class Run:
+    """One workload resident on the device and its step: slot mapping + KV
+    write (`write`), then the attention call (`attend`), all through the
+    library's public Python API."""
+
+    def __init__(self, pa, W, name: str, dev, partition: int, kw: dict):
+        import torch
+
+        self.pa = pa
+        self.name = name
+        w = self.w = W.make(name, device=dev, **kw)
+        self.T = w.num_tokens
+        self.decode = w.is_decode
+        self.fp8 = w.meta.get("cache_dtype") == "fp8"
+        self.kv_scale = w.meta.get("kv_scale", 1.0)
+        self.bt = torch.from_numpy(w.block_tables).to(dev)
+        self.sl = torch.from_numpy(w.seq_lens).to(dev)
+        self.cu = None if self.decode else torch.from_numpy(w.cu_q_lens).to(dev)
+        self.slots = torch.empty(self.T, dtype=torch.int64, device=dev)
+        self.out = torch.empty_like(w.q)
+        self.partition_arg = partition if self.decode else 0
+        if self.decode:
+            nbytes = pa.decode_workspace_bytes(w.batch, w.num_q_heads, w.head_dim, w.max_seq_len, partition)
+        else:
+            nbytes = pa.prefill_workspace_bytes(w.batch, self.T, w.num_q_heads, w.head_dim, w.max_seq_len)
+        self.wsp = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        self.max_len = w.max_seq_len
+        self.partition = pa.decode_partition(self.max_len, self.partition_arg)
+        parts = -(-self.max_len // self.partition)
+        # slot mapping + KV write; the decode plan + decode kernels; the
+        # log-sum-exp reduce when a sequence can span several partitions; the
+        # prefill plan + prefill kernels when a chunk is longer than 8 queries
+        self.launches_per_step = 4 + (1 if parts > 1 else 0) + (2 if not self.decode and w.max_q_len > 8 else 0)
+
+    def write(self, key=None, value=None, bt=None, sl=None, cu=None):
+        pa, w = self.pa, self.w
+        pa.slot_mapping(self.bt if bt is None else bt, self.sl if sl is None else sl,
+                        self.cu if cu is None else cu, self.T, w.num_blocks, out=self.slots)
+        key = w.key if key is None else key
+        value = w.value if value is None else value
+        if self.fp8:
+            pa.paged_kv_write_fp8(key, value, w.k_cache, w.v_cache, self.slots, self.kv_scale, self.kv_scale)
+        else:
+            pa.paged_kv_write(key, value, w.k_cache, w.v_cache, self.slots)
+
+    def attend(self, q=None, bt=None, sl=None, cu=None):
+        pa, w = self.pa, self.w
+        q = w.q if q is None else q
+        bt = self.bt if bt is None else bt
+        sl = self.sl if sl is None else sl
+        if self.fp8:
+            pa.paged_attention_decode_fp8(q, w.k_cache, w.v_cache, bt, sl, w.scale, self.kv_scale, self.kv_scale,
+                                          self.max_len, out=self.out, partition_size=self.partition_arg,
+                                          workspace=self.wsp)
+        elif self.decode:
+            pa.paged_attention_decode(q, w.k_cache, w.v_cache, bt, sl, w.scale, self.max_len, out=self.out,
+                                      partition_size=self.partition_arg, workspace=self.wsp)
+        else:
+            pa.paged_attention_prefill(q, w.k_cache, w.v_cache, bt, sl, self.cu if cu is None else cu, w.scale,
+                                       w.max_q_len, self.max_len, out=self.out, workspace=self.wsp)
+
+    def step(self):
+        self.write()
+        self.attend()
+
+    def timed(self, steps: int, stream):
+        """CUDA events around each step's write and attention call, on the
+        launch stream: (whole-run ms, mean attention ms, mean write ms)."""
+        import torch
+
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for e0, e1, e2 in ev:
+            e0.record(stream)
+            self.write()
+            e1.record(stream)
+            self.attend()
+            e2.record(stream)
+        torch.cuda.synchronize()
+        total_ms = ev[0][0].elapsed_time(ev[-1][2])
+        attn_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / steps
+        write_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in ev) / steps
+        return total_ms, attn_ms, write_ms
+
+    def roofline(self, attn_ms: float) -> dict:
+        """Roofline of the attention call: algorithmic bytes over HBM, or, for
+        a call of chunked-prefill rows only, algorithmic FLOPs over the dense
+        bf16 tensor peak."""
+        w = self.w
+        if not self.decode and int(w.q_lens.min()) > 8:
+            tpeak, tkind = _tensor_peak()
+            fl = _prefill_flops(w)
+            tf = fl / (attn_ms / 1e3) / 1e12
+            return {"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s", "frac": tf / tpeak,
+                    "peak_kind": f"{tkind} dense bf16 GEMM (burst)", "algorithmic_flops_per_launch": fl}
+        peak, kind = _peaks()
+        ab = _algorithmic_bytes(w)
+        gbs = ab["total"] / (attn_ms / 1e3) / 1e9
+        r = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+             "peak_kind": f"{kind} HBM copy", "frac_of_8TBs_spec": gbs / SPEC_HBM_GBS,
+             "algorithmic_bytes_per_launch": ab["total"]}
+        if ab["kv"] != ab["kv_unique"]:
+            r["logical_gbs"] = ab["total_logical"] / (attn_ms / 1e3) / 1e9
+        return r
+
+
+def _sig(x: float, digits: int = 4):
+    return float(f"{x:.{digits}g}")
+
+
+def sweep(pa, W, dev, stream, partition: int, warmup: int, names=SWEEP, seconds: float = SWEEP_SECONDS) -> dict:
+    """Time each named workload's step on its own for about `seconds`; one
+    compact record per workload (attention ms per launch, its roofline and the
+    median SM clock of its timed region)."""
+    import torch
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.5)
+    windows, rows = {}, {}
+    for name in names:
+        r = Run(pa, W, name, dev, partition, {})
+        for _ in range(max(warmup, 3)):
+            r.step()
+        est_total, _, _ = r.timed(5, stream)
+        steps = int(min(4000, max(20, seconds * 1e3 / max(est_total / 5, 1e-3))))
+        t0 = time.time()
+        total_ms, attn_ms, write_ms = r.timed(steps, stream)
+        windows[name] = (t0, time.time())
+        rl = r.roofline(attn_ms)
+        rows[name] = {"ms": _sig(attn_ms), "write_ms": _sig(write_ms), "steps": steps, "bound": rl["bound"],
+                      "achieved": _sig(rl["achieved"]), "unit": rl["unit"], "frac": _sig(rl["frac"], 3)}
+        if "logical_gbs" in rl:
+            rows[name]["logical"] = _sig(rl["logical_gbs"])
+        del r
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    clocks.stop()
+    for name, (t0, t1) in windows.items():
+        c = clocks.window(t0, t1)
+        rows[name]["sm_mhz"] = c["sm_mhz"] if c else None
+        if c and c["reasons"]:
+            rows[name]["reasons"] = c["reasons"]
+    return rows
+
+
 def run_ours(args):
     import torch
 
@@ -311,80 +494,25 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     pa.load_library()
-
-    w = W.make(args.workload, device=dev, **_workload_kw(args))
-    B = w.batch
-    T = w.num_tokens
-    decode = w.is_decode
-    fp8 = w.meta.get("cache_dtype") == "fp8"
-    kv_scale = w.meta.get("kv_scale", 1.0)
-    bt = torch.from_numpy(w.block_tables).to(dev)
-    sl = torch.from_numpy(w.seq_lens).to(dev)
-    cu = None if decode else torch.from_numpy(w.cu_q_lens).to(dev)
-    slots = torch.empty(T, dtype=torch.int64, device=dev)
-    out = torch.empty_like(w.q)
-    if decode:
-        nbytes = pa.decode_workspace_bytes(B, w.num_q_heads, w.head_dim, w.max_seq_len, args.partition)
-    else:
-        nbytes = pa.prefill_workspace_bytes(B, T, w.num_q_heads, w.head_dim, w.max_seq_len)
-    wsp = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
-    max_len = w.max_seq_len
     stream = torch.cuda.current_stream()
 
-    def step():
-        pa.slot_mapping(bt, sl, cu, T, w.num_blocks, out=slots)
-        if fp8:
-            pa.paged_kv_write_fp8(w.key, w.value, w.k_cache, w.v_cache, slots, kv_scale, kv_scale)
-        else:
-            pa.paged_kv_write(w.key, w.value, w.k_cache, w.v_cache, slots)
-
-    def attend(q=None, btab=None, lens=None, cul=None):
-        q = w.q if q is None else q
-        btab = bt if btab is None else btab
-        lens = sl if lens is None else lens
-        if fp8:
-            pa.paged_attention_decode_fp8(q, w.k_cache, w.v_cache, btab, lens, w.scale, kv_scale, kv_scale,
-                                          max_len, out=out, partition_size=args.partition, workspace=wsp)
-        elif decode:
-            pa.paged_attention_decode(q, w.k_cache, w.v_cache, btab, lens, w.scale, max_len, out=out,
-                                      partition_size=args.partition, workspace=wsp)
-        else:
-            pa.paged_attention_prefill(q, w.k_cache, w.v_cache, btab, lens, cu if cul is None else cul,
-                                       w.scale, w.max_q_len, max_len, out=out, workspace=wsp)
-
+    r = Run(pa, W, args.workload, dev, args.partition, _workload_kw(args))
+    w, T, decode, fp8 = r.w, r.T, r.decode, r.fp8
+    B = w.batch
     for _ in range(args.warmup):
-        step()
-        attend()
+        r.step()
     torch.cuda.synchronize()
-    # slot mapping + KV write; the decode plan + decode kernels; the
-    # log-sum-exp reduce when a sequence can span several partitions; the
-    # prefill plan + prefill kernels when a chunk is longer than 8 queries
-    partition = pa.decode_partition(max_len, args.partition if decode else 0)
-    parts = -(-max_len // partition)
-    launches_per_step = 4 + (1 if parts > 1 else 0) + (2 if not decode and w.max_q_len > 8 else 0)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if clocks:
         clocks.start()
         time.sleep(0.5)
     if dist:
         dist.barrier()
-    torch.cuda.synchronize()
-    for e0, e1, e2 in ev:
-        e0.record(stream)
-        step()
-        e1.record(stream)
-        attend()
-        e2.record(stream)
-    torch.cuda.synchronize()
+    total_ms, attn_ms, write_ms = r.timed(args.steps, stream)
     if dist:
         dist.barrier()
     clk = clocks.stop() if clocks else None
-    total_ms = ev[0][0].elapsed_time(ev[-1][2])
-    attn_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / args.steps
-    write_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in ev) / args.steps
     total_ms = max_over_ranks(total_ms, dist, dev)
     value = replica_throughput(ws, T, args.steps, total_ms)
 
@@ -398,7 +526,7 @@ def run_ours(args):
     bt_h = torch.from_numpy(w.block_tables).pin_memory()
     sl_h = torch.from_numpy(w.seq_lens).pin_memory()
     cu_h = None if decode else torch.from_numpy(w.cu_q_lens).pin_memory()
-    out_h = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    out_h = [torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory() for _ in range(2)]
     host_in = [t for t in (q_h, k_h, v_h, bt_h, sl_h, cu_h) if t is not None]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = out_h[0].numel() * out_h[0].element_size()
@@ -426,13 +554,9 @@ def run_ours(args):
             stream.wait_event(h2d_done[k])
             q_d, k_d, v_d, bt_d, sl_d = sets[k][:5]
             cu_d = sets[k][5] if cu_h is not None else None
-            pa.slot_mapping(bt_d, sl_d, cu_d, T, w.num_blocks, out=slots)
-            if fp8:
-                pa.paged_kv_write_fp8(k_d, v_d, w.k_cache, w.v_cache, slots, kv_scale, kv_scale)
-            else:
-                pa.paged_kv_write(k_d, v_d, w.k_cache, w.v_cache, slots)
-            attend(q_d, bt_d, sl_d, cu_d)
-            out_h[k].copy_(out, non_blocking=True)
+            r.write(k_d, v_d, bt_d, sl_d, cu_d)
+            r.attend(q_d, bt_d, sl_d, cu_d)
+            out_h[k].copy_(r.out, non_blocking=True)
             comp_done[k].record(stream)
         stream.synchronize()
         copy_stream.synchronize()
@@ -451,51 +575,47 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
 
-    peak, peak_kind = _peaks()
     ab = _algorithmic_bytes(w)
-    achieved = ab["total"] / (attn_ms / 1e3) / 1e9
-    ctx = _ctx(args.workload, w)
+    rl = r.roofline(attn_ms)
+    rl["ms_per_launch"] = attn_ms
+    if rl["bound"] == "hbm":
+        rl["traffic"] = _traffic_per_launch(args.workload)
+        rl["kernel"] = ("decode attention call (work-list plan + persistent decode kernel + log-sum-exp reduce)"
+                        if decode or w.max_q_len <= 8 else
+                        "attention call (decode and verify rows: plan + decode + reduce kernels; longer chunks: "
+                        "prefill plan + tcgen05 prefill kernel)")
+    else:
+        rl["traffic"] = None
+        rl["kernel"] = "prefill call (prefill plan + tcgen05 prefill kernel)"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": ("e4m3 cache, " if fp8 else "") + ("f16" if w.dtype == "f16" else "bf16"),
         "data": "synthetic",
-        "config": {"workload": args.workload, "batch": B, "new_tokens_per_step": T, "ctx": ctx,
+        "config": {"workload": args.workload, "batch": B, "new_tokens_per_step": T, "ctx": _ctx(args.workload, w),
                    "heads": f"{w.num_q_heads}/{w.num_kv_heads}", "head_dim": w.head_dim, "block_size": 16,
-                   "partition": partition, "pool_blocks": w.num_blocks,
+                   "partition": r.partition, "pool_blocks": w.num_blocks,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {ab['kv_unique'] / 1e9:.2f} GB of KV read per step"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _traffic_per_launch(args.workload),
-                     "kernel": ("decode attention call (work-list plan + persistent decode kernel + log-sum-exp "
-                                "reduce)" if decode or w.max_q_len <= 8 else
-                                "attention call (decode and verify rows: plan + decode + reduce kernels; "
-                                "longer chunks: prefill plan + tcgen05 prefill kernel)"),
-                     "peak_kind": f"{peak_kind} HBM copy", "frac_of_8TBs_spec": achieved / SPEC_HBM_GBS,
-                     "algorithmic_bytes_per_launch": ab["total"], "ms_per_launch": attn_ms},
+        "roofline": rl,
         "write_ms_per_step": write_ms,
         "attention_tokens_per_s": T / (attn_ms / 1e3),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "pipeline": "2-deep: next step's inputs copied on a second stream"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": r.launches_per_step * args.steps,
         "clocks": clk,
     }
-    if ab["kv"] != ab["kv_unique"]:
-        line["roofline"]["logical_gbs"] = ab["total_logical"] / (attn_ms / 1e3) / 1e9
-    if not decode and int(w.q_lens.min()) > 8:
-        # chunked prefill only: the tcgen05 kernel is bound by the tensor pipe
-        tpeak, tkind = _tensor_peak()
-        fl = _prefill_flops(w)
-        tf = fl / (attn_ms / 1e3) / 1e12
-        line["roofline"] = {"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s", "frac": tf / tpeak,
-                            "traffic": None, "kernel": "prefill call (prefill plan + tcgen05 prefill kernel)",
-                            "peak_kind": f"{tkind} dense bf16 GEMM (burst)", "algorithmic_flops_per_launch": fl,
-                            "ms_per_launch": attn_ms}
     if not decode:
         line["prefill_gflop_per_step"] = _prefill_flops(w) / 1e9
     if ws == 1 and decode and not fp8 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, seconds=args.cpu_seconds)
+    del r, w, sets
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if ws == 1 and not args.no_sweep:
+        names = [n for n in ("llama7b_decode",) + SWEEP if n != args.workload]
+        line["configs"] = sweep(pa, W, dev, stream, args.partition, 5, names)
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -515,6 +635,8 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the short timing of the other workloads after the headline")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
