@@ -370,14 +370,16 @@ int pa_paged_attention_decode(void* out, const void* q, const void* k_cache, con
                        workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream), 1, num_seqs);
 }
 
-// Prefill workspace: [tile work list: num_seqs + 1 int32, 256-aligned][decode-row partials].
-// prefill plan: offsets (num_seqs + 1) and the cost-sorted pair list.  A pair
+// Prefill workspace: [tile work list, 256-aligned][decode-row partials].
+// prefill plan: offsets (num_seqs + 1), the cost-sorted pair list and each
+// pair's sequence (pair_cap entries each, pair_cap = num_tokens / 4 +
+// num_seqs).  A pair
 // is two tiles of at least 2 queries (128 rows / at most PA_MAX_GROUP = 64
 // heads), so a chunk of q queries has at most q / 4 + 1 pairs.
 static_assert(PA_MAX_GROUP <= 64, "the plan's pair bound assumes tiles of at least 2 queries");
 static size_t plan_bytes(int num_seqs, int num_tokens) {
     const size_t pairs = static_cast<size_t>(num_tokens) / 4 + static_cast<size_t>(num_seqs);
-    return align256((static_cast<size_t>(num_seqs) + 1 + pairs) * sizeof(int32_t));
+    return align256((static_cast<size_t>(num_seqs) + 1 + 2 * pairs) * sizeof(int32_t));
 }
 
 int pa_paged_kv_write_fp8(const void* key, const void* value, void* k_cache, void* v_cache,
@@ -484,11 +486,13 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
     // tiles of 128 / group queries (every supported grouping) on the tcgen05
     // tensor cores, running beside the decode rows: the decode plan and the
     // prefill kernel go first; the decode kernel then starts on the SMs the
-    // prefill kernel leaves free
+    // prefill kernel leaves free.  K comes in one box per 64-dim half of a
+    // block, V in one box per block.
     if (!make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) ||
-        !make_kv_map(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype))
+        !make_kv_map_block(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype))
         return PA_ERR_CUDA;
     p.q_per_tile = 128 / group;
+    p.pair_cap = num_tokens / 4 + num_seqs;
     CUtensorMap qmap;
     if (!make_q_map(&qmap, q, num_tokens, num_q_heads, head_dim, group, p.q_per_tile, dtype)) return PA_ERR_CUDA;
     if (pa::launch_decode_plan(dc.p, s) != cudaSuccess) return PA_ERR_CUDA;

@@ -98,6 +98,7 @@ struct PrefillParams {
     // the first overlap_ctas CTAs take prefill work; the others leave their SMs
     const int32_t* decode_units;
     int overlap_ctas;
+    int pair_cap;                 // pair-list capacity of the plan (num_tokens / 4 + num_seqs)
 };
 
 // Launchers (return cudaError_t of the launch).

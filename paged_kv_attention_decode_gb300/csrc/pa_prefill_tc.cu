@@ -71,7 +71,10 @@ constexpr unsigned kFullMask = 0xffffffffu;
 template <int D>
 struct TcShape {
     static constexpr int kKeyHalf = kTcKeys * 128;          // 128 keys x one 64-dim half
-    static constexpr int kKV = (D / 64) * kKeyHalf;         // K or V of one tile: [half][key][128 B]
+    // K or V of one tile: K as [half][key][128 B] (the S MMA's N = 128 keys
+    // need one stride between 8-key groups), V as [block][half][16 keys][128 B]
+    // (a P V MMA's K = 16 keys are one block: one box per block)
+    static constexpr int kKV = (D / 64) * kKeyHalf;
     static constexpr int kQHalf = 128 * 128;                // 128 rows x one half
     static constexpr int kQ = (D / 64) * kQHalf;            // one query tile
     static constexpr int kBudget = 227 * 1024 - 1024;      // dynamic shared memory less alignment slack
@@ -184,15 +187,20 @@ static_assert(kPlanBuckets == 2 * 1024, "the plan's class scan takes two classes
 // rows and belong to the decode kernel); offsets[B] = total.  order[0 ..
 // total) = the global pair indices sorted by the number of key tiles they
 // read, longest first (a counting sort; the order within a cost class is
-// arbitrary and does not affect any result).  One CTA.
+// arbitrary and does not affect any result).  seq_of_pair[l] = the sequence
+// of global pair l, so that an item finds its sequence with one load.  The
+// pair lists hold at most pair_cap = num_tokens / 4 + num_seqs entries.
+// One CTA.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __restrict__ cu_q_lens,
                                                             const int32_t* __restrict__ seq_lens, int num_seqs,
                                                             int num_tokens, int q_per_tile,
-                                                            int32_t* __restrict__ offsets, unsigned int* err) {
+                                                            int32_t* __restrict__ offsets, int pair_cap,
+                                                            unsigned int* err) {
     __shared__ int warp_tot[32];
     __shared__ int carry;
     __shared__ int hist[kPlanBuckets];
     int32_t* order = offsets + num_seqs + 1;
+    int32_t* seq_of_pair = order + pair_cap;
     const int tid = threadIdx.x;
     if (tid == 0) carry = 0;
     for (int i = tid; i < kPlanBuckets; i += 1024) hist[i] = 0;
@@ -225,7 +233,10 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
             for (int pr = 0; pr < v; ++pr) atomicAdd(&hist[bucket(n, ql, pr)], 1);
         }
         const int start = block_exclusive_scan_1024(v, warp_tot, &carry);
-        if (b < num_seqs) offsets[b] = start;
+        if (b < num_seqs) {
+            offsets[b] = start;
+            for (int pr = 0; pr < v; ++pr) seq_of_pair[start + pr] = b;
+        }
     }
     if (tid == 0) offsets[num_seqs] = carry;
     __syncthreads();
@@ -377,12 +388,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     auto decode_item = [&](int w, Item& it) -> bool {
         it.g = w % p.num_kv_heads;
         const int l = snake ? plan[p.num_seqs + 1 + w / p.num_kv_heads] : w / p.num_kv_heads;
-        int lo = 0, hi = p.num_seqs - 1;  // last b with plan[b] <= l
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (plan[mid] <= l) lo = mid; else hi = mid - 1;
-        }
-        const int b = lo;
+        const int b = plan[p.num_seqs + 1 + p.pair_cap + l];   // the pair's sequence
         it.row0 = p.cu_q_lens[b];
         it.qlen = p.cu_q_lens[b + 1] - it.row0;
         const int ntiles = (it.qlen + QT - 1) / QT;
@@ -606,8 +612,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             const int key = idx / CPR;
                             const int c = idx - key * CPR;
                             if (key0 + key > it.pos_pair || ((bad >> (key >> 4)) & 1u))
-                                *reinterpret_cast<uint4*>(vt + (c >> 3) * Sh::kKeyHalf + key * 128 +
-                                                          (((c & 7) ^ (key & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+                                *reinterpret_cast<uint4*>(vt + (key >> 4) * (D / 64) * 2048 + (c >> 3) * 2048 +
+                                                          (key & 15) * 128 + (((c & 7) ^ (key & 7)) << 4)) =
+                                    make_uint4(0, 0, 0, 0);
                         }
                         fence_proxy_async_smem();
                     }
@@ -686,7 +693,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ++s_issued[x];
             };
             // O_X += P_X(j) V(j): P is read from tensor memory, where the softmax
-            // stored it over the first 64 columns of S_X
+            // stored it over the first 64 columns of S_X; MMA kp reads block kp
+            // of the V tile (its two 64-dim halves 2 KB apart)
             auto mma_pv = [&](int x, int j) {
                 const int Tx = t0[x] + j;
                 if (lane == 0) {
@@ -695,7 +703,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t va = smem_addr(vst((kv0 + j) % NV));
 #pragma unroll
                     for (int kp = 0; kp < kTcKeys / 16; ++kp) {
-                        const uint64_t bd = smem_desc_sw128(va + kp * 2048, Sh::kKeyHalf, 1024);
+                        const uint64_t bd = smem_desc_sw128(va + kp * (D / 64) * 2048, 2048, 1024);
                         tc_mma_f16_ta(o_tm, p_tm + static_cast<uint32_t>(kp * 8), bd, kIdescPV,
                                       (j > 0 || kp > 0) ? 1u : 0u);
                     }
@@ -767,11 +775,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ================================ loaders ===============================
-        // Loader li issues the boxes b = li, li + 3, ... of each K and V tile,
-        // box b = one 64-dim half (b % (D/64)) of one 16-token block
-        // (b / (D/64)); lane 0 issues, and arrives on the tile's barrier with
-        // its bytes.  Before a stage is refilled, the MMA warp's k_free /
-        // v_free for the stage's previous tile is awaited.
+        // Loader li issues the boxes b = li, li + 3, ... of each K tile, box
+        // b = one 64-dim half (b % (D/64)) of one 16-token block (b / (D/64)),
+        // and the boxes of blocks li, li + 3, ... of each V tile, one box per
+        // block (all D dims of its 16 rows); lane 0 issues, and arrives on the
+        // tile's barrier with its bytes.  Before a stage is refilled, the MMA
+        // warp's k_free / v_free for the stage's previous tile is awaited.
+        // Loader 0 also loads the query tiles, after the item's first K and V
+        // boxes: only the query tiles wait for the previous item to drain.
         reg_dealloc<kTcOtherRegs>();
         const int li = warp - kTcMmaWarp - 1;
         constexpr int kHalves = D / 64;
@@ -791,10 +802,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                         for (int h = 0; h < kHalves; ++h) mine |= (blk * kHalves + h) % kTcLoaders == li;
                         int id = -1;
-                        if (mine && j * kTcBlocks + blk < it.nblk_live) {
+                        if (j * kTcBlocks + blk < it.nblk_live) {
                             id = it.bt[j * kTcBlocks + blk];
                             if (id < 0 || id >= p.num_blocks) {
-                                record_error(p.err, PA_DEVERR_BLOCK_ID_);
+                                if (mine) record_error(p.err, PA_DEVERR_BLOCK_ID_);
                                 id = -1;
                             }
                         }
@@ -812,22 +823,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int sk = J % NK;
                     if (!v) ids_of(j, sk);
                     uint32_t bytes = 0;
-                    for (int b = li; b < kBoxes; b += kTcLoaders)
-                        if (stage_blocks[li][sk][b / kHalves] >= 0) bytes += 2048;
+                    if (v) {
+                        for (int blk = li; blk < kTcBlocks; blk += kTcLoaders)
+                            if (stage_blocks[li][sk][blk] >= 0) bytes += kHalves * 2048;
+                    } else {
+                        for (int b = li; b < kBoxes; b += kTcLoaders)
+                            if (stage_blocks[li][sk][b / kHalves] >= 0) bytes += 2048;
+                    }
                     uint64_t* bar = v ? &v_full[s] : &k_full[s];
                     mbar_arrive_expect_tx(bar, bytes);
-                    uint8_t* dst = v ? vst(s) : kst(s);
-                    const CUtensorMap* map = v ? &vmap : &kmap;
-                    for (int b = li; b < kBoxes; b += kTcLoaders) {
-                        const int blk = b / kHalves, h = b % kHalves;
-                        const int id = stage_blocks[li][sk][blk];
-                        if (id >= 0) tma_load_4d(dst + h * Sh::kKeyHalf + blk * 2048, map, bar, 0, h, it.g, id * 16);
+                    if (v) {
+                        for (int blk = li; blk < kTcBlocks; blk += kTcLoaders) {
+                            const int id = stage_blocks[li][sk][blk];
+                            if (id >= 0) tma_load_4d(vst(s) + blk * kHalves * 2048, &vmap, bar, 0, id * 16, 0, it.g);
+                        }
+                    } else {
+                        for (int b = li; b < kBoxes; b += kTcLoaders) {
+                            const int blk = b / kHalves, h = b % kHalves;
+                            const int id = stage_blocks[li][sk][blk];
+                            if (id >= 0) tma_load_4d(kst(s) + h * Sh::kKeyHalf + blk * 2048, &kmap, bar, 0, h, it.g, id * 16);
+                        }
                     }
                     if (v) ++v_total; else ++k_total;
                     return true;
                 };
                 // the item's query tiles, once the previous item's MMAs are done
-                if (li == 0) {
+                auto load_q = [&]() {
                     if (items > 0) ok = wait_or_abort(&item_done, (items - 1) & 1, abort_v);
                     if (ok) {
                         mbar_arrive_expect_tx(&q_full, static_cast<uint32_t>((it.nkx[1] ? 2 : 1) * q_tile_bytes));
@@ -840,8 +861,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                             it.row0 + it.q0[x]);
                         }
                     }
+                };
+                for (int j = 0; ok && j < it.nkt; ++j) {
+                    ok = issue(j, false) && issue(j, true);
+                    if (j == 0 && li == 0 && ok) load_q();
                 }
-                for (int j = 0; ok && j < it.nkt; ++j) ok = issue(j, false) && issue(j, true);
                 if (!ok) *abort_v = 1;
             }
             ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
@@ -877,7 +901,7 @@ cudaError_t launch_t(const PrefillParams& p, int32_t* plan, const CUtensorMap& k
     }();
     if (launch_regs < kTcLaunchRegs) return cudaErrorInvalidConfiguration;
     prefill_plan_kernel<<<1, 1024, 0, s>>>(p.cu_q_lens, p.seq_lens, p.num_seqs, num_tokens, p.q_per_tile, plan,
-                                           p.err);
+                                           p.pair_cap, p.err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // upper bound on the work items: each listed chunk (length > 8) has at

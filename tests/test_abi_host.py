@@ -92,7 +92,8 @@ def test_workspace_sizes(lib):
     # prefill: [plan: offsets (B + 1) + cost-sorted pair list (T / 4 + B) int32]
     # + the decode part, partials rows = min(num_tokens, 8 * num_seqs) (decode and verify chunks)
     def _plan(B, T):
-        return _align((B + 1 + T // 4 + B) * 4)
+        # offsets, then two pair lists (the cost order, each pair's sequence)
+        return _align((B + 1 + 2 * (T // 4 + B)) * 4)
     assert pa.prefill_workspace_bytes(8, 8, 64, 128, 131072) == (_plan(8, 8)
                                                                  + pa.decode_workspace_bytes(8, 64, 128, 131072, 0))
     assert pa.prefill_workspace_bytes(8, 6000, 64, 128, 131072) == (_plan(8, 6000) + 256 + _align(8 * 64 * 4)
