@@ -50,10 +50,14 @@ def _load():
         lib.oracle_paged_attention_decode_fp8.argtypes = [
             _p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32, _i32,
             ctypes.c_double, _i32, ctypes.c_double, ctypes.c_double, _p, _i64, _i32]
+        lib.oracle_paged_attention_prefill_fp8.argtypes = [
+            _p, _p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32,
+            ctypes.c_double, _i32, ctypes.c_double, ctypes.c_double, _p, _i64, _i32]
         for f in ("oracle_decode_values", "oracle_slot_mapping", "oracle_kv_write",
                   "oracle_paged_attention_decode", "oracle_paged_attention_prefill",
                   "oracle_num_threads", "oracle_decode_e4m3", "oracle_encode_e4m3",
-                  "oracle_kv_write_fp8", "oracle_paged_attention_decode_fp8"):
+                  "oracle_kv_write_fp8", "oracle_paged_attention_decode_fp8",
+                  "oracle_paged_attention_prefill_fp8"):
             getattr(lib, f).restype = _i32
         _lib = lib
     return _lib
@@ -209,5 +213,30 @@ def paged_attention_decode_fp8(q_bits, k_cache_codes, v_cache_codes, block_table
     _check(_load().oracle_paged_attention_decode_fp8(
         _ptr(out), _ptr(q_bits), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(sl), B, NB, Hq, Hkv, D, bs,
         float(scale), _DT[q_dtype], float(k_scale), float(v_scale), _ptr(sel),
+        0 if sel is None else sel.size, threads))
+    return out
+
+
+def paged_attention_prefill_fp8(q_bits, k_cache_codes, v_cache_codes, block_tables, seq_lens, q_lens,
+                                scale: float, q_dtype: str, k_scale: float, v_scale: float, select=None,
+                                threads: int = 0) -> np.ndarray:
+    """fp64 causal varlen attention over a head-major E4M3 cache [NB, Hkv, bs, D]
+    (values = code * scale): q [T, Hq, D] -> out [n, Hq, D] (n = T or len(select))."""
+    q_bits = _c(q_bits, np.uint16)
+    T, Hq, D = q_bits.shape
+    NB, Hkv, bs, D2 = k_cache_codes.shape
+    assert D2 == D
+    kc = _c(k_cache_codes, np.uint8)
+    vc = _c(v_cache_codes, np.uint8)
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    ql = _c(q_lens, np.int32)
+    assert int(ql.sum()) == T
+    sel = None if select is None else _c(select, np.int64)
+    n = T if sel is None else sel.size
+    out = np.empty((n, Hq, D), dtype=np.float64)
+    _check(_load().oracle_paged_attention_prefill_fp8(
+        _ptr(out), _ptr(q_bits), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(sl), _ptr(ql), sl.size, NB,
+        Hq, Hkv, D, bs, float(scale), _DT[q_dtype], float(k_scale), float(v_scale), _ptr(sel),
         0 if sel is None else sel.size, threads))
     return out

@@ -399,10 +399,49 @@ int oracle_paged_attention_decode(double* out, const uint16_t* q, const uint16_t
     return rc;
 }
 
+/* The rows of a varlen call: row i of sequence b sits at position
+ * seq_lens[b] - q_lens[b] + i and sees positions 0..that position
+ * ("vLLM-Ascend 原理", section 2.3, causal self-attention; section 2.4: a
+ * later chunk reads what earlier chunks wrote).  sel (optional) lists the q
+ * rows to compute.  Fills J's row arrays; *buf is freed by the caller. */
+static int prefill_rows(job_t* J, int64_t** buf, const int32_t* seq_lens, const int32_t* q_lens, int B,
+                        const int64_t* sel, int64_t n_sel) {
+    *buf = NULL;
+    int64_t T = 0;
+    for (int b = 0; b < B; ++b) {
+        if (q_lens[b] < 0 || q_lens[b] > seq_lens[b]) return OR_ERR_ARG;
+        T += q_lens[b];
+    }
+    int64_t n = sel ? n_sel : T;
+    /* per packed row: sequence, position; per computed row: sequence, position, q row */
+    int64_t* m = (int64_t*)malloc(sizeof(int64_t) * (size_t)((T > 0 ? T : 1) * 2 + (n > 0 ? n : 1) * 3));
+    if (!m) return OR_ERR_NOMEM;
+    int64_t *seq_of = m, *pos_of = m + T;
+    int64_t *row_seq = m + 2 * T, *row_pos = row_seq + n, *row_q = row_seq + 2 * n;
+    int64_t r = 0;
+    for (int b = 0; b < B; ++b)
+        for (int i = 0; i < q_lens[b]; ++i, ++r) {
+            seq_of[r] = b;
+            pos_of[r] = (int64_t)seq_lens[b] - q_lens[b] + i;
+        }
+    int max_len = 1;
+    for (int64_t k = 0; k < n; ++k) {
+        int64_t qr = sel ? sel[k] : k;
+        if (qr < 0 || qr >= T) { free(m); return OR_ERR_ARG; }
+        row_seq[k] = seq_of[qr];
+        row_pos[k] = pos_of[qr];
+        row_q[k] = qr;
+        if (pos_of[qr] + 1 > max_len) max_len = (int)(pos_of[qr] + 1);
+    }
+    J->row_seq = row_seq; J->row_pos = row_pos; J->row_qrow = row_q;
+    J->n_rows = n; J->max_len = max_len;
+    *buf = m;
+    return OR_OK;
+}
+
 /* Varlen causal attention over the paged cache.  q [T, Hq, D], rows packed
- * per sequence (q_lens[b] rows each).  Row i of sequence b sits at position
- * seq_lens[b] - q_lens[b] + i and sees positions 0..that position.
- * sel (optional) lists the q rows to compute; out is [n, Hq, D] fp64. */
+ * per sequence (q_lens[b] rows each); out is [n, Hq, D] fp64 (n = T, or the
+ * sel rows). */
 int oracle_paged_attention_prefill(double* out, const uint16_t* q, const uint16_t* k_cache,
                                    const uint16_t* v_cache, const int32_t* block_tables,
                                    int max_blocks, const int32_t* seq_lens,
@@ -411,42 +450,46 @@ int oracle_paged_attention_prefill(double* out, const uint16_t* q, const uint16_
                                    const int64_t* sel, int64_t n_sel, int num_threads) {
     int rc = check_common(B, Hq, Hkv, D, block_size, dtype);
     if (rc) return rc;
-    int64_t T = 0;
-    for (int b = 0; b < B; ++b) {
-        if (q_lens[b] < 0 || q_lens[b] > seq_lens[b]) return OR_ERR_ARG;
-        T += q_lens[b];
-    }
-    int64_t* seq_of = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T > 0 ? T : 1) * 2);
-    if (!seq_of) return OR_ERR_NOMEM;
-    int64_t* pos_of = seq_of + T;
-    int64_t r = 0;
-    for (int b = 0; b < B; ++b)
-        for (int i = 0; i < q_lens[b]; ++i, ++r) {
-            seq_of[r] = b;
-            pos_of[r] = (int64_t)seq_lens[b] - q_lens[b] + i;
-        }
-    int64_t n = sel ? n_sel : T;
-    int64_t* rs = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1) * 3);
-    if (!rs) { free(seq_of); return OR_ERR_NOMEM; }
-    int64_t *row_seq = rs, *row_pos = rs + n, *row_q = rs + 2 * n;
-    int max_len = 1;
-    for (int64_t k = 0; k < n; ++k) {
-        int64_t qr = sel ? sel[k] : k;
-        if (qr < 0 || qr >= T) { free(rs); free(seq_of); return OR_ERR_ARG; }
-        row_seq[k] = seq_of[qr];
-        row_pos[k] = pos_of[qr];
-        row_q[k] = qr;
-        if (pos_of[qr] + 1 > max_len) max_len = (int)(pos_of[qr] + 1);
-    }
     job_t J;
     memset(&J, 0, sizeof J);
+    int64_t* buf = NULL;
+    rc = prefill_rows(&J, &buf, seq_lens, q_lens, B, sel, n_sel);
+    if (rc) return rc;
     J.q = q; J.k_cache = k_cache; J.v_cache = v_cache; J.block_tables = block_tables;
-    J.seq_lens = seq_lens; J.row_seq = row_seq; J.row_pos = row_pos; J.row_qrow = row_q;
-    J.n_rows = n; J.max_blocks = max_blocks; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
+    J.seq_lens = seq_lens; J.max_blocks = max_blocks; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
     J.block_size = block_size; J.num_blocks = num_blocks; J.scale = scale;
-    J.tab = table_for(dtype); J.out = out; J.max_len = max_len;
+    J.tab = table_for(dtype); J.out = out;
     rc = run_rows(&J, num_threads);
-    free(rs); free(seq_of);
+    free(buf);
+    return rc;
+}
+
+/* Varlen causal attention over a head-major E4M3 cache: the rows of
+ * oracle_paged_attention_prefill, the keys and values of
+ * oracle_paged_attention_decode_fp8 (k_t = e4m3(code) * k_scale,
+ * v_t = e4m3(code) * v_scale; "vLLM-Ascend 原理", section 4 "量化": the cache
+ * itself is quantised, so prefill chunks and speculative-verify rows read it
+ * the same way decode rows do). */
+int oracle_paged_attention_prefill_fp8(double* out, const uint16_t* q, const uint8_t* k_cache,
+                                       const uint8_t* v_cache, const int32_t* block_tables, int max_blocks,
+                                       const int32_t* seq_lens, const int32_t* q_lens, int B, int num_blocks,
+                                       int Hq, int Hkv, int D, int block_size, double scale, int q_dtype,
+                                       double k_scale, double v_scale, const int64_t* sel, int64_t n_sel,
+                                       int num_threads) {
+    int rc = check_common(B, Hq, Hkv, D, block_size, q_dtype);
+    if (rc) return rc;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    int64_t* buf = NULL;
+    rc = prefill_rows(&J, &buf, seq_lens, q_lens, B, sel, n_sel);
+    if (rc) return rc;
+    J.q = q; J.k8 = k_cache; J.v8 = v_cache; J.k_scale = k_scale; J.v_scale = v_scale;
+    J.tab8 = table_e4m3(); J.block_tables = block_tables;
+    J.seq_lens = seq_lens; J.max_blocks = max_blocks; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
+    J.block_size = block_size; J.num_blocks = num_blocks; J.scale = scale;
+    J.tab = table_for(q_dtype); J.out = out;
+    rc = run_rows(&J, num_threads);
+    free(buf);
     return rc;
 }
 
