@@ -326,7 +326,7 @@ def run_reference(args):
 # Workloads timed after the headline, one at a time (each freed before the
 # next), each for about SWEEP_SECONDS: every other configuration's attention
 # call with its roofline and the SM clock seen during its own timed region.
-SWEEP = ("llama7b_ctx4096", "gqa_prefix", "long_context", "mixed", "llama7b_decode_fp8", "prefill",
+SWEEP = ("llama7b_ctx4096", "gqa_prefix", "long_context", "mixed", "llama7b_decode_fp8", "mixed_fp8", "prefill",
          "spec_verify")
 SWEEP_SECONDS = 1.0
 
@@ -381,10 +381,14 @@ class Run:
         q = w.q if q is None else q
         bt = self.bt if bt is None else bt
         sl = self.sl if sl is None else sl
-        if self.fp8:
+        if self.fp8 and self.decode:
             pa.paged_attention_decode_fp8(q, w.k_cache, w.v_cache, bt, sl, w.scale, self.kv_scale, self.kv_scale,
                                           self.max_len, out=self.out, partition_size=self.partition_arg,
                                           workspace=self.wsp)
+        elif self.fp8:
+            pa.paged_attention_prefill_fp8(q, w.k_cache, w.v_cache, bt, sl, self.cu if cu is None else cu, w.scale,
+                                           self.kv_scale, self.kv_scale, w.max_q_len, self.max_len, out=self.out,
+                                           workspace=self.wsp)
         elif self.decode:
             pa.paged_attention_decode(q, w.k_cache, w.v_cache, bt, sl, w.scale, self.max_len, out=self.out,
                                       partition_size=self.partition_arg, workspace=self.wsp)
@@ -462,8 +466,9 @@ def sweep(pa, W, dev, stream, partition: int, warmup: int, names=SWEEP, seconds:
         total_ms, attn_ms, write_ms = r.timed(steps, stream)
         windows[name] = (t0, time.time())
         rl = r.roofline(attn_ms)
-        rows[name] = {"ms": _sig(attn_ms), "write_ms": _sig(write_ms), "steps": steps, "bound": rl["bound"],
-                      "achieved": _sig(rl["achieved"]), "unit": rl["unit"], "frac": _sig(rl["frac"], 3)}
+        # achieved is GB/s for an "hbm" bound, TFLOP/s for "tensor"
+        rows[name] = {"ms": _sig(attn_ms), "write_ms": _sig(write_ms, 3), "steps": steps, "bound": rl["bound"],
+                      "achieved": _sig(rl["achieved"]), "frac": _sig(rl["frac"], 3)}
         if "logical_gbs" in rl:
             rows[name]["logical"] = _sig(rl["logical_gbs"])
         del r

@@ -287,6 +287,26 @@ int pa_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache,
                                   void* workspace, size_t workspace_bytes, int dtype, void* stream);
 
 /*
+ * A continuous-batching step over an FP8 cache ("vLLM-Ascend 原理", section 4
+ * "量化": the cache itself is quantised, so every row kind reads it through
+ * the block table and dequantises it; section 4 "推测解码" for the verify
+ * rows): as pa_paged_attention_prefill with k_t = code * k_scale and
+ * v_t = code * v_scale over the head-major E4M3 pools described above.
+ * head_dim must be 128; q and out keep `dtype`; the workspace is sized by
+ * pa_prefill_workspace_bytes.  Rows of at most PA_VERIFY_MAX_Q queries read
+ * the codes like pa_paged_attention_decode_fp8; longer chunks widen each
+ * (block, kv head) tile to 16-bit in shared memory (exact: every E4M3 value is
+ * an fp16 and a bf16 value) for the tensor cores.
+ */
+int pa_paged_attention_prefill_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* seq_lens, const int32_t* cu_q_lens, int num_seqs,
+                                   int num_tokens, int max_q_len, int max_seq_len, int num_blocks,
+                                   float scale, float k_scale, float v_scale, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size, void* workspace,
+                                   size_t workspace_bytes, int dtype, void* stream);
+
+/*
  * Decode attention for callers that cannot allocate device memory.
  *
  * No counterpart in the pages: this is a deployment variant of

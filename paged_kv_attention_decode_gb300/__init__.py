@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     paged_attention_decode,
     paged_attention_decode_fp8,
     paged_attention_prefill,
+    paged_attention_prefill_fp8,
     paged_kv_gather,
     paged_kv_write,
     paged_kv_write_fp8,

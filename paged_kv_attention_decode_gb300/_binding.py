@@ -44,6 +44,8 @@ _SIGNATURES = {
     "pa_paged_kv_write_fp8": (_i32, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _p]),
     "pa_paged_attention_decode_fp8": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _f32, _f32, _f32,
                                              _i32, _i32, _i32, _i32, _i32, _p, _sz, _i32, _p]),
+    "pa_paged_attention_prefill_fp8": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32, _i32,
+                                              _f32, _f32, _f32, _i32, _i32, _i32, _i32, _p, _sz, _i32, _p]),
     "pa_copy_blocks": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _p]),
     "pa_decode_partition": (_i32, [_i32, _i32]),
     "pa_selftest_wait_timeout": (_i32, [_p]),
@@ -331,4 +333,33 @@ def paged_attention_decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
         block_tables.shape[1], seq_lens.data_ptr(), B, max_seq_len, NB, float(scale), float(k_scale),
         float(v_scale), Hq, Hkv, D, bs, partition_size, _ptr(workspace), ws_bytes, _dt(q), _stream(stream))
     _check(rc, "pa_paged_attention_decode_fp8")
+    return out
+
+
+def paged_attention_prefill_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                block_tables: torch.Tensor, seq_lens: torch.Tensor, cu_q_lens: torch.Tensor,
+                                scale: float, k_scale: float, v_scale: float, max_q_len: int, max_seq_len: int,
+                                out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                                stream=None) -> torch.Tensor:
+    """Causal varlen attention of new query rows over head-major FP8 (E4M3)
+    pools [NB, Hkv, 16, 128] (decodes, speculative-verify rows and prefill
+    chunks in one call)."""
+    _cuda(q, k_cache, v_cache, block_tables, seq_lens, cu_q_lens, out, workspace)
+    _u8(k_cache), _u8(v_cache)
+    T, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    _need(D2 == D and v_cache.shape == k_cache.shape, "cache shape")
+    B = seq_lens.shape[0]
+    _need(cu_q_lens.shape[0] == B + 1 and cu_q_lens.dtype == torch.int32, "cu_q_lens")
+    if out is None:
+        out = torch.empty_like(q)
+    nbytes = prefill_workspace_bytes(B, T, Hq, D, max_seq_len)
+    workspace = _workspace(nbytes, q.device, workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().pa_paged_attention_prefill_fp8(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        block_tables.shape[1], seq_lens.data_ptr(), cu_q_lens.data_ptr(), B, T, max_q_len, max_seq_len, NB,
+        float(scale), float(k_scale), float(v_scale), Hq, Hkv, D, bs, _ptr(workspace), ws_bytes, _dt(q),
+        _stream(stream))
+    _check(rc, "pa_paged_attention_prefill_fp8")
     return out

@@ -319,9 +319,8 @@ static int decode_prepare(DecodeCall& c, void* out, const void* q, const void* k
     p.max_rows = max_rows;
     p.num_rows = num_rows;
     // (query, head) columns per work item: 8, or 16 once a row can have more
-    // (the FP8 kernels take 8 per item)
     const int cols = max_q * p.group;
-    const int chunk = (cols > 8 && !fp8) ? 16 : 8;
+    const int chunk = cols > 8 ? 16 : 8;
     p.col_chunks = (cols + chunk - 1) / chunk;
     p.scale_log2 = scale_log2(scale) * k_scale;
     p.v_scale = v_scale;
@@ -433,22 +432,14 @@ size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_q_heads,
                                                   parts_for(max_seq_len, effective_partition(max_seq_len, 0)));
 }
 
-int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
-                               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
-                               const int32_t* cu_q_lens, int num_seqs, int num_tokens, int max_q_len,
-                               int max_seq_len, int num_blocks, float scale, int num_q_heads, int num_kv_heads,
-                               int head_dim, int block_size, void* workspace, size_t workspace_bytes, int dtype,
-                               void* stream) {
-    int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size, dtype, num_blocks);
-    if (rc) return rc;
-    if (num_seqs < 0 || num_seqs > kMaxGrid || num_tokens < 0 || max_q_len < 0 || max_seq_len < 0 ||
-        max_blocks_per_seq <= 0)
-        return PA_ERR_INVALID_ARG;
-    if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
-    if (num_seqs == 0 || num_tokens == 0) return PA_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_q_lens) return PA_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+// Everything a varlen call does, for either cache type; arguments are
+// validated by the entry points.
+static int prefill_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                        const int32_t* cu_q_lens, int num_seqs, int num_tokens, int max_q_len, int max_seq_len,
+                        int num_blocks, float scale, int num_q_heads, int num_kv_heads, int head_dim,
+                        void* workspace, size_t workspace_bytes, int dtype, cudaStream_t s, bool fp8,
+                        float k_scale, float v_scale) {
     const size_t pb = plan_bytes(num_seqs, num_tokens);
     if (!workspace ||
         workspace_bytes < pa_prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, head_dim, max_seq_len))
@@ -460,10 +451,10 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
     // through the decode kernel
     const int max_q = std::max(1, std::min(max_q_len, PA_VERIFY_MAX_Q));
     DecodeCall dc;
-    rc = decode_prepare(dc, out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens, num_seqs,
-                        max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, 0,
-                        static_cast<uint8_t*>(workspace) + pb, workspace_bytes - pb, dtype, max_q,
-                        verify_rows_bound(num_seqs, num_tokens), num_tokens);
+    int rc = decode_prepare(dc, out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens,
+                            num_seqs, max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, 0,
+                            static_cast<uint8_t*>(workspace) + pb, workspace_bytes - pb, dtype, max_q,
+                            verify_rows_bound(num_seqs, num_tokens), num_tokens, fp8, k_scale, v_scale);
     if (rc) return rc;
     if (max_q_len <= PA_VERIFY_MAX_Q) return decode_launch(dc, s);
     unsigned int* err = error_word();
@@ -481,16 +472,20 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
     p.num_q_heads = num_q_heads;
     p.num_kv_heads = num_kv_heads;
     p.group = group;
-    p.scale_log2 = scale_log2(scale);
+    p.scale_log2 = scale_log2(scale) * k_scale;
+    p.v_scale = v_scale;
     CUtensorMap kmap, vmap;
     // tiles of 128 / group queries (every supported grouping) on the tcgen05
     // tensor cores, running beside the decode rows: the decode plan and the
     // prefill kernel go first; the decode kernel then starts on the SMs the
-    // prefill kernel leaves free.  K comes in one box per 64-dim half of a
-    // block, V in one box per block.
-    if (!make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) ||
-        !make_kv_map_block(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype))
-        return PA_ERR_CUDA;
+    // prefill kernel leaves free.  16-bit K comes in one box per 64-dim half
+    // of a block, 16-bit V in one box per block; E4M3 K and V in one box per
+    // (block, kv head) of the head-major pools, widened in shared memory.
+    const bool maps_ok = fp8 ? make_kv_map_fp8(&kmap, k_cache, num_blocks, num_kv_heads) &&
+                                   make_kv_map_fp8(&vmap, v_cache, num_blocks, num_kv_heads)
+                             : make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) &&
+                                   make_kv_map_block(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype);
+    if (!maps_ok) return PA_ERR_CUDA;
     p.q_per_tile = 128 / group;
     p.pair_cap = num_tokens / 4 + num_seqs;
     CUtensorMap qmap;
@@ -498,10 +493,53 @@ int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, co
     if (pa::launch_decode_plan(dc.p, s) != cudaSuccess) return PA_ERR_CUDA;
     p.decode_units = dc.p.unit_count;
     p.overlap_ctas = std::max(1, pa::sm_count() * kOverlapPrefillNum / kOverlapPrefillDen);
-    if (pa::launch_prefill_tc(p, plan, kmap, vmap, qmap, head_dim, dtype, max_q_len, num_tokens, s) != cudaSuccess)
+    if (pa::launch_prefill_tc(p, plan, kmap, vmap, qmap, head_dim, dtype, max_q_len, num_tokens, fp8, s) !=
+        cudaSuccess)
         return PA_ERR_CUDA;
     dc.p.overlap = 1;
     return decode_launch(dc, s);
+}
+
+int pa_paged_attention_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                               const int32_t* cu_q_lens, int num_seqs, int num_tokens, int max_q_len,
+                               int max_seq_len, int num_blocks, float scale, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, void* workspace, size_t workspace_bytes, int dtype,
+                               void* stream) {
+    int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size, dtype, num_blocks);
+    if (rc) return rc;
+    if (num_seqs < 0 || num_seqs > kMaxGrid || num_tokens < 0 || max_q_len < 0 || max_seq_len < 0 ||
+        max_blocks_per_seq <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || num_tokens == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_q_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+    return prefill_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens, num_seqs,
+                        num_tokens, max_q_len, max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim,
+                        workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream), false, 1.f, 1.f);
+}
+
+int pa_paged_attention_prefill_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+                                   const int32_t* cu_q_lens, int num_seqs, int num_tokens, int max_q_len,
+                                   int max_seq_len, int num_blocks, float scale, float k_scale, float v_scale,
+                                   int num_q_heads, int num_kv_heads, int head_dim, int block_size, void* workspace,
+                                   size_t workspace_bytes, int dtype, void* stream) {
+    int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size, dtype, num_blocks);
+    if (rc) return rc;
+    if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || num_seqs > kMaxGrid || num_tokens < 0 || max_q_len < 0 || max_seq_len < 0 ||
+        max_blocks_per_seq <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale)) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || num_tokens == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_q_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+    return prefill_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, cu_q_lens, num_seqs,
+                        num_tokens, max_q_len, max_seq_len, num_blocks, scale, num_q_heads, num_kv_heads, head_dim,
+                        workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream), true, k_scale,
+                        v_scale);
 }
 
 int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs, int num_blocks,

@@ -1217,15 +1217,23 @@ cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// FP8 cache: one query per row and one q head per kv head on the FMA path;
+// several (query, head) columns per kv head (GQA, or the queries of a
+// speculative-verify row) on the tensor cores, with a second column tile
+// once a row has more than 8 columns.
+template <typename T>
+cudaError_t launch_decode_fp8_t(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                cudaStream_t s) {
+    if (p.max_q * p.group > 8) return launch_decode_t<T, 128, true, true, 2>(p, kmap, vmap, s);
+    if (p.group > 1 || p.max_q > 1) return launch_decode_t<T, 128, true, true, 1>(p, kmap, vmap, s);
+    return launch_decode_t<T, 128, false, true, 1>(p, kmap, vmap, s);
+}
+
 cudaError_t launch_decode_fp8(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                               int dtype, cudaStream_t s) {
     if (p.num_seqs == 0) return cudaSuccess;
-    const bool mma = p.group > 1;
-    if (dtype == 0)
-        return mma ? launch_decode_t<__half, 128, true, true>(p, kmap, vmap, s)
-                   : launch_decode_t<__half, 128, false, true>(p, kmap, vmap, s);
-    return mma ? launch_decode_t<__nv_bfloat16, 128, true, true>(p, kmap, vmap, s)
-               : launch_decode_t<__nv_bfloat16, 128, false, true>(p, kmap, vmap, s);
+    return dtype == 0 ? launch_decode_fp8_t<__half>(p, kmap, vmap, s)
+                      : launch_decode_fp8_t<__nv_bfloat16>(p, kmap, vmap, s);
 }
 
 template <typename T, int D>

@@ -93,7 +93,8 @@ struct PrefillParams {
     int num_kv_heads;
     int group;
     int q_per_tile;               // queries per tile: rows = q_per_tile * group <= 128
-    float scale_log2;
+    float scale_log2;             // scale * log2(e) (times the K dequantisation scale for FP8)
+    float v_scale;                // V dequantisation scale (1 for 16-bit caches)
     // when *decode_units > 0 (decode rows will run next to this kernel), only
     // the first overlap_ctas CTAs take prefill work; the others leave their SMs
     const int32_t* decode_units;
@@ -131,8 +132,9 @@ cudaError_t launch_kv_gather(void* k_out, void* v_out, const void* k_cache, cons
 cudaError_t launch_wait_selftest(unsigned int* err, cudaStream_t s);
 // tcgen05 prefill: groups of 1 to PA_MAX_GROUP q heads per kv head; q_per_tile = 128 / group.
 // `plan` is device scratch of num_seqs + 1 int32 (the work list of query-tile pairs).
+// fp8: K and V maps over head-major E4M3 pools (make_kv_map_fp8), head_dim 128.
 cudaError_t launch_prefill_tc(const PrefillParams& p, int32_t* plan, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, const CUtensorMap& qmap, int head_dim, int dtype,
-                              int max_q_len, int num_tokens, cudaStream_t s);
+                              int max_q_len, int num_tokens, bool fp8, cudaStream_t s);
 
 }  // namespace pa

@@ -146,6 +146,45 @@ __device__ __forceinline__ int pair_key_tiles(int n, int ql, int qt, int pr) {
     return (n - ql + q_last + kTcKeys) / kTcKeys;
 }
 
+// In-place widening of one 16-token block of E4M3 codes to 16-bit rows of
+// type T (exact: every E4M3 value is an fp16 and a bf16 value).  `codes`
+// holds the block's 16 rows of 128 codes (128-byte swizzled), and is also
+// where the rows' second 64-dim half goes; `half0` is where the first half
+// goes.  Row r's second half overwrites row r's codes, so the eight lanes of
+// a row read all of its codes before any of them writes (each step below
+// covers rows 4k .. 4k + 3 and no other).
+template <typename T>
+__device__ __forceinline__ void widen_fp8_block(uint8_t* codes, uint8_t* half0, int lane) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int ci = lane + 32 * k;   // 128 chunks of 16 codes: row ci / 8, chunk ci % 8
+        const int r = ci >> 3, c = ci & 7;
+        const uint4 in = *reinterpret_cast<const uint4*>(codes + r * 128 + ((c ^ (r & 7)) << 4));
+        __syncwarp();
+        const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t h01 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] & 0xffffu));
+            const uint32_t h23 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] >> 16));
+            if constexpr (std::is_same<T, __half>::value) {
+                o[2 * j] = h01;
+                o[2 * j + 1] = h23;
+            } else {
+                const float2 a = Elem<__half>::to_float2(h01);
+                const float2 b = Elem<__half>::to_float2(h23);
+                o[2 * j] = Elem<T>::pack(a.x, a.y);
+                o[2 * j + 1] = Elem<T>::pack(b.x, b.y);
+            }
+        }
+        // dims 16c .. 16c + 15: 16-byte chunks 2 (c % 4) and 2 (c % 4) + 1 of half c / 4
+        uint8_t* row = (c < 4 ? half0 : codes) + r * 128;
+        const int oc = 2 * (c & 3);
+        *reinterpret_cast<uint4*>(row + ((oc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(row + (((oc + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
 // Exclusive prefix sum of one value per thread over a 1024-thread block, plus
 // the running total `carry` of earlier calls (updated).  Every thread calls.
 __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* warp_tot, int* carry) {
@@ -270,7 +309,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
 // k * C + i for even k and k * C + C - 1 - i for odd k, so the CTAs' total
 // costs stay even.  (Beside decode rows: pair w / num_kv_heads of the plan's
 // own order, round-robin.)
-template <typename T, int D>
+template <typename T, int D, bool kFp8>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const int32_t* __restrict__ plan,
                       const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -285,6 +324,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t k_full[NK];               // K tile landed (one arrival per loader)
     __shared__ uint64_t v_full[NV];               // V tile landed (one arrival per loader)
+    // E4M3 cache: K / V tile widened to 16-bit in place (one arrival per
+    // loader); the MMAs and the V-row clearing wait for these instead
+    __shared__ uint64_t k_conv[NK];
+    __shared__ uint64_t v_conv[NV];
     __shared__ uint64_t k_free[NK];               // every S of the stage's tile complete
     __shared__ uint64_t v_free[NV];               // every P V of the stage's tile complete
     __shared__ uint64_t q_full;                   // the item's query tiles landed
@@ -353,10 +396,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < NK; ++s) {
             mbar_init(&k_full[s], kTcLoaders);
+            mbar_init(&k_conv[s], kTcLoaders);
             mbar_init(&k_free[s], 1);
         }
         for (int s = 0; s < NV; ++s) {
             mbar_init(&v_full[s], kTcLoaders);
+            mbar_init(&v_conv[s], kTcLoaders);
             mbar_init(&v_free[s], 1);
         }
         mbar_init(&q_full, 1);
@@ -375,6 +420,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = tmem_slot;
     volatile int* abort_v = &abort_flag;
+    // a K / V stage holds 16-bit rows the MMAs can read
+    uint64_t* const k_ready = kFp8 ? k_conv : k_full;
+    uint64_t* const v_ready = kFp8 ? v_conv : v_full;
 
     // Work item w: (tile pair, kv head) of the plan; within a sequence the
     // pairs nearest the end (the longest key ranges) come first.  Query
@@ -602,7 +650,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // tile's P V is issued after it)
                     const bool clearer = x == 0 || j >= nk_a;
                     if (clearer && (j == it.nkt - 1 || bad)) {
-                        if (!__all_sync(kFullMask, wait_or_abort(&v_full[J % NV], (J / NV) & 1, abort_v))) {
+                        if (!__all_sync(kFullMask, wait_or_abort(&v_ready[J % NV], (J / NV) & 1, abort_v))) {
                             ok = false;
                             break;
                         }
@@ -628,7 +676,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const bool got = wait_or_abort(&o_done[x][Tl & 1], (Tl >> 1) & 1, abort_v);
                     if (__all_sync(kFullMask, got)) {
                         tc_fence_after_sync();
-                        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                        const float inv = l_run > 0.f ? p.v_scale / l_run : 0.f;
                         const int64_t grow =
                             static_cast<int64_t>(it.row0 + qi_row) * p.num_q_heads + it.g * G + (r % G);
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + grow * D);
@@ -722,7 +770,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // the previous item's MMAs must be complete: its S/P buffers and
             // accumulators are reused
             if (items > 0) ok = wait_all(&item_done, (items - 1) & 1);
-            if (ok) ok = wait_all(&q_full, items & 1) && wait_all(&k_full[kv0 % NK], (kv0 / NK) & 1);
+            if (ok) ok = wait_all(&q_full, items & 1) && wait_all(&k_ready[kv0 % NK], (kv0 / NK) & 1);
             if (ok) {
                 tc_fence_after_sync();
 #pragma unroll
@@ -732,7 +780,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             for (int j = 0; ok && j < it.nkt; ++j) {
                 const int J = kv0 + j;
-                ok = wait_all(&v_full[J % NV], (J / NV) & 1);
+                ok = wait_all(&v_ready[J % NV], (J / NV) & 1);
                 if (!ok) break;
                 bool k_next = false;   // K(j+1) seen landed
                 // per tile: P V(j) once its softmax stored P, then S(j+1) into
@@ -749,7 +797,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mma_pv(x, j);
                     if (j + 1 >= it.nkx[x]) continue;
                     if (!k_next) {
-                        if (!(ok = wait_all(&k_full[(J + 1) % NK], ((J + 1) / NK) & 1))) break;
+                        if (!(ok = wait_all(&k_ready[(J + 1) % NK], ((J + 1) / NK) & 1))) break;
                         k_next = true;
                     }
                     mma_s(x, j + 1);
@@ -772,6 +820,117 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     (void)mbar_wait(&o_done[x][Tl & 1], (Tl >> 1) & 1);
                 }
             }
+        }
+    } else if constexpr (kFp8) {
+        // ========================= loaders (E4M3 cache) =========================
+        // Loader li takes blocks li, li + 3, ... of every K and V tile.  Lane
+        // 0 issues one 2 KB box per (block, kv head) of the head-major E4M3
+        // pool, landing where the block's rows of the second 64-dim half go
+        // (K: [half][key], V: [block][half][16 keys]); once the tile has landed
+        // the whole warp widens its blocks in place to 16-bit rows and arrives
+        // on k_conv / v_conv.  Tile J of a kind is widened right after tile
+        // J + 1's boxes of that kind are issued, so the copies overlap the
+        // widening; only the query tiles wait for the previous item to drain.
+        reg_dealloc<kTcOtherRegs>();
+        const int li = warp - kTcMmaWarp - 1;
+        int k_total = 0, v_total = 0;   // K and V tiles issued so far (lane 0), for the abort path
+        // lane 0: issue this loader's boxes of tile j of item `it`
+        auto issue = [&](const Item& it, int j, bool v) -> bool {
+            const int J = kv0 + j;
+            const int N = v ? NV : NK;
+            const int s = J % N;
+            if (J >= N && !wait_or_abort(v ? &v_free[s] : &k_free[s], ((J - N) / N) & 1, abort_v)) return false;
+            // K(J) is issued before V(J) and both are widened before K(J + NK)
+            // is issued: the K stage's record holds tile J's ids until then
+            const int sk = J % NK;
+            if (!v) {
+                for (int blk = li; blk < kTcBlocks; blk += kTcLoaders) {
+                    int id = -1;
+                    if (j * kTcBlocks + blk < it.nblk_live) {
+                        id = it.bt[j * kTcBlocks + blk];
+                        if (id < 0 || id >= p.num_blocks) {
+                            record_error(p.err, PA_DEVERR_BLOCK_ID_);
+                            id = -1;
+                        }
+                    }
+                    stage_blocks[li][sk][blk] = id;
+                }
+            }
+            uint32_t bytes = 0;
+            for (int blk = li; blk < kTcBlocks; blk += kTcLoaders)
+                if (stage_blocks[li][sk][blk] >= 0) bytes += 2048;
+            uint64_t* bar = v ? &v_full[s] : &k_full[s];
+            mbar_arrive_expect_tx(bar, bytes);
+            for (int blk = li; blk < kTcBlocks; blk += kTcLoaders) {
+                const int id = stage_blocks[li][sk][blk];
+                if (id < 0) continue;
+                uint8_t* dst = v ? vst(s) + blk * 4096 + 2048 : kst(s) + Sh::kKeyHalf + blk * 2048;
+                tma_load_4d(dst, v ? &vmap : &kmap, bar, 0, 0, it.g, id);
+            }
+            if (v) ++v_total; else ++k_total;
+            return true;
+        };
+        // whole warp: widen this loader's blocks of ring tile J
+        auto widen = [&](int J, bool v) -> bool {
+            const int N = v ? NV : NK;
+            const int s = J % N;
+            if (!__all_sync(kFullMask, wait_or_abort(v ? &v_full[s] : &k_full[s], (J / N) & 1, abort_v)))
+                return false;
+            const int sk = J % NK;
+            for (int blk = li; blk < kTcBlocks; blk += kTcLoaders) {
+                // a block not loaded (past the live table, or outside the pool)
+                // is masked (K) or cleared (V) by the softmax
+                if (stage_blocks[li][sk][blk] < 0) continue;
+                if (v)
+                    widen_fp8_block<T>(vst(s) + blk * 4096 + 2048, vst(s) + blk * 4096, lane);
+                else
+                    widen_fp8_block<T>(kst(s) + Sh::kKeyHalf + blk * 2048, kst(s) + blk * 2048, lane);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(v ? &v_conv[s] : &k_conv[s]);
+            return true;
+        };
+        // lane 0: the item's query tiles, once the previous item's MMAs are done
+        auto load_q = [&](const Item& it) -> bool {
+            if (items > 0 && !wait_or_abort(&item_done, (items - 1) & 1, abort_v)) return false;
+            mbar_arrive_expect_tx(&q_full, static_cast<uint32_t>((it.nkx[1] ? 2 : 1) * q_tile_bytes));
+#pragma unroll
+            for (int x = 0; x < kTcTiles; ++x) {
+                if (!it.nkx[x]) continue;
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h)
+                    tma_load_4d(qs(x) + h * Sh::kQHalf, &qmap, &q_full, 0, h, it.g * G, it.row0 + it.q0[x]);
+            }
+            return true;
+        };
+        auto lane0 = [&](bool r) { return __shfl_sync(kFullMask, r ? 1 : 0, 0) != 0; };
+        for (int k = 0; ok; ++k) {
+            const int w0 = item_at(k);
+            if (w0 == kNoMoreItems) break;
+            Item it;
+            if (w0 < 0 || !decode_item(w0, it)) continue;
+            for (int j = 0; ok && j < it.nkt; ++j) {
+                const int J = kv0 + j;
+                // K(J), then widen K(J - 1); V(J), then widen V(J - 1)
+                ok = lane0(lane == 0 ? issue(it, j, false) : true);
+                __syncwarp();
+                if (ok && J > 0) ok = widen(J - 1, false);
+                if (ok) ok = lane0(lane == 0 ? issue(it, j, true) : true);
+                __syncwarp();
+                if (ok && J > 0) ok = widen(J - 1, true);
+                if (ok && j == 0 && li == 0) ok = lane0(lane == 0 ? load_q(it) : true);
+            }
+            if (!ok && lane == 0) *abort_v = 1;
+            next_item(it);
+        }
+        // the last tile issued
+        if (ok && kv0 > 0) ok = widen(kv0 - 1, false) && widen(kv0 - 1, true);
+        if (!ok && lane == 0) *abort_v = 1;
+        if ((!ok || *abort_v) && lane == 0) {
+            // this loader's copies still in flight: each stage's last issued phase
+            for (int t = max(0, k_total - NK); t < k_total; ++t) (void)mbar_wait(&k_full[t % NK], (t / NK) & 1);
+            for (int t = max(0, v_total - NV); t < v_total; ++t) (void)mbar_wait(&v_full[t % NV], (t / NV) & 1);
         }
     } else {
         // ================================ loaders ===============================
@@ -886,11 +1045,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 
-template <typename T, int D>
+template <typename T, int D, bool kFp8>
 cudaError_t launch_t(const PrefillParams& p, int32_t* plan, const CUtensorMap& kmap, const CUtensorMap& vmap,
                      const CUtensorMap& qmap, int max_q_len, int num_tokens, cudaStream_t s) {
     constexpr int smem = TcShape<D>::kSmem;
-    auto kern = prefill_tc_kernel<T, D>;
+    auto kern = prefill_tc_kernel<T, D, kFp8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // the softmax warpgroups' register increase is granted from the pool the
@@ -920,13 +1079,19 @@ cudaError_t launch_t(const PrefillParams& p, int32_t* plan, const CUtensorMap& k
 
 cudaError_t launch_prefill_tc(const PrefillParams& p, int32_t* plan, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, const CUtensorMap& qmap, int head_dim, int dtype,
-                              int max_q_len, int num_tokens, cudaStream_t s) {
+                              int max_q_len, int num_tokens, bool fp8, cudaStream_t s) {
     if (p.num_seqs == 0 || max_q_len <= PA_VERIFY_MAX_Q_) return cudaSuccess;
+    if (fp8) {
+        if (head_dim != 128) return cudaErrorInvalidValue;
+        return dtype == 0 ? launch_t<__half, 128, true>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s)
+                          : launch_t<__nv_bfloat16, 128, true>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s);
+    }
     if (dtype == 0)
-        return head_dim == 128 ? launch_t<__half, 128>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s)
-                               : launch_t<__half, 64>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s);
-    return head_dim == 128 ? launch_t<__nv_bfloat16, 128>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s)
-                           : launch_t<__nv_bfloat16, 64>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s);
+        return head_dim == 128 ? launch_t<__half, 128, false>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s)
+                               : launch_t<__half, 64, false>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s);
+    return head_dim == 128
+               ? launch_t<__nv_bfloat16, 128, false>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s)
+               : launch_t<__nv_bfloat16, 64, false>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s);
 }
 
 }  // namespace pa

@@ -433,6 +433,21 @@ def config_llama7b_decode_fp8(device="cpu", batch=64, lo=512, hi=4096, **kw) -> 
                           device=device, cache_dtype="fp8", **kw)
 
 
+def config_mixed_fp8(device="cpu", **kw) -> Workload:
+    """The continuous-batching step (``mixed``) with an FP8 (E4M3) cache: the
+    same lengths and chunks, pools of E4M3 codes of N(0, 1) values (scale 1/16)."""
+    w = config_mixed(device=device, cache_dtype="fp8", **kw)
+    w.name = "mixed_fp8"
+    return w
+
+
+def config_prefill_fp8(device="cpu", **kw) -> Workload:
+    """Chunked prefill on its own (``prefill``) over an FP8 (E4M3) cache."""
+    w = config_prefill(device=device, cache_dtype="fp8", **kw)
+    w.name = "prefill_fp8"
+    return w
+
+
 def config_spec_verify(device="cpu", batch=64, drafts=3, lo=512, hi=4096, **kw) -> Workload:
     """Speculative-decoding verify step: each sequence appends its last
     accepted token and `drafts` draft tokens (q_len = drafts + 1) onto a cached
@@ -456,6 +471,8 @@ CONFIGS = {
     "llama7b_decode_fp8": config_llama7b_decode_fp8,
     "spec_verify": config_spec_verify,
     "prefill": config_prefill,
+    "mixed_fp8": config_mixed_fp8,
+    "prefill_fp8": config_prefill_fp8,
 }
 
 
