@@ -45,11 +45,10 @@ constexpr unsigned kFull = 0xffffffffu;
 // it by this much (log2 units), so softmax weights stay within [0, 2^8].
 constexpr float kLazyRescaleLog2 = 8.f;
 
-// Per-warp shared memory: a ring of kStages (K tile, V tile) slots, plus, for
-// the FP8 GQA path, one K and one V tile converted to 16-bit for the MMA.
-// A warp handles one block at a time, so it moves bytes at (tile bytes) /
-// (block latency); FP8 tiles are half the bytes, so the FP8 MHA kernel keeps
-// small rings and runs more CTAs (warps) per SM instead.
+// Per-warp shared memory: a ring of kStages (K tile, V tile) slots.  A warp
+// handles one block at a time, so it moves bytes at (tile bytes) / (block
+// latency); FP8 tiles are half the bytes, so the FP8 MHA kernel keeps small
+// rings and runs more CTAs (warps) per SM instead.
 template <int D, bool kFp8, bool kMma, int kMaxNT = 1>
 struct DecodeShape {
     static constexpr int kTileBytes = 16 * D * (kFp8 ? 1 : 2);  // one (block, kv head) tile
@@ -61,8 +60,7 @@ struct DecodeShape {
     // kernel keeps 5 CTAs (20 warps) per SM: registers capped at 96.
     static constexpr int kStages = kFp8 ? (kMma ? 4 : 2) : (kMma ? (kMaxNT > 1 ? 3 : 2) : 3);
     static constexpr int kMinCtasPerSm = (kMma && !kFp8) ? (kMaxNT > 1 ? 2 : 3) : (kFp8 && !kMma ? 5 : 1);
-    static constexpr int kConvBytes = (kFp8 && kMma) ? 2 * 16 * D * 2 : 0;
-    static constexpr int kWarpBytes = kStages * kStageBytes + kConvBytes;
+    static constexpr int kWarpBytes = kStages * kStageBytes;
     static constexpr int kSmemBytes = kDecodeWarps * kWarpBytes + 1024;  // + alignment slack
 };
 
@@ -86,37 +84,6 @@ __device__ __forceinline__ void issue_tile(const WarpRing& ring, int slot, int p
         // one box per tile: both 64-dim halves of the 16 rows (block tensor map)
         tma_load_4d(dst, kmap, &ring.bars[slot], 0, phys * 16, 0, kv_head);
         tma_load_4d(dst + Shape::kTileBytes, vmap, &ring.bars[slot], 0, phys * 16, 0, kv_head);
-    }
-}
-
-// FP8 tile (16 rows x 128 codes) -> 16-bit tile in the swizzled layout the
-// MMA step reads (exact: every E4M3 value is an fp16 and a bf16 value).
-template <typename T>
-__device__ __forceinline__ void convert_fp8_tile(const uint8_t* src, uint8_t* dst, int lane) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int ci = lane + 32 * k;  // 128 chunks of 16 codes
-        const int row = ci >> 3;
-        const int c = ci & 7;
-        const uint4 raw = *reinterpret_cast<const uint4*>(src + fp8_off(row, c * 16));
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t o[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t h01 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] & 0xffffu));
-            const uint32_t h23 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] >> 16));
-            if constexpr (std::is_same<T, __half>::value) {
-                o[2 * j] = h01;
-                o[2 * j + 1] = h23;
-            } else {
-                const float2 a = Elem<__half>::to_float2(h01);
-                const float2 b = Elem<__half>::to_float2(h23);
-                o[2 * j] = Elem<T>::pack(a.x, a.y);
-                o[2 * j + 1] = Elem<T>::pack(b.x, b.y);
-            }
-        }
-        *reinterpret_cast<uint4*>(dst + tile_off<128>(row, c * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(dst + tile_off<128>(row, c * 16 + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
     }
 }
 
@@ -306,6 +273,18 @@ struct AluState {
     }
 };
 
+// Two E4M3 codes (low byte first) as a 16-bit pair of type T (exact).
+template <typename T>
+__device__ __forceinline__ uint32_t codes_to(uint16_t codes) {
+    const uint32_t h = e4m3x2_to_f16x2(codes);
+    if constexpr (std::is_same<T, __half>::value) {
+        return h;
+    } else {
+        const float2 f = Elem<__half>::to_float2(h);
+        return Elem<T>::pack(f.x, f.y);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Query-group x K-block step on the tensor cores (mma.sync m16n8k16, fp32
 // accumulate).  The columns are (query, head) pairs that share one kv head:
@@ -317,7 +296,17 @@ struct AluState {
 // j sees the tokens below lim[nt][e]: its query's causal limit, capped at the
 // partition end.
 // ---------------------------------------------------------------------------
-template <typename T, int D, int NT>
+// FP8 (E4M3) tiles (kFp8, head_dim 128) are read without a 16-bit copy:
+// ldmatrix treats two codes as one 16-bit element.  For S^T, lane (g, c) then
+// holds codes 4c .. 4c+3 of a 16-dim chunk of tokens g and g+8; within each
+// k-step the dims are taken in the order 4c, 4c+1 | 4c+2, 4c+3 for the
+// logical columns 2c, 2c+1 | 2c+8, 2c+9, and Q^T is loaded in the same order
+// (a dot product does not depend on the order of its terms).  For O^T the
+// transposing ldmatrix gives lane (g, c) dims 2g, 2g+1 of tokens 2c, 2c+1 of a
+// chunk; one byte permute pairs the tokens of each dim, so the m-tile's rows
+// g and g+8 are dims 2g and 2g+1 of the chunk (undone when O^T is written).
+// P and the converted V are fp16 (every E4M3 value is an fp16 value; P <= 2^8).
+template <typename T, int D, int NT, bool kFp8 = false>
 struct MmaState {
     static constexpr int KS = D / 16;
     uint32_t qb[KS][NT][2];   // Q^T as the B operand, per 16-dim k-step and column tile
@@ -347,14 +336,40 @@ struct MmaState {
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) c2[nt][e] = 0.f;
+            if constexpr (kFp8) {
+                // lane l addresses row l % 8 of matrix l / 8: tokens 0-7 / 8-15
+                // of chunks 2kp and 2kp + 1
+                const int ft = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                uint32_t a[4];
-                ldsm_x4(ka + tile_off<D>(tok, kk * 16 + dsub), a[0], a[1], a[2], a[3]);
+                for (int kp = 0; kp < KS / 2; ++kp) {
+                    const int chunk = 2 * kp + (lane >> 4);
+                    uint32_t x[4];
+                    ldsm_x4(ka + ft * 128 + ((chunk ^ (ft & 7)) << 4), x[0], x[1], x[2], x[3]);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    if (kk & 1) Mma<T>::run(c2[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
-                    else Mma<T>::run(c[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
+                    for (int h = 0; h < 2; ++h) {
+                        const int kk = 2 * kp + h;
+                        uint32_t a[4];
+                        a[0] = codes_to<T>(static_cast<uint16_t>(x[2 * h] & 0xffffu));
+                        a[1] = codes_to<T>(static_cast<uint16_t>(x[2 * h + 1] & 0xffffu));
+                        a[2] = codes_to<T>(static_cast<uint16_t>(x[2 * h] >> 16));
+                        a[3] = codes_to<T>(static_cast<uint16_t>(x[2 * h + 1] >> 16));
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            if (kk & 1) Mma<T>::run(c2[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
+                            else Mma<T>::run(c[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    uint32_t a[4];
+                    ldsm_x4(ka + tile_off<D>(tok, kk * 16 + dsub), a[0], a[1], a[2], a[3]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (kk & 1) Mma<T>::run(c2[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
+                        else Mma<T>::run(c[nt], a, qb[kk][nt][0], qb[kk][nt][1]);
+                    }
                 }
             }
 #pragma unroll
@@ -417,8 +432,9 @@ struct MmaState {
             l[nt][0] += p0 + p2;
             l[nt][1] += p1 + p3;
             // P^T as the B operand: lane l needs P[token 2*(l%4)+e (+8)][column l/4].
-            const uint32_t lo = Elem<T>::pack(p0, p1);
-            const uint32_t hi = Elem<T>::pack(p2, p3);
+            using PT = typename std::conditional<kFp8, __half, T>::type;
+            const uint32_t lo = Elem<PT>::pack(p0, p1);
+            const uint32_t hi = Elem<PT>::pack(p2, p3);
             const int src0 = ((lane & 3) << 3) + (lane >> 3);
             const uint32_t x0 = __shfl_sync(kFull, lo, src0);
             const uint32_t x1 = __shfl_sync(kFull, lo, src0 + 4);
@@ -433,15 +449,41 @@ struct MmaState {
             // there, but 0 * NaN would poison the product, so clear them.
             // (Rows before the end that a column may not see are cache data
             // of the sequence: finite.)
-            const int nchunks = (16 - nvalid) * 8;   // 16-byte chunks per half
-#pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
-                uint4* z = reinterpret_cast<uint4*>(vt + h * TileGeom<D>::kHalfBytes + nvalid * 128);
+            const int nchunks = (16 - nvalid) * 8;   // 16-byte chunks per half (per FP8 tile)
+            if constexpr (kFp8) {
+                uint4* z = reinterpret_cast<uint4*>(vt + nvalid * 128);
                 for (int i = lane; i < nchunks; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+            } else {
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h) {
+                    uint4* z = reinterpret_cast<uint4*>(vt + h * TileGeom<D>::kHalfBytes + nvalid * 128);
+                    for (int i = lane; i < nchunks; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+                }
             }
             __syncwarp();
         }
-        {
+        if constexpr (kFp8) {
+            const int ft = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int mp = 0; mp < KS / 2; ++mp) {
+                const int chunk = 2 * mp + (lane >> 4);
+                uint32_t x[4];
+                ldsm_x4_t(va + ft * 128 + ((chunk ^ (ft & 7)) << 4), x[0], x[1], x[2], x[3]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    // [dim 2g: tokens 2c, 2c+1 | dim 2g+1: tokens 2c, 2c+1] of tokens 0-7 and 8-15
+                    const uint32_t y0 = __byte_perm(x[2 * h], 0u, 0x3120u);
+                    const uint32_t y1 = __byte_perm(x[2 * h + 1], 0u, 0x3120u);
+                    uint32_t a[4];
+                    a[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(y0 & 0xffffu));
+                    a[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(y0 >> 16));
+                    a[2] = e4m3x2_to_f16x2(static_cast<uint16_t>(y1 & 0xffffu));
+                    a[3] = e4m3x2_to_f16x2(static_cast<uint16_t>(y1 >> 16));
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) Mma<__half>::run(o[2 * mp + h][nt], a, b0[nt], b1[nt]);
+                }
+            }
+        } else {
             const int tok = (lane & 7) + ((lane >> 4) & 1) * 8;
             const int dsub = ((lane >> 3) & 1) * 8;
 #pragma unroll
@@ -703,9 +745,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
                 qbase + (static_cast<int64_t>(it.qrow0 + qi) * p.num_q_heads + it.g * G + h) * D;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const int d = kk * 16 + 2 * (lane & 3);
+                // logical k rows 2c, 2c+1 | 2c+8, 2c+9: dims 2c, 2c+1 | 2c+8, 2c+9
+                // (16-bit tiles) or 4c, 4c+1 | 4c+2, 4c+3 (FP8 tiles) of the k-step
+                const int d = kk * 16 + (kFp8 ? 4 : 2) * (lane & 3);
+                const int d2 = d + (kFp8 ? 2 : 8);
                 dst[(kk * nt_count + nt) * 2] = ok ? *reinterpret_cast<const uint32_t*>(qq + d) : 0u;
-                dst[(kk * nt_count + nt) * 2 + 1] = ok ? *reinterpret_cast<const uint32_t*>(qq + d + 8) : 0u;
+                dst[(kk * nt_count + nt) * 2 + 1] = ok ? *reinterpret_cast<const uint32_t*>(qq + d2) : 0u;
             }
         }
     };
@@ -864,7 +909,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
     // (query, head) columns of a decode or verify row: tensor-core path
     auto run_mma = [&](auto nt_tag, const Item& it, int w) -> bool {
         constexpr int NT = decltype(nt_tag)::value;
-        MmaState<T, D, NT> mma;
+        MmaState<T, D, NT, kFp8> mma;
         if (kPrefetchQ && NT == 1 && qpre_item == w) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -890,17 +935,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
         }
         const bool ok = for_each_block(it, [&](uint8_t* kt, uint8_t* vt, int base, int nvalid) {
             const bool masked = base + 16 > it.lim_min;
-            if constexpr (kFp8) {
-                uint8_t* ck = ring.base + kDecodeStages * Shape::kStageBytes;
-                uint8_t* cv = ck + 16 * D * 2;
-                convert_fp8_tile<T>(kt, ck, lane);
-                convert_fp8_tile<T>(vt, cv, lane);
-                __syncwarp();
-                mma.step(ck, cv, base, nvalid, masked, lane, p.scale_log2);
-                __syncwarp();  // the next block's conversion overwrites ck / cv
-            } else {
-                mma.step(kt, vt, base, nvalid, masked, lane, p.scale_log2);
-            }
+            mma.step(kt, vt, base, nvalid, masked, lane, p.scale_log2);
         });
         if (!ok) return false;
         const bool split = it.n > P;
@@ -924,8 +959,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
                                   (static_cast<int64_t>(it.qrow0 + qi) * p.num_q_heads + hq) * D;
 #pragma unroll
                     for (int mt = 0; mt < D / 16; ++mt) {
-                        o[mt * 16 + dr] = Elem<T>::from_float(mma.o[mt][nt][e] * inv);
-                        o[mt * 16 + dr + 8] = Elem<T>::from_float(mma.o[mt][nt][2 + e] * inv);
+                        if constexpr (kFp8) {   // rows dr, dr + 8 of the m-tile are dims 2 dr, 2 dr + 1
+                            *reinterpret_cast<uint32_t*>(o + mt * 16 + 2 * dr) =
+                                Elem<T>::pack(mma.o[mt][nt][e] * inv, mma.o[mt][nt][2 + e] * inv);
+                        } else {
+                            o[mt * 16 + dr] = Elem<T>::from_float(mma.o[mt][nt][e] * inv);
+                            o[mt * 16 + dr + 8] = Elem<T>::from_float(mma.o[mt][nt][2 + e] * inv);
+                        }
                     }
                 } else {
                     const int64_t pi =
@@ -937,8 +977,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, DecodeShape<D, kFp8, kMma, 
                     float* a = p.ws_acc + pi * D;
 #pragma unroll
                     for (int mt = 0; mt < D / 16; ++mt) {
-                        a[mt * 16 + dr] = mma.o[mt][nt][e] * p.v_scale;
-                        a[mt * 16 + dr + 8] = mma.o[mt][nt][2 + e] * p.v_scale;
+                        if constexpr (kFp8) {
+                            *reinterpret_cast<float2*>(a + mt * 16 + 2 * dr) =
+                                make_float2(mma.o[mt][nt][e] * p.v_scale, mma.o[mt][nt][2 + e] * p.v_scale);
+                        } else {
+                            a[mt * 16 + dr] = mma.o[mt][nt][e] * p.v_scale;
+                            a[mt * 16 + dr + 8] = mma.o[mt][nt][2 + e] * p.v_scale;
+                        }
                     }
                 }
             }
