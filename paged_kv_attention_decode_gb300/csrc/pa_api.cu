@@ -132,6 +132,10 @@ constexpr int kMaxGrid = 65535;
 #endif
 constexpr int kOverlapPrefillNum = PA_OVERLAP_NUM;
 constexpr int kOverlapPrefillDen = PA_OVERLAP_DEN;
+// Over an FP8 cache the chunks cost more (their tiles are widened in shared
+// memory) and the decode rows less (half the bytes): the prefill keeps half.
+constexpr int kOverlapPrefillNumFp8 = 1;
+constexpr int kOverlapPrefillDenFp8 = 2;
 constexpr int kMaxPoolBlocks = (1 << 27) - 1;  // token-row coordinate stays below 2^31
 
 int check_shape(int num_q_heads, int num_kv_heads, int head_dim, int block_size, int dtype, int num_blocks) {
@@ -492,7 +496,8 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
     if (!make_q_map(&qmap, q, num_tokens, num_q_heads, head_dim, group, p.q_per_tile, dtype)) return PA_ERR_CUDA;
     if (pa::launch_decode_plan(dc.p, s) != cudaSuccess) return PA_ERR_CUDA;
     p.decode_units = dc.p.unit_count;
-    p.overlap_ctas = std::max(1, pa::sm_count() * kOverlapPrefillNum / kOverlapPrefillDen);
+    p.overlap_ctas = std::max(1, fp8 ? pa::sm_count() * kOverlapPrefillNumFp8 / kOverlapPrefillDenFp8
+                                     : pa::sm_count() * kOverlapPrefillNum / kOverlapPrefillDen);
     if (pa::launch_prefill_tc(p, plan, kmap, vmap, qmap, head_dim, dtype, max_q_len, num_tokens, fp8, s) !=
         cudaSuccess)
         return PA_ERR_CUDA;
