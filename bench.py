@@ -255,9 +255,9 @@ def cpu_baseline(w, seconds: float = 10.0) -> dict:
 def _workload_kw(args) -> dict:
     if not args.batch:
         return {}
-    if args.workload == "mixed":
+    if args.workload in ("mixed", "mixed_fp8"):
         return {"n_decode": args.batch}
-    if args.workload == "prefill":
+    if args.workload in ("prefill", "prefill_fp8"):
         return {"n_prefill": args.batch}
     return {"batch": args.batch}
 
