@@ -340,12 +340,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // only after S_X(j+1), which the MMA warp issues after it saw this phase
     // complete, so no warp arrives twice in one phase.
     __shared__ uint64_t p_full[kTcTiles];
-    // P_X(j) V(j) complete, by tile parity.  A parity wait is only sound when
-    // the barrier's previous phase is known complete: waiting for P V(T)
-    // needs P V(T-2) done.  The waits (the softmax epilogue after its last
-    // tile T, the abort path) come after S(T) completed, and S(T) was issued
-    // after P V(T-1): a completed commit means every earlier MMA completed
-    // (tcgen05.commit tracks all of them), so both earlier P V are done.
+    // o_done[X][0]: the last P_X V of an item complete, one phase per item
+    // that has a tile X (its epilogue is the only waiter; an item's next phase
+    // needs this item's softmax, which comes after the epilogue, so the
+    // barrier never runs two phases ahead).  o_done[0][1]: drains every MMA in
+    // flight on the abort path.
     __shared__ uint64_t o_done[kTcTiles][2];
     __shared__ int32_t stage_blocks[kTcLoaders][NK][kTcBlocks];   // each loader's block ids per K stage
     __shared__ uint32_t tmem_slot;
@@ -504,6 +503,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t s_tm = tmem + lane_base + static_cast<uint32_t>(x * kTcKeys);
         const uint32_t o_tm = tmem + lane_base + static_cast<uint32_t>(kTcTiles * kTcKeys + x * D);
         const bool fold = p.scale_log2 > 0.f;   // scale folded into the exponent's FMA
+        int n_items_x = 0;   // items of this tile so far (o_done phases)
         for (int k = 0; ok; ++k) {
             const int w0 = item_at(k);
             if (w0 == kNoMoreItems) break;
@@ -672,8 +672,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (lane == 0) mbar_arrive(&p_full[x]);
                 }
                 if (ok) {
-                    const int Tl = tx0 + nk - 1;
-                    const bool got = wait_or_abort(&o_done[x][Tl & 1], (Tl >> 1) & 1, abort_v);
+                    const bool got = wait_or_abort(&o_done[x][0], n_items_x & 1, abort_v);
                     if (__all_sync(kFullMask, got)) {
                         tc_fence_after_sync();
                         const float inv = l_run > 0.f ? p.v_scale / l_run : 0.f;
@@ -706,6 +705,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ok = false;
                     }
                 }
+                ++n_items_x;
             }
             if (!ok) *abort_v = 1;
             next_item(it);
@@ -755,7 +755,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tc_mma_f16_ta(o_tm, p_tm + static_cast<uint32_t>(kp * 8), bd, kIdescPV,
                                       (j > 0 || kp > 0) ? 1u : 0u);
                     }
-                    tc_commit(&o_done[x][Tx & 1]);
+                    if (j + 1 == it.nkx[x]) tc_commit(&o_done[x][0]);   // the item's last P V of tile x
                 }
                 __syncwarp();
                 ++pv_issued[x];
@@ -812,13 +812,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if ((!ok || *abort_v) && lane == 0) {
             // let MMAs still in flight finish before the CTA's memory is reused
+            tc_commit(&o_done[0][1]);
+            (void)mbar_wait(&o_done[0][1], 0);
 #pragma unroll
             for (int x = 0; x < kTcTiles; ++x) {
                 if (s_issued[x]) (void)mbar_wait(&s_full[x], (s_issued[x] - 1) & 1);
-                if (pv_issued[x]) {
-                    const int Tl = pv_issued[x] - 1;
-                    (void)mbar_wait(&o_done[x][Tl & 1], (Tl >> 1) & 1);
-                }
+                (void)pv_issued[x];
             }
         }
     } else if constexpr (kFp8) {
