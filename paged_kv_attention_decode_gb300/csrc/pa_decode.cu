@@ -57,9 +57,11 @@ struct DecodeShape {
     // warp: the single-tile one (group heads of decode rows) runs best with
     // 2-stage rings and 3 CTAs (12 warps) per SM; the two-tile one (verify
     // rows, 16 columns) with 3-stage rings and 2 CTAs per SM.  The FP8 MHA
-    // kernel keeps 5 CTAs (20 warps) per SM: registers capped at 96.
+    // kernel keeps 5 CTAs (20 warps) per SM: registers capped at 96.  The FP8
+    // tensor-core kernels keep 3 (registers capped at 168; the two-tile one,
+    // which also serves the decode rows of a varlen call, would take 207).
     static constexpr int kStages = kFp8 ? (kMma ? 4 : 2) : (kMma ? (kMaxNT > 1 ? 3 : 2) : 3);
-    static constexpr int kMinCtasPerSm = (kMma && !kFp8) ? (kMaxNT > 1 ? 2 : 3) : (kFp8 && !kMma ? 5 : 1);
+    static constexpr int kMinCtasPerSm = (kMma && !kFp8) ? (kMaxNT > 1 ? 2 : 3) : (kFp8 && !kMma ? 5 : 3);
     static constexpr int kWarpBytes = kStages * kStageBytes;
     static constexpr int kSmemBytes = kDecodeWarps * kWarpBytes + 1024;  // + alignment slack
 };

@@ -15,6 +15,9 @@ previous call's contents, and a call's work list must not be rewritten by the
 next call while it still runs.  This file is collected last on purpose.
 """
 import ctypes
+import os
+import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -29,6 +32,7 @@ from tests._gpu_util import TOL, bits, max_err, snapshot
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 SCRATCH = 32 << 20   # PA_NOALLOC_SCRATCH_BYTES
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _noalloc(lib, out, w, bt, sl, max_len, partition=0, num_seqs=None):
@@ -115,3 +119,37 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     assert _noalloc(lib, out, w, bt, sl, 16 * 1024, partition=16) == 3   # PA_ERR_WORKSPACE_TOO_SMALL
     torch.cuda.synchronize()
     assert torch.count_nonzero(out) == 0
+
+
+_LAZY_PROBE = r"""
+import ctypes
+import torch
+from paged_kv_attention_decode_gb300 import _binding
+lib = _binding.load_library()
+torch.zeros(1, device="cuda")
+torch.cuda.synchronize()
+def call():
+    return lib.pa_paged_attention_decode_noalloc(None, None, None, None, None, 1, None, 0, 16, 1,
+                                                 ctypes.c_float(0.1), 8, 8, 128, 16, 0, 0, None)
+f0 = torch.cuda.mem_get_info()[0]
+rc1 = call()
+f1 = torch.cuda.mem_get_info()[0]
+rc2 = call()
+f2 = torch.cuda.mem_get_info()[0]
+print(rc1, rc2, f0 - f1, f1 - f2)
+"""
+
+
+def test_first_call_reserves_the_scratch_under_lazy_module_loading():
+    """With lazy module loading the scratch array is reserved by the first call
+    on a device, not when the library is loaded: a runtime that hands all free
+    memory to its KV pool must make that call (num_seqs = 0 does only the
+    set-up) before.  A fresh process, so that no earlier test loaded it."""
+    env = dict(os.environ, CUDA_MODULE_LOADING="LAZY")
+    r = subprocess.run([sys.executable, "-c", _LAZY_PROBE], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    rc1, rc2, first, second = (int(x) for x in r.stdout.split()[-4:])
+    assert rc1 == 0 and rc2 == 0
+    assert first >= SCRATCH, first          # the first call reserved the array
+    assert abs(second) < (2 << 20), second  # later calls reserve nothing
