@@ -352,8 +352,14 @@ class Run:
         self.slots = torch.empty(self.T, dtype=torch.int64, device=dev)
         self.out = torch.empty_like(w.q)
         self.partition_arg = partition if self.decode else 0
+        # FP8 chunks longer than 8 queries: the 16-bit copy of their blocks
+        # (sized from the workload's host arrays, as a scheduler would)
+        self.chunk_kv = int(w.seq_lens[w.q_lens > 8].astype(np.int64).sum()) if self.fp8 and not self.decode else 0
         if self.decode:
             nbytes = pa.decode_workspace_bytes(w.batch, w.num_q_heads, w.head_dim, w.max_seq_len, partition)
+        elif self.fp8 and w.max_q_len > 8:
+            nbytes = pa.prefill_fp8_workspace_bytes(w.batch, self.T, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                                    w.max_seq_len, w.max_blocks_per_seq, self.chunk_kv)
         else:
             nbytes = pa.prefill_workspace_bytes(w.batch, self.T, w.num_q_heads, w.head_dim, w.max_seq_len)
         self.wsp = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
@@ -363,7 +369,9 @@ class Run:
         # slot mapping + KV write; the decode plan + decode kernels; the
         # log-sum-exp reduce when a sequence can span several partitions; the
         # prefill plan + prefill kernels when a chunk is longer than 8 queries
-        self.launches_per_step = 4 + (1 if parts > 1 else 0) + (2 if not self.decode and w.max_q_len > 8 else 0)
+        # (and, over an FP8 cache, the kernel that widens the chunks' blocks)
+        chunks = not self.decode and w.max_q_len > 8
+        self.launches_per_step = 4 + (1 if parts > 1 else 0) + (2 if chunks else 0) + (1 if chunks and self.fp8 else 0)
 
     def write(self, key=None, value=None, bt=None, sl=None, cu=None):
         pa, w = self.pa, self.w
@@ -388,7 +396,7 @@ class Run:
         elif self.fp8:
             pa.paged_attention_prefill_fp8(q, w.k_cache, w.v_cache, bt, sl, self.cu if cu is None else cu, w.scale,
                                            self.kv_scale, self.kv_scale, w.max_q_len, self.max_len, out=self.out,
-                                           workspace=self.wsp)
+                                           workspace=self.wsp, chunk_kv_tokens=self.chunk_kv)
         elif self.decode:
             pa.paged_attention_decode(q, w.k_cache, w.v_cache, bt, sl, w.scale, self.max_len, out=self.out,
                                       partition_size=self.partition_arg, workspace=self.wsp)

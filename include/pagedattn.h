@@ -86,6 +86,7 @@ typedef enum {
 #define PA_DEVERR_SLOT 2       /* a slot at or past num_blocks * block_size */
 #define PA_DEVERR_SEQ_LEN 4    /* seq_len above max_seq_len or the table's capacity */
 #define PA_DEVERR_TIMEOUT 8    /* a bounded wait for a TMA copy ran out (the work was abandoned) */
+#define PA_DEVERR_WORKSPACE 16 /* an FP8 prefill chunk's 16-bit copy did not fit (its rows were skipped) */
 
 /* Library ABI version (major * 100 + minor). */
 int pa_version(void);
@@ -292,12 +293,31 @@ int pa_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache,
  * the block table and dequantises it; section 4 "推测解码" for the verify
  * rows): as pa_paged_attention_prefill with k_t = code * k_scale and
  * v_t = code * v_scale over the head-major E4M3 pools described above.
- * head_dim must be 128; q and out keep `dtype`; the workspace is sized by
- * pa_prefill_workspace_bytes.  Rows of at most PA_VERIFY_MAX_Q queries read
- * the codes like pa_paged_attention_decode_fp8; longer chunks widen each
- * (block, kv head) tile to 16-bit in shared memory (exact: every E4M3 value is
- * an fp16 and a bf16 value) for the tensor cores.
+ * head_dim must be 128; q and out keep `dtype`.  Rows of at most
+ * PA_VERIFY_MAX_Q queries read the codes like pa_paged_attention_decode_fp8.
+ * For longer chunks a kernel first widens every block of the chunk's
+ * sequence to 16-bit values of `dtype` in the workspace (exact: every E4M3
+ * value is an fp16 and a bf16 value; the scales are applied as above), and
+ * the tensor-core prefill kernel reads that copy like a 16-bit cache.
+ *   workspace  >= pa_prefill_fp8_workspace_bytes(..., chunk_kv_tokens) bytes,
+ *              256-byte aligned (pa_prefill_workspace_bytes suffices when
+ *              max_q_len <= PA_VERIFY_MAX_Q: there is no chunk to copy).
+ *              Chunks take copy blocks in sequence order; from the first
+ *              chunk whose blocks do not fit in the rest of the workspace on,
+ *              every chunk is skipped (its rows are left unwritten) and
+ *              PA_DEVERR_WORKSPACE is set.
  */
+/* Workspace bytes for pa_paged_attention_prefill_fp8: those of
+ * pa_prefill_workspace_bytes, plus the chunks' 16-bit copy (a table of
+ * num_seqs * max_blocks_per_seq block ids, and 2 * 16 * num_kv_heads *
+ * head_dim * 2 bytes per copied block).  chunk_kv_tokens = the sum of
+ * seq_lens[b] over the sequences with more than PA_VERIFY_MAX_Q new tokens
+ * (a chunk copies ceil(seq_len / 16) blocks); any larger value is also fine.
+ * 0 for a non-positive size or a negative argument. */
+size_t pa_prefill_fp8_workspace_bytes(int num_seqs, int num_tokens, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int max_seq_len, int max_blocks_per_seq,
+                                      int64_t chunk_kv_tokens);
+
 int pa_paged_attention_prefill_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
                                    const int32_t* block_tables, int max_blocks_per_seq,
                                    const int32_t* seq_lens, const int32_t* cu_q_lens, int num_seqs,

@@ -8,6 +8,7 @@ fails loudly if the library has not been built.
 from ._binding import (  # noqa: F401
     PagedAttnError,
     copy_blocks,
+    count_chunk_kv_tokens,
     decode_partition,
     decode_workspace_bytes,
     library_path,
@@ -19,6 +20,7 @@ from ._binding import (  # noqa: F401
     paged_kv_gather,
     paged_kv_write,
     paged_kv_write_fp8,
+    prefill_fp8_workspace_bytes,
     prefill_workspace_bytes,
     selftest_wait_timeout,
     slot_mapping,

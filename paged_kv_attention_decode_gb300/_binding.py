@@ -44,6 +44,7 @@ _SIGNATURES = {
     "pa_paged_kv_write_fp8": (_i32, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _p]),
     "pa_paged_attention_decode_fp8": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _f32, _f32, _f32,
                                              _i32, _i32, _i32, _i32, _i32, _p, _sz, _i32, _p]),
+    "pa_prefill_fp8_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int64]),
     "pa_paged_attention_prefill_fp8": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32, _i32,
                                               _f32, _f32, _f32, _i32, _i32, _i32, _i32, _p, _sz, _i32, _p]),
     "pa_copy_blocks": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _p]),
@@ -172,6 +173,22 @@ def prefill_workspace_bytes(num_seqs: int, num_tokens: int, num_q_heads: int, he
                             max_seq_len: int) -> int:
     return int(load_library().pa_prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, head_dim,
                                                          max_seq_len))
+
+
+def prefill_fp8_workspace_bytes(num_seqs: int, num_tokens: int, num_q_heads: int, num_kv_heads: int,
+                                head_dim: int, max_seq_len: int, max_blocks_per_seq: int,
+                                chunk_kv_tokens: int) -> int:
+    return int(load_library().pa_prefill_fp8_workspace_bytes(num_seqs, num_tokens, num_q_heads, num_kv_heads,
+                                                             head_dim, max_seq_len, max_blocks_per_seq,
+                                                             chunk_kv_tokens))
+
+
+def count_chunk_kv_tokens(seq_lens: torch.Tensor, cu_q_lens: torch.Tensor) -> int:
+    """Sum of seq_lens over the rows with more than 8 new tokens (the FP8
+    prefill copy's size argument), from host copies of the two arrays."""
+    sl = seq_lens.detach().to("cpu", torch.int64)
+    cu = cu_q_lens.detach().to("cpu", torch.int64)
+    return int(sl[(cu[1:] - cu[:-1]) > 8].sum())
 
 
 def _workspace(nbytes: int, device, workspace):
@@ -340,10 +357,12 @@ def paged_attention_prefill_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache:
                                 block_tables: torch.Tensor, seq_lens: torch.Tensor, cu_q_lens: torch.Tensor,
                                 scale: float, k_scale: float, v_scale: float, max_q_len: int, max_seq_len: int,
                                 out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                                stream=None) -> torch.Tensor:
+                                stream=None, chunk_kv_tokens: int | None = None) -> torch.Tensor:
     """Causal varlen attention of new query rows over head-major FP8 (E4M3)
     pools [NB, Hkv, 16, 128] (decodes, speculative-verify rows and prefill
-    chunks in one call)."""
+    chunks in one call).  `chunk_kv_tokens` sizes the chunks' 16-bit copy
+    (see `count_chunk_kv_tokens()`); when it is None and a chunk can be longer than
+    8 queries, it is computed from host copies of seq_lens and cu_q_lens."""
     _cuda(q, k_cache, v_cache, block_tables, seq_lens, cu_q_lens, out, workspace)
     _u8(k_cache), _u8(v_cache)
     T, Hq, D = q.shape
@@ -353,7 +372,13 @@ def paged_attention_prefill_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache:
     _need(cu_q_lens.shape[0] == B + 1 and cu_q_lens.dtype == torch.int32, "cu_q_lens")
     if out is None:
         out = torch.empty_like(q)
-    nbytes = prefill_workspace_bytes(B, T, Hq, D, max_seq_len)
+    if max_q_len > 8 and B > 0 and T > 0:
+        if chunk_kv_tokens is None:
+            chunk_kv_tokens = count_chunk_kv_tokens(seq_lens, cu_q_lens)
+        nbytes = prefill_fp8_workspace_bytes(B, T, Hq, Hkv, D, max_seq_len, block_tables.shape[1],
+                                             chunk_kv_tokens)
+    else:
+        nbytes = prefill_workspace_bytes(B, T, Hq, D, max_seq_len)
     workspace = _workspace(nbytes, q.device, workspace)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load_library().pa_paged_attention_prefill_fp8(

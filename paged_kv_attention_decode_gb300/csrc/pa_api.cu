@@ -132,10 +132,16 @@ constexpr int kMaxGrid = 65535;
 #endif
 constexpr int kOverlapPrefillNum = PA_OVERLAP_NUM;
 constexpr int kOverlapPrefillDen = PA_OVERLAP_DEN;
-// Over an FP8 cache the chunks cost more (their tiles are widened in shared
-// memory) and the decode rows less (half the bytes): the prefill keeps half.
-constexpr int kOverlapPrefillNumFp8 = 1;
-constexpr int kOverlapPrefillDenFp8 = 2;
+// Over an FP8 cache the decode rows cost less (half the bytes) while the
+// chunks cost the same (the kernel reads their 16-bit copy).
+#ifndef PA_OVERLAP_NUM_FP8
+#define PA_OVERLAP_NUM_FP8 1
+#endif
+#ifndef PA_OVERLAP_DEN_FP8
+#define PA_OVERLAP_DEN_FP8 4
+#endif
+constexpr int kOverlapPrefillNumFp8 = PA_OVERLAP_NUM_FP8;
+constexpr int kOverlapPrefillDenFp8 = PA_OVERLAP_DEN_FP8;
 constexpr int kMaxPoolBlocks = (1 << 27) - 1;  // token-row coordinate stays below 2^31
 
 int check_shape(int num_q_heads, int num_kv_heads, int head_dim, int block_size, int dtype, int num_blocks) {
@@ -436,6 +442,36 @@ size_t pa_prefill_workspace_bytes(int num_seqs, int num_tokens, int num_q_heads,
                                                   parts_for(max_seq_len, effective_partition(max_seq_len, 0)));
 }
 
+// FP8 varlen calls: after the 16-bit call's workspace, the chunks' 16-bit
+// copy ([256 B header | chunk_seq | chunk_base | table | K copy | V copy],
+// every part 256-byte aligned).  Copy blocks hold 16 rows of num_kv_heads *
+// head_dim 16-bit values, for K and for V.
+static size_t fp8_copy_fixed_bytes(int num_seqs, int max_blocks_per_seq) {
+    return 256 + 2 * align256(static_cast<size_t>(num_seqs) * sizeof(int32_t)) +
+           align256(static_cast<size_t>(num_seqs) * static_cast<size_t>(max_blocks_per_seq) * sizeof(int32_t));
+}
+
+static size_t fp8_copy_block_bytes(int num_kv_heads, int head_dim) {
+    return 2 * static_cast<size_t>(PA_BLOCK_SIZE) * num_kv_heads * head_dim * 2;   // K and V
+}
+
+size_t pa_prefill_fp8_workspace_bytes(int num_seqs, int num_tokens, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int max_seq_len, int max_blocks_per_seq,
+                                      int64_t chunk_kv_tokens) {
+    if (num_seqs <= 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        max_seq_len < 0 || max_blocks_per_seq <= 0 || chunk_kv_tokens < 0)
+        return 0;
+    // each chunk rounds its length up to whole blocks: at most one partial
+    // block per chunk, and at most num_tokens / (PA_VERIFY_MAX_Q + 1) chunks
+    const int64_t chunks = std::min<int64_t>(num_seqs, num_tokens / (PA_VERIFY_MAX_Q + 1));
+    int64_t blocks = (chunk_kv_tokens + PA_BLOCK_SIZE - 1) / PA_BLOCK_SIZE + chunks;
+    blocks = std::min<int64_t>(blocks, static_cast<int64_t>(num_seqs) * max_blocks_per_seq);
+    blocks = std::min<int64_t>(blocks, kMaxPoolBlocks);
+    return pa_prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, head_dim, max_seq_len) +
+           fp8_copy_fixed_bytes(num_seqs, max_blocks_per_seq) +
+           static_cast<size_t>(blocks) * fp8_copy_block_bytes(num_kv_heads, head_dim);
+}
+
 // Everything a varlen call does, for either cache type; arguments are
 // validated by the entry points.
 static int prefill_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -445,10 +481,33 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
                         void* workspace, size_t workspace_bytes, int dtype, cudaStream_t s, bool fp8,
                         float k_scale, float v_scale) {
     const size_t pb = plan_bytes(num_seqs, num_tokens);
-    if (!workspace ||
-        workspace_bytes < pa_prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, head_dim, max_seq_len))
-        return PA_ERR_WORKSPACE_TOO_SMALL;
+    const size_t base_bytes = pa_prefill_workspace_bytes(num_seqs, num_tokens, num_q_heads, head_dim, max_seq_len);
+    if (!workspace || workspace_bytes < base_bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned256(workspace)) return PA_ERR_INVALID_ARG;
+    // FP8 chunks: room for the 16-bit copy of at least one block
+    pa::Fp8Copy copy{};
+    if (fp8 && max_q_len > PA_VERIFY_MAX_Q) {
+        const size_t fixed = fp8_copy_fixed_bytes(num_seqs, max_blocks_per_seq);
+        const size_t per = fp8_copy_block_bytes(num_kv_heads, head_dim);
+        if (workspace_bytes < base_bytes + fixed + per) return PA_ERR_WORKSPACE_TOO_SMALL;
+        const size_t cap = std::min<size_t>((workspace_bytes - base_bytes - fixed) / per, kMaxPoolBlocks);
+        uint8_t* c = static_cast<uint8_t*>(workspace) + base_bytes;
+        copy.hdr = reinterpret_cast<int32_t*>(c);
+        c += 256;
+        copy.chunk_seq = reinterpret_cast<int32_t*>(c);
+        c += align256(static_cast<size_t>(num_seqs) * sizeof(int32_t));
+        copy.chunk_base = reinterpret_cast<int32_t*>(c);
+        c += align256(static_cast<size_t>(num_seqs) * sizeof(int32_t));
+        copy.table = reinterpret_cast<int32_t*>(c);
+        c += align256(static_cast<size_t>(num_seqs) * static_cast<size_t>(max_blocks_per_seq) * sizeof(int32_t));
+        copy.k16 = c;
+        copy.v16 = c + cap * (per / 2);
+        copy.cap_blocks = static_cast<int>(cap);
+        copy.k_codes = k_cache;
+        copy.v_codes = v_cache;
+        copy.src_tables = block_tables;
+        copy.src_num_blocks = num_blocks;
+    }
     int32_t* plan = static_cast<int32_t*>(workspace);
     const int group = num_q_heads / num_kv_heads;
     // decode rows (q_len == 1) and speculative-verify rows (q_len <= PA_VERIFY_MAX_Q)
@@ -465,14 +524,14 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
     pa::PrefillParams p{};
     p.out = out;
     p.q = q;
-    p.block_tables = block_tables;
+    p.block_tables = fp8 ? copy.table : block_tables;
     p.seq_lens = seq_lens;
     p.cu_q_lens = cu_q_lens;
     p.err = err;
     p.num_seqs = num_seqs;
     p.max_blocks = max_blocks_per_seq;
     p.max_seq_len = max_seq_len;
-    p.num_blocks = num_blocks;
+    p.num_blocks = fp8 ? copy.cap_blocks : num_blocks;
     p.num_q_heads = num_q_heads;
     p.num_kv_heads = num_kv_heads;
     p.group = group;
@@ -482,14 +541,14 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
     // tiles of 128 / group queries (every supported grouping) on the tcgen05
     // tensor cores, running beside the decode rows: the decode plan and the
     // prefill kernel go first; the decode kernel then starts on the SMs the
-    // prefill kernel leaves free.  16-bit K comes in one box per 64-dim half
-    // of a block, 16-bit V in one box per block; E4M3 K and V in one box per
-    // (block, kv head) of the head-major pools, widened in shared memory.
-    const bool maps_ok = fp8 ? make_kv_map_fp8(&kmap, k_cache, num_blocks, num_kv_heads) &&
-                                   make_kv_map_fp8(&vmap, v_cache, num_blocks, num_kv_heads)
-                             : make_kv_map(&kmap, k_cache, num_blocks, num_kv_heads, head_dim, dtype) &&
-                                   make_kv_map_block(&vmap, v_cache, num_blocks, num_kv_heads, head_dim, dtype);
-    if (!maps_ok) return PA_ERR_CUDA;
+    // prefill kernel leaves free.  K comes in one box per 64-dim half of a
+    // block, V in one box per block, from the 16-bit cache or (FP8 cache)
+    // from the chunks' 16-bit copy.
+    const void* kc = fp8 ? copy.k16 : k_cache;
+    const void* vc = fp8 ? copy.v16 : v_cache;
+    if (!make_kv_map(&kmap, kc, p.num_blocks, num_kv_heads, head_dim, dtype) ||
+        !make_kv_map_block(&vmap, vc, p.num_blocks, num_kv_heads, head_dim, dtype))
+        return PA_ERR_CUDA;
     p.q_per_tile = 128 / group;
     p.pair_cap = num_tokens / 4 + num_seqs;
     CUtensorMap qmap;
@@ -498,7 +557,8 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
     p.decode_units = dc.p.unit_count;
     p.overlap_ctas = std::max(1, fp8 ? pa::sm_count() * kOverlapPrefillNumFp8 / kOverlapPrefillDenFp8
                                      : pa::sm_count() * kOverlapPrefillNum / kOverlapPrefillDen);
-    if (pa::launch_prefill_tc(p, plan, kmap, vmap, qmap, head_dim, dtype, max_q_len, num_tokens, fp8, s) !=
+    if (pa::launch_prefill_tc(p, plan, kmap, vmap, qmap, head_dim, dtype, max_q_len, num_tokens,
+                              fp8 ? &copy : nullptr, s) !=
         cudaSuccess)
         return PA_ERR_CUDA;
     dc.p.overlap = 1;

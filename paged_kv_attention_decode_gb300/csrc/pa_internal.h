@@ -11,6 +11,7 @@
 #define PA_DEVERR_SLOT_ 2u
 #define PA_DEVERR_SEQ_LEN_ 4u
 #define PA_DEVERR_TIMEOUT_ 8u
+#define PA_DEVERR_WORKSPACE_ 16u
 
 namespace pa {
 
@@ -102,6 +103,25 @@ struct PrefillParams {
     int pair_cap;                 // pair-list capacity of the plan (num_tokens / 4 + num_seqs)
 };
 
+// FP8 (E4M3) cache: the prefill chunks' blocks widened to a 16-bit copy in
+// the workspace, which the tensor-core kernel reads like a 16-bit cache.  The
+// plan lists each chunk whose copy fits (`chunk_seq`, with its first copy
+// block in `chunk_base`); sequence b's block i goes to copy block
+// chunk_base[k] + i, recorded in row b of `table` (-1: not loaded).
+struct Fp8Copy {
+    int32_t* hdr;                 // [0] chunks listed, [1] copy blocks in use
+    int32_t* chunk_seq;           // [num_seqs]
+    int32_t* chunk_base;          // [num_seqs]
+    int32_t* table;               // [num_seqs, max_blocks] copy block ids (rows of listed chunks)
+    void* k16;                    // [cap_blocks, 16, Hkv, D] of the query type
+    void* v16;
+    int cap_blocks;
+    const void* k_codes;          // the caller's E4M3 pools [num_blocks, Hkv, 16, D]
+    const void* v_codes;
+    const int32_t* src_tables;    // the caller's block table [num_seqs, max_blocks]
+    int src_num_blocks;
+};
+
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_slot_mapping(int64_t* slots, const int32_t* block_tables, int max_blocks,
                                 const int32_t* seq_lens, const int32_t* cu_q_lens, int num_seqs,
@@ -131,10 +151,13 @@ cudaError_t launch_kv_gather(void* k_out, void* v_out, const void* k_cache, cons
 // One-thread kernel whose bounded mbarrier wait runs out (records a timeout).
 cudaError_t launch_wait_selftest(unsigned int* err, cudaStream_t s);
 // tcgen05 prefill: groups of 1 to PA_MAX_GROUP q heads per kv head; q_per_tile = 128 / group.
-// `plan` is device scratch of num_seqs + 1 int32 (the work list of query-tile pairs).
-// fp8: K and V maps over head-major E4M3 pools (make_kv_map_fp8), head_dim 128.
+// `plan` is device scratch of num_seqs + 1 + 2 * pair_cap int32 (the work list
+// of query-tile pairs).  With `copy` (FP8 cache, head_dim 128) the plan also
+// lists the chunks' copy blocks, a kernel widens them, and K and V come from
+// the copy: p.block_tables = copy->table, p.num_blocks = copy->cap_blocks,
+// kmap / vmap over copy->k16 / v16.
 cudaError_t launch_prefill_tc(const PrefillParams& p, int32_t* plan, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, const CUtensorMap& qmap, int head_dim, int dtype,
-                              int max_q_len, int num_tokens, bool fp8, cudaStream_t s);
+                              int max_q_len, int num_tokens, const Fp8Copy* copy, cudaStream_t s);
 
 }  // namespace pa

@@ -146,43 +146,29 @@ __device__ __forceinline__ int pair_key_tiles(int n, int ql, int qt, int pr) {
     return (n - ql + q_last + kTcKeys) / kTcKeys;
 }
 
-// In-place widening of one 16-token block of E4M3 codes to 16-bit rows of
-// type T (exact: every E4M3 value is an fp16 and a bf16 value).  `codes`
-// holds the block's 16 rows of 128 codes (128-byte swizzled), and is also
-// where the rows' second 64-dim half goes; `half0` is where the first half
-// goes.  Row r's second half overwrites row r's codes, so the eight lanes of
-// a row read all of its codes before any of them writes (each step below
-// covers rows 4k .. 4k + 3 and no other).
+// One 16-byte run of E4M3 codes (16 elements) widened to 16-bit values of
+// type T: two 16-byte runs (exact: every E4M3 value is an fp16 and a bf16
+// value).
 template <typename T>
-__device__ __forceinline__ void widen_fp8_block(uint8_t* codes, uint8_t* half0, int lane) {
+__device__ __forceinline__ void widen16(const uint4& in, uint4& lo, uint4& hi) {
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t o[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int ci = lane + 32 * k;   // 128 chunks of 16 codes: row ci / 8, chunk ci % 8
-        const int r = ci >> 3, c = ci & 7;
-        const uint4 in = *reinterpret_cast<const uint4*>(codes + r * 128 + ((c ^ (r & 7)) << 4));
-        __syncwarp();
-        const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-        uint32_t o[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t h01 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] & 0xffffu));
-            const uint32_t h23 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] >> 16));
-            if constexpr (std::is_same<T, __half>::value) {
-                o[2 * j] = h01;
-                o[2 * j + 1] = h23;
-            } else {
-                const float2 a = Elem<__half>::to_float2(h01);
-                const float2 b = Elem<__half>::to_float2(h23);
-                o[2 * j] = Elem<T>::pack(a.x, a.y);
-                o[2 * j + 1] = Elem<T>::pack(b.x, b.y);
-            }
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t h01 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] & 0xffffu));
+        const uint32_t h23 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] >> 16));
+        if constexpr (std::is_same<T, __half>::value) {
+            o[2 * j] = h01;
+            o[2 * j + 1] = h23;
+        } else {
+            const float2 a = Elem<__half>::to_float2(h01);
+            const float2 b = Elem<__half>::to_float2(h23);
+            o[2 * j] = Elem<T>::pack(a.x, a.y);
+            o[2 * j + 1] = Elem<T>::pack(b.x, b.y);
         }
-        // dims 16c .. 16c + 15: 16-byte chunks 2 (c % 4) and 2 (c % 4) + 1 of half c / 4
-        uint8_t* row = (c < 4 ? half0 : codes) + r * 128;
-        const int oc = 2 * (c & 3);
-        *reinterpret_cast<uint4*>(row + ((oc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(row + (((oc + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
     }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 // Exclusive prefix sum of one value per thread over a 1024-thread block, plus
@@ -229,19 +215,25 @@ static_assert(kPlanBuckets == 2 * 1024, "the plan's class scan takes two classes
 // arbitrary and does not affect any result).  seq_of_pair[l] = the sequence
 // of global pair l, so that an item finds its sequence with one load.  The
 // pair lists hold at most pair_cap = num_tokens / 4 + num_seqs entries.
+// With an FP8 copy (copy.hdr non-null) each chunk with pairs also gets
+// ceil(seq_len / 16) consecutive copy blocks, in sequence order; a chunk
+// whose blocks would pass copy.cap_blocks (and so every later chunk) gets
+// neither blocks nor pairs (its rows are left unwritten) and sets
+// PA_DEVERR_WORKSPACE.
 // One CTA.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __restrict__ cu_q_lens,
                                                             const int32_t* __restrict__ seq_lens, int num_seqs,
                                                             int num_tokens, int q_per_tile,
                                                             int32_t* __restrict__ offsets, int pair_cap,
-                                                            unsigned int* err) {
+                                                            unsigned int* err, const Fp8Copy copy, int max_seq_len,
+                                                            int max_blocks) {
     __shared__ int warp_tot[32];
-    __shared__ int carry;
+    __shared__ int carry, blk_carry, chunk_carry, blk_end;
     __shared__ int hist[kPlanBuckets];
     int32_t* order = offsets + num_seqs + 1;
     int32_t* seq_of_pair = order + pair_cap;
     const int tid = threadIdx.x;
-    if (tid == 0) carry = 0;
+    if (tid == 0) carry = blk_carry = chunk_carry = blk_end = 0;
     for (int i = tid; i < kPlanBuckets; i += 1024) hist[i] = 0;
     __syncthreads();
     // the pairs of sequence b: count them (offsets) and their cost classes
@@ -269,15 +261,39 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
         if (b < num_seqs) {
             v = pairs_of(b, ql, n);
             if (ql == 0 && cu_q_lens[b + 1] != cu_q_lens[b]) record_error(err, PA_DEVERR_SEQ_LEN_);
-            for (int pr = 0; pr < v; ++pr) atomicAdd(&hist[bucket(n, ql, pr)], 1);
         }
+        if (copy.hdr) {
+            // the copy blocks of a chunk the kernel will read (a malformed
+            // length is skipped there, and needs none)
+            int nb = (v > 0 && n >= ql && n <= max_seq_len && n <= max_blocks * 16) ? (n + 15) >> 4 : 0;
+            const int first = block_exclusive_scan_1024(nb, warp_tot, &blk_carry);
+            if (nb > 0 && first + nb > copy.cap_blocks) {
+                record_error(err, PA_DEVERR_WORKSPACE_);
+                nb = 0;
+                v = 0;
+            }
+            const int k = block_exclusive_scan_1024(nb > 0 ? 1 : 0, warp_tot, &chunk_carry);
+            if (nb > 0) {
+                copy.chunk_seq[k] = b;
+                copy.chunk_base[k] = first;
+                atomicMax(&blk_end, first + nb);
+            }
+        }
+        if (b < num_seqs)
+            for (int pr = 0; pr < v; ++pr) atomicAdd(&hist[bucket(n, ql, pr)], 1);
         const int start = block_exclusive_scan_1024(v, warp_tot, &carry);
         if (b < num_seqs) {
             offsets[b] = start;
             for (int pr = 0; pr < v; ++pr) seq_of_pair[start + pr] = b;
         }
     }
-    if (tid == 0) offsets[num_seqs] = carry;
+    if (tid == 0) {
+        offsets[num_seqs] = carry;
+        if (copy.hdr) {
+            copy.hdr[0] = chunk_carry;
+            copy.hdr[1] = blk_end;
+        }
+    }
     __syncthreads();
     // bucket starts (exclusive scan of the histogram, two classes per thread)
     if (tid == 0) carry = 0;
@@ -290,15 +306,69 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
         hist[2 * tid + 1] = start + h0;
     }
     __syncthreads();
-    // scatter each pair's global index to its class
+    // scatter each pair's global index to its class (the pair counts from
+    // offsets: a chunk without copy blocks has none)
     for (int b = tid; b < num_seqs; b += 1024) {
         int ql = 0, n = 0;
-        const int v = pairs_of(b, ql, n);
+        (void)pairs_of(b, ql, n);
         const int first = offsets[b];
+        const int v = offsets[b + 1] - first;
         for (int pr = 0; pr < v; ++pr) {
             // the kernel's pair index l within the sequence counts from the last pair
             const int l = first + (v - 1 - pr);
             order[atomicAdd(&hist[bucket(n, ql, pr)], 1)] = l;
+        }
+    }
+}
+
+// FP8 (E4M3) cache: the blocks of the chunks the plan listed, widened to
+// 16-bit rows of the query type in the workspace copy [cap, 16, Hkv, D]
+// (token-major, like a 16-bit cache), which the kernel below then reads
+// through copy.table.  The conversion is exact (every E4M3 value is an fp16
+// and a bf16 value); the scales stay folded into the softmax scale and the
+// epilogue.  Copy block u belongs to the last listed chunk k with
+// chunk_base[k] <= u; one CTA widens its K and V rows of every kv head (the
+// (block, kv head) runs of the head-major pools are 2 KB apart).
+constexpr int kWidenThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kWidenThreads) widen_chunk_blocks_kernel(const Fp8Copy c,
+                                                                           const int32_t* __restrict__ seq_lens,
+                                                                           int max_blocks, int num_kv_heads) {
+    constexpr int D = 128;
+    const int nchunks = c.hdr[0];
+    const int used = min(c.hdr[1], c.cap_blocks);
+    const int runs = num_kv_heads * 16 * (D / 16);   // 16-code runs per block and pool
+    for (int u = blockIdx.x; u < used && nchunks > 0; u += gridDim.x) {
+        int lo = 0, hi = nchunks - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (c.chunk_base[mid] <= u) lo = mid;
+            else hi = mid - 1;
+        }
+        const int b = c.chunk_seq[lo];
+        const int i = u - c.chunk_base[lo];
+        if (i < 0 || i >= ((seq_lens[b] + 15) >> 4)) continue;
+        const int src = c.src_tables[static_cast<int64_t>(b) * max_blocks + i];
+        const bool ok = src >= 0 && src < c.src_num_blocks;   // else the kernel flags and masks it
+        if (threadIdx.x == 0) c.table[static_cast<int64_t>(b) * max_blocks + i] = ok ? u : -1;
+        if (!ok) continue;
+        const int64_t src_off = static_cast<int64_t>(src) * num_kv_heads * 16 * D;
+        const int64_t dst_off = static_cast<int64_t>(u) * 16 * num_kv_heads * D;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint8_t* sp = static_cast<const uint8_t*>(kv ? c.v_codes : c.k_codes) + src_off;
+            T* dp = static_cast<T*>(kv ? c.v16 : c.k16) + dst_off;
+            for (int x = threadIdx.x; x < runs; x += kWidenThreads) {
+                const int row = x >> 3, ch = x & 7;     // row = h * 16 + t of the head-major block
+                const int h = row >> 4, t = row & 15;
+                const uint4 in = __ldcs(reinterpret_cast<const uint4*>(sp + row * D + ch * 16));
+                uint4 lo4, hi4;
+                widen16<T>(in, lo4, hi4);
+                uint4* o = reinterpret_cast<uint4*>(dp + (t * num_kv_heads + h) * D + ch * 16);
+                o[0] = lo4;
+                o[1] = hi4;
+            }
         }
     }
 }
@@ -309,7 +379,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
 // k * C + i for even k and k * C + C - 1 - i for odd k, so the CTAs' total
 // costs stay even.  (Beside decode rows: pair w / num_kv_heads of the plan's
 // own order, round-robin.)
-template <typename T, int D, bool kFp8>
+template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const int32_t* __restrict__ plan,
                       const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -324,10 +394,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t k_full[NK];               // K tile landed (one arrival per loader)
     __shared__ uint64_t v_full[NV];               // V tile landed (one arrival per loader)
-    // E4M3 cache: K / V tile widened to 16-bit in place (one arrival per
-    // loader); the MMAs and the V-row clearing wait for these instead
-    __shared__ uint64_t k_conv[NK];
-    __shared__ uint64_t v_conv[NV];
     __shared__ uint64_t k_free[NK];               // every S of the stage's tile complete
     __shared__ uint64_t v_free[NV];               // every P V of the stage's tile complete
     __shared__ uint64_t q_full;                   // the item's query tiles landed
@@ -395,12 +461,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < NK; ++s) {
             mbar_init(&k_full[s], kTcLoaders);
-            mbar_init(&k_conv[s], kTcLoaders);
             mbar_init(&k_free[s], 1);
         }
         for (int s = 0; s < NV; ++s) {
             mbar_init(&v_full[s], kTcLoaders);
-            mbar_init(&v_conv[s], kTcLoaders);
             mbar_init(&v_free[s], 1);
         }
         mbar_init(&q_full, 1);
@@ -419,9 +483,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = tmem_slot;
     volatile int* abort_v = &abort_flag;
-    // a K / V stage holds 16-bit rows the MMAs can read
-    uint64_t* const k_ready = kFp8 ? k_conv : k_full;
-    uint64_t* const v_ready = kFp8 ? v_conv : v_full;
 
     // Work item w: (tile pair, kv head) of the plan; within a sequence the
     // pairs nearest the end (the longest key ranges) come first.  Query
@@ -650,7 +711,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // tile's P V is issued after it)
                     const bool clearer = x == 0 || j >= nk_a;
                     if (clearer && (j == it.nkt - 1 || bad)) {
-                        if (!__all_sync(kFullMask, wait_or_abort(&v_ready[J % NV], (J / NV) & 1, abort_v))) {
+                        if (!__all_sync(kFullMask, wait_or_abort(&v_full[J % NV], (J / NV) & 1, abort_v))) {
                             ok = false;
                             break;
                         }
@@ -770,7 +831,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // the previous item's MMAs must be complete: its S/P buffers and
             // accumulators are reused
             if (items > 0) ok = wait_all(&item_done, (items - 1) & 1);
-            if (ok) ok = wait_all(&q_full, items & 1) && wait_all(&k_ready[kv0 % NK], (kv0 / NK) & 1);
+            if (ok) ok = wait_all(&q_full, items & 1) && wait_all(&k_full[kv0 % NK], (kv0 / NK) & 1);
             if (ok) {
                 tc_fence_after_sync();
 #pragma unroll
@@ -780,7 +841,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             for (int j = 0; ok && j < it.nkt; ++j) {
                 const int J = kv0 + j;
-                ok = wait_all(&v_ready[J % NV], (J / NV) & 1);
+                ok = wait_all(&v_full[J % NV], (J / NV) & 1);
                 if (!ok) break;
                 bool k_next = false;   // K(j+1) seen landed
                 // per tile: P V(j) once its softmax stored P, then S(j+1) into
@@ -797,7 +858,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mma_pv(x, j);
                     if (j + 1 >= it.nkx[x]) continue;
                     if (!k_next) {
-                        if (!(ok = wait_all(&k_ready[(J + 1) % NK], ((J + 1) / NK) & 1))) break;
+                        if (!(ok = wait_all(&k_full[(J + 1) % NK], ((J + 1) / NK) & 1))) break;
                         k_next = true;
                     }
                     mma_s(x, j + 1);
@@ -819,117 +880,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (s_issued[x]) (void)mbar_wait(&s_full[x], (s_issued[x] - 1) & 1);
                 (void)pv_issued[x];
             }
-        }
-    } else if constexpr (kFp8) {
-        // ========================= loaders (E4M3 cache) =========================
-        // Loader li takes blocks li, li + 3, ... of every K and V tile.  Lane
-        // 0 issues one 2 KB box per (block, kv head) of the head-major E4M3
-        // pool, landing where the block's rows of the second 64-dim half go
-        // (K: [half][key], V: [block][half][16 keys]); once the tile has landed
-        // the whole warp widens its blocks in place to 16-bit rows and arrives
-        // on k_conv / v_conv.  Tile J of a kind is widened right after tile
-        // J + 1's boxes of that kind are issued, so the copies overlap the
-        // widening; only the query tiles wait for the previous item to drain.
-        reg_dealloc<kTcOtherRegs>();
-        const int li = warp - kTcMmaWarp - 1;
-        int k_total = 0, v_total = 0;   // K and V tiles issued so far (lane 0), for the abort path
-        // lane 0: issue this loader's boxes of tile j of item `it`
-        auto issue = [&](const Item& it, int j, bool v) -> bool {
-            const int J = kv0 + j;
-            const int N = v ? NV : NK;
-            const int s = J % N;
-            if (J >= N && !wait_or_abort(v ? &v_free[s] : &k_free[s], ((J - N) / N) & 1, abort_v)) return false;
-            // K(J) is issued before V(J) and both are widened before K(J + NK)
-            // is issued: the K stage's record holds tile J's ids until then
-            const int sk = J % NK;
-            if (!v) {
-                for (int blk = li; blk < kTcBlocks; blk += kTcLoaders) {
-                    int id = -1;
-                    if (j * kTcBlocks + blk < it.nblk_live) {
-                        id = it.bt[j * kTcBlocks + blk];
-                        if (id < 0 || id >= p.num_blocks) {
-                            record_error(p.err, PA_DEVERR_BLOCK_ID_);
-                            id = -1;
-                        }
-                    }
-                    stage_blocks[li][sk][blk] = id;
-                }
-            }
-            uint32_t bytes = 0;
-            for (int blk = li; blk < kTcBlocks; blk += kTcLoaders)
-                if (stage_blocks[li][sk][blk] >= 0) bytes += 2048;
-            uint64_t* bar = v ? &v_full[s] : &k_full[s];
-            mbar_arrive_expect_tx(bar, bytes);
-            for (int blk = li; blk < kTcBlocks; blk += kTcLoaders) {
-                const int id = stage_blocks[li][sk][blk];
-                if (id < 0) continue;
-                uint8_t* dst = v ? vst(s) + blk * 4096 + 2048 : kst(s) + Sh::kKeyHalf + blk * 2048;
-                tma_load_4d(dst, v ? &vmap : &kmap, bar, 0, 0, it.g, id);
-            }
-            if (v) ++v_total; else ++k_total;
-            return true;
-        };
-        // whole warp: widen this loader's blocks of ring tile J
-        auto widen = [&](int J, bool v) -> bool {
-            const int N = v ? NV : NK;
-            const int s = J % N;
-            if (!__all_sync(kFullMask, wait_or_abort(v ? &v_full[s] : &k_full[s], (J / N) & 1, abort_v)))
-                return false;
-            const int sk = J % NK;
-            for (int blk = li; blk < kTcBlocks; blk += kTcLoaders) {
-                // a block not loaded (past the live table, or outside the pool)
-                // is masked (K) or cleared (V) by the softmax
-                if (stage_blocks[li][sk][blk] < 0) continue;
-                if (v)
-                    widen_fp8_block<T>(vst(s) + blk * 4096 + 2048, vst(s) + blk * 4096, lane);
-                else
-                    widen_fp8_block<T>(kst(s) + Sh::kKeyHalf + blk * 2048, kst(s) + blk * 2048, lane);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(v ? &v_conv[s] : &k_conv[s]);
-            return true;
-        };
-        // lane 0: the item's query tiles, once the previous item's MMAs are done
-        auto load_q = [&](const Item& it) -> bool {
-            if (items > 0 && !wait_or_abort(&item_done, (items - 1) & 1, abort_v)) return false;
-            mbar_arrive_expect_tx(&q_full, static_cast<uint32_t>((it.nkx[1] ? 2 : 1) * q_tile_bytes));
-#pragma unroll
-            for (int x = 0; x < kTcTiles; ++x) {
-                if (!it.nkx[x]) continue;
-#pragma unroll
-                for (int h = 0; h < D / 64; ++h)
-                    tma_load_4d(qs(x) + h * Sh::kQHalf, &qmap, &q_full, 0, h, it.g * G, it.row0 + it.q0[x]);
-            }
-            return true;
-        };
-        auto lane0 = [&](bool r) { return __shfl_sync(kFullMask, r ? 1 : 0, 0) != 0; };
-        for (int k = 0; ok; ++k) {
-            const int w0 = item_at(k);
-            if (w0 == kNoMoreItems) break;
-            Item it;
-            if (w0 < 0 || !decode_item(w0, it)) continue;
-            for (int j = 0; ok && j < it.nkt; ++j) {
-                const int J = kv0 + j;
-                // K(J), then widen K(J - 1); V(J), then widen V(J - 1)
-                ok = lane0(lane == 0 ? issue(it, j, false) : true);
-                __syncwarp();
-                if (ok && J > 0) ok = widen(J - 1, false);
-                if (ok) ok = lane0(lane == 0 ? issue(it, j, true) : true);
-                __syncwarp();
-                if (ok && J > 0) ok = widen(J - 1, true);
-                if (ok && j == 0 && li == 0) ok = lane0(lane == 0 ? load_q(it) : true);
-            }
-            if (!ok && lane == 0) *abort_v = 1;
-            next_item(it);
-        }
-        // the last tile issued
-        if (ok && kv0 > 0) ok = widen(kv0 - 1, false) && widen(kv0 - 1, true);
-        if (!ok && lane == 0) *abort_v = 1;
-        if ((!ok || *abort_v) && lane == 0) {
-            // this loader's copies still in flight: each stage's last issued phase
-            for (int t = max(0, k_total - NK); t < k_total; ++t) (void)mbar_wait(&k_full[t % NK], (t / NK) & 1);
-            for (int t = max(0, v_total - NV); t < v_total; ++t) (void)mbar_wait(&v_full[t % NV], (t / NV) & 1);
         }
     } else {
         // ================================ loaders ===============================
@@ -1044,11 +994,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 
-template <typename T, int D, bool kFp8>
+template <typename T, int D>
 cudaError_t launch_t(const PrefillParams& p, int32_t* plan, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                     const CUtensorMap& qmap, int max_q_len, int num_tokens, cudaStream_t s) {
+                     const CUtensorMap& qmap, int max_q_len, int num_tokens, const Fp8Copy* copy, cudaStream_t s) {
     constexpr int smem = TcShape<D>::kSmem;
-    auto kern = prefill_tc_kernel<T, D, kFp8>;
+    auto kern = prefill_tc_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // the softmax warpgroups' register increase is granted from the pool the
@@ -1058,10 +1008,19 @@ cudaError_t launch_t(const PrefillParams& p, int32_t* plan, const CUtensorMap& k
         return cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : 0;
     }();
     if (launch_regs < kTcLaunchRegs) return cudaErrorInvalidConfiguration;
+    const Fp8Copy none{};
     prefill_plan_kernel<<<1, 1024, 0, s>>>(p.cu_q_lens, p.seq_lens, p.num_seqs, num_tokens, p.q_per_tile, plan,
-                                           p.pair_cap, p.err);
+                                           p.pair_cap, p.err, copy ? *copy : none, p.max_seq_len, p.max_blocks);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (copy && copy->cap_blocks > 0) {
+        // a few CTAs per SM stream the copy blocks (at most cap_blocks of them)
+        const int wgrid = std::max(1, std::min(copy->cap_blocks, 8 * sm_count()));
+        widen_chunk_blocks_kernel<T><<<wgrid, kWidenThreads, 0, s>>>(*copy, p.seq_lens, p.max_blocks,
+                                                                     p.num_kv_heads);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     // upper bound on the work items: each listed chunk (length > 8) has at
     // most ceil(len / q_per_tile) <= len / 2 tiles, and there are at most
     // max_q_len tokens per chunk; an item is a pair of tiles.  One CTA per SM.
@@ -1078,19 +1037,15 @@ cudaError_t launch_t(const PrefillParams& p, int32_t* plan, const CUtensorMap& k
 
 cudaError_t launch_prefill_tc(const PrefillParams& p, int32_t* plan, const CUtensorMap& kmap,
                               const CUtensorMap& vmap, const CUtensorMap& qmap, int head_dim, int dtype,
-                              int max_q_len, int num_tokens, bool fp8, cudaStream_t s) {
+                              int max_q_len, int num_tokens, const Fp8Copy* copy, cudaStream_t s) {
     if (p.num_seqs == 0 || max_q_len <= PA_VERIFY_MAX_Q_) return cudaSuccess;
-    if (fp8) {
-        if (head_dim != 128) return cudaErrorInvalidValue;
-        return dtype == 0 ? launch_t<__half, 128, true>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s)
-                          : launch_t<__nv_bfloat16, 128, true>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s);
-    }
+    if (copy && head_dim != 128) return cudaErrorInvalidValue;
     if (dtype == 0)
-        return head_dim == 128 ? launch_t<__half, 128, false>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s)
-                               : launch_t<__half, 64, false>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s);
+        return head_dim == 128 ? launch_t<__half, 128>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, copy, s)
+                               : launch_t<__half, 64>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, copy, s);
     return head_dim == 128
-               ? launch_t<__nv_bfloat16, 128, false>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s)
-               : launch_t<__nv_bfloat16, 64, false>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, s);
+               ? launch_t<__nv_bfloat16, 128>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, copy, s)
+               : launch_t<__nv_bfloat16, 64>(p, plan, kmap, vmap, qmap, max_q_len, num_tokens, copy, s);
 }
 
 }  // namespace pa

@@ -205,6 +205,37 @@ def test_fp8_entry_points_reject_bad_arguments_on_the_host(lib):
     assert decode(a7=0) == 0
 
 
+def test_fp8_prefill_workspace_size(lib):
+    # the 16-bit call's workspace, then [256 B header | chunk_seq | chunk_base |
+    # table (B x max_blocks)], then K and V copy blocks of 16 rows x Hkv x D x 2 bytes
+    B, T, Hq, Hkv, D, msl, mb = 4, 3000, 32, 8, 128, 4096, 256
+    base = pa.prefill_workspace_bytes(B, T, Hq, D, msl)
+    fixed = 256 + 2 * _align(B * 4) + _align(B * mb * 4)
+    per = 2 * 16 * Hkv * D * 2
+    chunks = min(B, T // 9)                  # at most one partial block per chunk
+    for ckv in (0, 1, 16, 17, 5000):
+        blocks = -(-ckv // 16) + chunks
+        assert pa.prefill_fp8_workspace_bytes(B, T, Hq, Hkv, D, msl, mb, ckv) == base + fixed + blocks * per
+    # never more copy blocks than the block tables can name
+    assert pa.prefill_fp8_workspace_bytes(B, T, Hq, Hkv, D, msl, 2, 10**6) == \
+        base + 256 + 2 * _align(B * 4) + _align(B * 2 * 4) + B * 2 * per
+    assert pa.prefill_fp8_workspace_bytes(2, 10, 8, 8, 128, 64, 4, 32) == \
+        pa.prefill_workspace_bytes(2, 10, 8, 128, 64) + 256 + 2 * _align(8) + _align(32) + (2 + 1) * 2 * 16 * 8 * 128 * 2
+    assert pa.prefill_fp8_workspace_bytes(B, T, Hq, Hkv, D, msl, mb, -1) == 0
+    assert pa.prefill_fp8_workspace_bytes(0, T, Hq, Hkv, D, msl, mb, 0) == 0
+
+
+def test_fp8_prefill_rejects_a_workspace_without_copy_room(lib):
+    # a chunk longer than 8 queries needs room for at least one copy block past
+    # the 16-bit call's workspace and the copy's tables; checked before any CUDA call
+    f = lib.pa_paged_attention_prefill_fp8
+    B, T, Hq, Hkv, D, msl, mb = 2, 40, 8, 2, 128, 64, 4
+    need = pa.prefill_fp8_workspace_bytes(B, T, Hq, Hkv, D, msl, mb, 0) - (T // 9 if T // 9 < B else B) * 2 * 16 * Hkv * D * 2
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, mb, FAKE, FAKE, B, T, 32, msl, 8, 0.1, 1.0, 1.0, Hq, Hkv, D, 16,
+            FAKE, need + 2 * 16 * Hkv * D * 2 - 1, 0, None]
+    assert f(*args) == 3                               # PA_ERR_WORKSPACE_TOO_SMALL
+
+
 def test_gather_rejects_bad_arguments_on_the_host(lib):
     g = lib.pa_paged_kv_gather
     args = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 64, 8, 2, 128, 2, None]

@@ -97,6 +97,44 @@ def test_fp8_chunks_alone_on_many_tiles():
     check(w, *run_step(w))
 
 
+def test_fp8_chunks_that_do_not_fit_the_copy_are_skipped():
+    """Chunks take 16-bit copy blocks in sequence order.  With room for the
+    first chunk's 19 blocks only, the second chunk (63 blocks) and every later
+    one are skipped: their rows keep what was there and PA_DEVERR_WORKSPACE is
+    set.  The first chunk and the decode rows are still exact."""
+    lens, qlens = [300, 1000, 213, 50, 700], [300, 37, 9, 1, 1]
+    w = W.build_workload(name="f8cap", seq_lens=lens, q_lens=qlens, num_q_heads=16, num_kv_heads=4,
+                         head_dim=128, dtype="bf16", seed=19, device=DEV, poison=True, pool_slack=0.3,
+                         cache_dtype="fp8")
+    sc = w.meta["kv_scale"]
+    bt = torch.from_numpy(w.block_tables).to(DEV)
+    sl = torch.from_numpy(w.seq_lens).to(DEV)
+    cu = torch.from_numpy(w.cu_q_lens).to(DEV)
+    k_ref, v_ref = u8(w.k_cache), u8(w.v_cache)
+    slots = pa.slot_mapping(bt, sl, cu, w.num_tokens, w.num_blocks)
+    pa.paged_kv_write_fp8(w.key, w.value, w.k_cache, w.v_cache, slots, sc, sc)
+    oracle.kv_write_fp8(bits(w.key), bits(w.value), k_ref, v_ref,
+                        oracle.slot_mapping(w.block_tables, w.seq_lens, w.q_lens, 16, w.num_blocks), w.dtype, sc, sc)
+    B, T, mb = w.batch, w.num_tokens, w.max_blocks_per_seq
+    per = 2 * 16 * w.num_kv_heads * 128 * 2
+    slack = min(B, T // 9) * per                      # the size function's one partial block per chunk
+    fixed = pa.prefill_fp8_workspace_bytes(B, T, w.num_q_heads, w.num_kv_heads, 128, w.max_seq_len, mb, 0) - slack
+    ws = torch.empty(fixed + 19 * per, dtype=torch.uint8, device=DEV)
+    out = torch.full_like(w.q, 7.0)
+    pa.device_error()
+    pa.paged_attention_prefill_fp8(w.q, w.k_cache, w.v_cache, bt, sl, cu, w.scale, sc, sc, w.max_q_len,
+                                   w.max_seq_len, out=out, workspace=ws, chunk_kv_tokens=0)
+    assert pa.device_error() == 16                    # PA_DEVERR_WORKSPACE
+    ref = oracle.paged_attention_prefill_fp8(bits(w.q), k_ref, v_ref, w.block_tables, w.seq_lens, w.q_lens,
+                                             w.scale, w.dtype, sc, sc)
+    got = out.double().cpu().numpy()
+    cu_np = w.cu_q_lens
+    done = np.r_[cu_np[0]:cu_np[1], cu_np[3]:cu_np[5]]     # chunk 0 and the two decode rows
+    skipped = np.r_[cu_np[1]:cu_np[3]]
+    assert float(np.max(np.abs(got[done] - ref[done]))) <= TOL["bf16"]
+    assert np.all(got[skipped] == 7.0)
+
+
 def test_fp8_prefill_rejects_other_head_dims():
     q = torch.zeros(4, 4, 64, device=DEV, dtype=torch.float16)
     kc = torch.zeros(4, 4, 16, 64, device=DEV, dtype=torch.uint8)
