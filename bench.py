@@ -323,11 +323,23 @@ def run_reference(args):
     return 0
 
 
+def _compact(x):
+    """Floats of the JSON line to 6 significant digits (the line stays short
+    enough for a log tail to carry it whole)."""
+    if isinstance(x, float):
+        return float(f"{x:.6g}")
+    if isinstance(x, dict):
+        return {k: _compact(v) for k, v in x.items()}
+    if isinstance(x, (list, tuple)):
+        return [_compact(v) for v in x]
+    return x
+
+
 # Workloads timed after the headline, one at a time (each freed before the
 # next), each for about SWEEP_SECONDS: every other configuration's attention
 # call with its roofline and the SM clock seen during its own timed region.
 SWEEP = ("llama7b_ctx4096", "gqa_prefix", "long_context", "mixed", "llama7b_decode_fp8", "mixed_fp8", "prefill",
-         "spec_verify")
+         "prefill_fp8", "spec_verify")
 SWEEP_SECONDS = 1.0
 
 
@@ -629,7 +641,7 @@ def run_ours(args):
     if ws == 1 and not args.no_sweep:
         names = [n for n in ("llama7b_decode",) + SWEEP if n != args.workload]
         line["configs"] = sweep(pa, W, dev, stream, args.partition, 5, names)
-    print(json.dumps(line), flush=True)
+    print(json.dumps(_compact(line)), flush=True)
     if dist:
         dist.destroy_process_group()
     return 0

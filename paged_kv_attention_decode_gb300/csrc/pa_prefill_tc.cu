@@ -14,7 +14,8 @@
 //   * warps 0-3: softmax of tile A, warps 4-7: softmax of tile B (thread r of
 //     a group = row r), with 224 registers each (setmaxnreg) so that a row's
 //     128 scores stay in registers;
-//   * warp 8, lane 0: every tcgen05.mma;
+//   * warp 8: every tcgen05.mma and tcgen05.commit, issued by one elected
+//     lane of the converged warp (every lane computes the descriptors);
 //   * warps 9-11: the TMA loads (Q tiles; K and V tiles gathered block by
 //     block through the block table into a ring of K stages and a ring of V
 //     stages).  TMA issue is costly per issuing thread, so the boxes of a
@@ -28,9 +29,8 @@
 //                          stored over the row's S;
 //   O_X += P_X(j) V(j)    M=128 N=D, eight MMAs of K=16, A read from tensor
 //                          memory.
-// A tcgen05.mma instruction of M=128 costs the tensor pipe about the same time
-// for any N up to 128, so 128-key tiles (N=128 for S) do twice the work per
-// instruction of 64-key ones.  S_X is single-buffered: S_X(j+1) is issued
+// 128-key tiles (N=128 for S) halve the instructions, barrier waits and
+// commits per key of 64-key ones.  S_X is single-buffered: S_X(j+1) is issued
 // right behind P_X(j) V(j), which reads P_X(j) from the same columns (the
 // MMAs of one thread execute in issue order), so while one tile's softmax
 // runs, the tensor pipe works on the other tile (ping-pong).  K(j)'s
@@ -95,6 +95,31 @@ __device__ __forceinline__ void reg_alloc() {
 template <uint32_t N>
 __device__ __forceinline__ void reg_dealloc() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+
+// One elected lane of a converged warp issues (every lane computes the
+// operands, so they stay warp-uniform).
+__device__ __forceinline__ void el_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void el_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void el_commit(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_addr(bar))
+        : "memory");
 }
 
 // Bounded mbarrier wait that also gives up when another thread of the CTA has
@@ -785,46 +810,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (w0 < 0 || !decode_item(w0, it)) continue;
             // S_X(j) into S_X: eight MMAs of K=16 over the head dimension
             auto mma_s = [&](int x, int j) {
-                if (lane == 0) {
-                    const uint32_t qa = smem_addr(qs(x));
-                    const uint32_t ka = smem_addr(kst((kv0 + j) % NK));
-                    const uint32_t d_tm = tmem + static_cast<uint32_t>(x * kTcKeys);
+                const uint32_t d_tm = tmem + static_cast<uint32_t>(x * kTcKeys);
+                const uint64_t a0 = smem_desc_sw128(smem_addr(qs(x)), 16, 1024);
+                const uint64_t b0 = smem_desc_sw128(smem_addr(kst((kv0 + j) % NK)), 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t a = smem_desc_sw128(qa + (kk >> 2) * Sh::kQHalf + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd =
-                            smem_desc_sw128(ka + (kk >> 2) * Sh::kKeyHalf + (kk & 3) * 32, 16, 1024);
-                        tc_mma_f16(d_tm, a, bd, kIdescS, kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit(&s_full[x]);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    // the start-address field (bits 0-13, 16-byte units) never carries out
+                    const uint64_t a = a0 + static_cast<uint64_t>(((kk >> 2) * Sh::kQHalf + (kk & 3) * 32) >> 4);
+                    const uint64_t bd = b0 + static_cast<uint64_t>(((kk >> 2) * Sh::kKeyHalf + (kk & 3) * 32) >> 4);
+                    el_mma(d_tm, a, bd, kIdescS, kk > 0 ? 1u : 0u);
                 }
-                __syncwarp();
+                el_commit(&s_full[x]);
                 ++s_issued[x];
             };
             // O_X += P_X(j) V(j): P is read from tensor memory, where the softmax
             // stored it over the first 64 columns of S_X; MMA kp reads block kp
             // of the V tile (its two 64-dim halves 2 KB apart)
             auto mma_pv = [&](int x, int j) {
-                const int Tx = t0[x] + j;
-                if (lane == 0) {
-                    const uint32_t p_tm = tmem + static_cast<uint32_t>(x * kTcKeys);
-                    const uint32_t o_tm = tmem + static_cast<uint32_t>(kTcTiles * kTcKeys + x * D);
-                    const uint32_t va = smem_addr(vst((kv0 + j) % NV));
+                const uint32_t p_tm = tmem + static_cast<uint32_t>(x * kTcKeys);
+                const uint32_t o_tm = tmem + static_cast<uint32_t>(kTcTiles * kTcKeys + x * D);
+                const uint64_t v0 = smem_desc_sw128(smem_addr(vst((kv0 + j) % NV)), 2048, 1024);
 #pragma unroll
-                    for (int kp = 0; kp < kTcKeys / 16; ++kp) {
-                        const uint64_t bd = smem_desc_sw128(va + kp * (D / 64) * 2048, 2048, 1024);
-                        tc_mma_f16_ta(o_tm, p_tm + static_cast<uint32_t>(kp * 8), bd, kIdescPV,
-                                      (j > 0 || kp > 0) ? 1u : 0u);
-                    }
-                    if (j + 1 == it.nkx[x]) tc_commit(&o_done[x][0]);   // the item's last P V of tile x
+                for (int kp = 0; kp < kTcKeys / 16; ++kp) {
+                    const uint64_t bd = v0 + static_cast<uint64_t>((kp * (D / 64) * 2048) >> 4);
+                    el_mma_ta(o_tm, p_tm + static_cast<uint32_t>(kp * 8), bd, kIdescPV, (j > 0 || kp > 0) ? 1u : 0u);
                 }
-                __syncwarp();
+                if (j + 1 == it.nkx[x]) el_commit(&o_done[x][0]);   // the item's last P V of tile x
                 ++pv_issued[x];
             };
-            auto commit = [&](uint64_t* bar) {
-                if (lane == 0) tc_commit(bar);
-                __syncwarp();
-            };
+            auto commit = [&](uint64_t* bar) { el_commit(bar); };
             auto wait_all = [&](uint64_t* bar, uint32_t parity) {
                 return __all_sync(kFullMask, wait_or_abort(bar, parity, abort_v));
             };
@@ -871,14 +885,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!ok && lane == 0) *abort_v = 1;
             next_item(it);
         }
-        if ((!ok || *abort_v) && lane == 0) {
+        if (__any_sync(kFullMask, !ok || *abort_v)) {
             // let MMAs still in flight finish before the CTA's memory is reused
-            tc_commit(&o_done[0][1]);
-            (void)mbar_wait(&o_done[0][1], 0);
+            // (the commit comes from the lane that issued them)
+            el_commit(&o_done[0][1]);
+            if (lane == 0) {
+                (void)mbar_wait(&o_done[0][1], 0);
 #pragma unroll
-            for (int x = 0; x < kTcTiles; ++x) {
-                if (s_issued[x]) (void)mbar_wait(&s_full[x], (s_issued[x] - 1) & 1);
-                (void)pv_issued[x];
+                for (int x = 0; x < kTcTiles; ++x) {
+                    if (s_issued[x]) (void)mbar_wait(&s_full[x], (s_issued[x] - 1) & 1);
+                    (void)pv_issued[x];
+                }
             }
         }
     } else {
