@@ -15,11 +15,12 @@
 //     a group = row r), with 224 registers each (setmaxnreg) so that a row's
 //     128 scores stay in registers;
 //   * warp 8: every tcgen05.mma and tcgen05.commit, issued by one elected
-//     lane of the converged warp (every lane computes the descriptors);
-//   * warps 9-11: the TMA loads (Q tiles; K and V tiles gathered block by
-//     block through the block table into a ring of K stages and a ring of V
-//     stages).  TMA issue is costly per issuing thread, so the boxes of a
-//     tile are split over three warps.  Warps 8-11 keep 56 registers.
+//     lane of the converged warp (every lane computes the descriptors), and
+//     each item's query tiles (TMA, once the previous item's MMAs are done);
+//   * warps 9-11: the K and V tiles, gathered block by block through the
+//     block table into a ring of K stages and a ring of V stages.  Each stage
+//     belongs to one loader warp, whose eight lanes issue the boxes of a
+//     tile's eight blocks together.  Warps 8-11 keep 56 registers.
 // Tensor memory (512 columns): S_A | S_B (128 columns each) | O_A | O_B.
 // Per key tile j and query tile X:
 //   S_X(j) = Q_X K(j)^T   M=128 N=128, eight MMAs of K=16;
@@ -119,6 +120,22 @@ __device__ __forceinline__ void el_commit(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void el_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_addr(bar)), "r"(bytes)
+        : "memory");
+}
+__device__ __forceinline__ void el_tma_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                          int c3) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];\n\t}" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
 
@@ -417,8 +434,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr uint32_t kIdescPV = mma_idesc_f16(128, D, kBf16, true);
 
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t k_full[NK];               // K tile landed (one arrival per loader)
-    __shared__ uint64_t v_full[NV];               // V tile landed (one arrival per loader)
+    __shared__ uint64_t k_full[NK];               // K tile landed (one arrival, by the stage's loader)
+    __shared__ uint64_t v_full[NV];               // V tile landed (one arrival, by the stage's loader)
     __shared__ uint64_t k_free[NK];               // every S of the stage's tile complete
     __shared__ uint64_t v_free[NV];               // every P V of the stage's tile complete
     __shared__ uint64_t q_full;                   // the item's query tiles landed
@@ -437,7 +454,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // barrier never runs two phases ahead).  o_done[0][1]: drains every MMA in
     // flight on the abort path.
     __shared__ uint64_t o_done[kTcTiles][2];
-    __shared__ int32_t stage_blocks[kTcLoaders][NK][kTcBlocks];   // each loader's block ids per K stage
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -485,11 +501,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (tid == 0) {
         for (int s = 0; s < NK; ++s) {
-            mbar_init(&k_full[s], kTcLoaders);
+            mbar_init(&k_full[s], 1);
             mbar_init(&k_free[s], 1);
         }
         for (int s = 0; s < NV; ++s) {
-            mbar_init(&v_full[s], kTcLoaders);
+            mbar_init(&v_full[s], 1);
             mbar_init(&v_free[s], 1);
         }
         mbar_init(&q_full, 1);
@@ -845,6 +861,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // the previous item's MMAs must be complete: its S/P buffers and
             // accumulators are reused
             if (items > 0) ok = wait_all(&item_done, (items - 1) & 1);
+            if (ok) {
+                // the item's query tiles (the previous item's MMAs are done with theirs)
+                el_expect_tx(&q_full, static_cast<uint32_t>((it.nkx[1] ? 2 : 1) * q_tile_bytes));
+#pragma unroll
+                for (int x = 0; x < kTcTiles; ++x) {
+                    if (!it.nkx[x]) continue;
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h)
+                        el_tma_4d(qs(x) + h * Sh::kQHalf, &qmap, &q_full, 0, h, it.g * G, it.row0 + it.q0[x]);
+                }
+            }
             if (ok) ok = wait_all(&q_full, items & 1) && wait_all(&k_full[kv0 % NK], (kv0 / NK) & 1);
             if (ok) {
                 tc_fence_after_sync();
@@ -900,106 +927,73 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ================================ loaders ===============================
-        // Loader li issues the boxes b = li, li + 3, ... of each K tile, box
-        // b = one 64-dim half (b % (D/64)) of one 16-token block (b / (D/64)),
-        // and the boxes of blocks li, li + 3, ... of each V tile, one box per
-        // block (all D dims of its 16 rows); lane 0 issues, and arrives on the
-        // tile's barrier with its bytes.  Before a stage is refilled, the MMA
-        // warp's k_free / v_free for the stage's previous tile is awaited.
-        // Loader 0 also loads the query tiles, after the item's first K and V
-        // boxes: only the query tiles wait for the previous item to drain.
+        // Each ring stage has one loader: K stage s and V stage s belong to
+        // loader s % 3, which therefore sees every phase of the stage's
+        // k_free / v_free barrier (a parity wait is sound only for the phase
+        // after the last one its waiter saw).  A loader walks the key tiles J
+        // = kv0 + j in order and issues K(J) and V(J) when it owns their
+        // stages, eight lanes at once: lane l < 8 reads block l's id (one
+        // coalesced load) and issues that block's boxes (K: one per 64-dim
+        // half; V: one).  The MMA warp loads the query tiles.
         reg_dealloc<kTcOtherRegs>();
         const int li = warp - kTcMmaWarp - 1;
         constexpr int kHalves = D / 64;
-        constexpr int kBoxes = kTcBlocks * kHalves;
-        int k_total = 0, v_total = 0;   // K and V tiles issued so far (ring order), for the abort path
+        int k_last[NK], v_last[NV];   // ring index of the last tile issued per owned stage
+#pragma unroll
+        for (int s = 0; s < NK; ++s) k_last[s] = -1;
+#pragma unroll
+        for (int s = 0; s < NV; ++s) v_last[s] = -1;
         for (int k = 0; ok; ++k) {
             const int w0 = item_at(k);
             if (w0 == kNoMoreItems) break;
             Item it;
             if (w0 < 0 || !decode_item(w0, it)) continue;
-            if (lane == 0) {
-                auto ids_of = [&](int j, int sk) {
-                    // this loader's blocks of tile j, recorded for the V issue
-#pragma unroll
-                    for (int blk = 0; blk < kTcBlocks; ++blk) {
-                        bool mine = false;
-#pragma unroll
-                        for (int h = 0; h < kHalves; ++h) mine |= (blk * kHalves + h) % kTcLoaders == li;
-                        int id = -1;
-                        if (j * kTcBlocks + blk < it.nblk_live) {
-                            id = it.bt[j * kTcBlocks + blk];
-                            if (id < 0 || id >= p.num_blocks) {
-                                if (mine) record_error(p.err, PA_DEVERR_BLOCK_ID_);
-                                id = -1;
-                            }
-                        }
-                        stage_blocks[li][sk][blk] = id;
+            for (int j = 0; ok && j < it.nkt; ++j) {
+                const int J = kv0 + j;
+                const int sk = J % NK, sv = J % NV;
+                const bool do_k = sk % kTcLoaders == li, do_v = sv % kTcLoaders == li;
+                if (!do_k && !do_v) continue;
+                int id = -1;
+                if (lane < kTcBlocks && j * kTcBlocks + lane < it.nblk_live) {
+                    id = it.bt[j * kTcBlocks + lane];
+                    if (id < 0 || id >= p.num_blocks) {
+                        if (do_k) record_error(p.err, PA_DEVERR_BLOCK_ID_);
+                        id = -1;
                     }
-                };
-                auto issue = [&](int j, bool v) {
-                    const int J = kv0 + j;
-                    const int N = v ? NV : NK;
-                    const int s = J % N;
-                    if (J >= N && !wait_or_abort(v ? &v_free[s] : &k_free[s], ((J - N) / N) & 1, abort_v))
-                        return false;
-                    // K(J) is issued before V(J), and K(J + NK) after it: the
-                    // K stage's record still holds tile J's ids for the V issue
-                    const int sk = J % NK;
-                    if (!v) ids_of(j, sk);
-                    uint32_t bytes = 0;
-                    if (v) {
-                        for (int blk = li; blk < kTcBlocks; blk += kTcLoaders)
-                            if (stage_blocks[li][sk][blk] >= 0) bytes += kHalves * 2048;
-                    } else {
-                        for (int b = li; b < kBoxes; b += kTcLoaders)
-                            if (stage_blocks[li][sk][b / kHalves] >= 0) bytes += 2048;
-                    }
-                    uint64_t* bar = v ? &v_full[s] : &k_full[s];
-                    mbar_arrive_expect_tx(bar, bytes);
-                    if (v) {
-                        for (int blk = li; blk < kTcBlocks; blk += kTcLoaders) {
-                            const int id = stage_blocks[li][sk][blk];
-                            if (id >= 0) tma_load_4d(vst(s) + blk * kHalves * 2048, &vmap, bar, 0, id * 16, 0, it.g);
-                        }
-                    } else {
-                        for (int b = li; b < kBoxes; b += kTcLoaders) {
-                            const int blk = b / kHalves, h = b % kHalves;
-                            const int id = stage_blocks[li][sk][blk];
-                            if (id >= 0) tma_load_4d(kst(s) + h * Sh::kKeyHalf + blk * 2048, &kmap, bar, 0, h, it.g, id * 16);
-                        }
-                    }
-                    if (v) ++v_total; else ++k_total;
-                    return true;
-                };
-                // the item's query tiles, once the previous item's MMAs are done
-                auto load_q = [&]() {
-                    if (items > 0) ok = wait_or_abort(&item_done, (items - 1) & 1, abort_v);
-                    if (ok) {
-                        mbar_arrive_expect_tx(&q_full, static_cast<uint32_t>((it.nkx[1] ? 2 : 1) * q_tile_bytes));
-#pragma unroll
-                        for (int x = 0; x < kTcTiles; ++x) {
-                            if (!it.nkx[x]) continue;
-#pragma unroll
-                            for (int h = 0; h < D / 64; ++h)
-                                tma_load_4d(qs(x) + h * Sh::kQHalf, &qmap, &q_full, 0, h, it.g * G,
-                                            it.row0 + it.q0[x]);
-                        }
-                    }
-                };
-                for (int j = 0; ok && j < it.nkt; ++j) {
-                    ok = issue(j, false) && issue(j, true);
-                    if (j == 0 && li == 0 && ok) load_q();
                 }
-                if (!ok) *abort_v = 1;
+                const uint32_t live = static_cast<uint32_t>(__popc(__ballot_sync(kFullMask, id >= 0)));
+                bool r = true;
+                if (do_k) {
+                    // K(J): free once both S(J - NK) are done
+                    if (lane == 0 && J >= NK) r = wait_or_abort(&k_free[sk], ((J - NK) / NK) & 1, abort_v);
+                    if (!(ok = __shfl_sync(kFullMask, r ? 1 : 0, 0) != 0)) break;
+                    if (lane == 0) mbar_arrive_expect_tx(&k_full[sk], live * kHalves * 2048);
+                    __syncwarp();
+#pragma unroll
+                    for (int h = 0; h < kHalves; ++h)
+                        if (id >= 0)
+                            tma_load_4d(kst(sk) + h * Sh::kKeyHalf + lane * 2048, &kmap, &k_full[sk], 0, h, it.g, id * 16);
+                    k_last[sk] = J;
+                }
+                if (do_v) {
+                    // V(J): free once both P V(J - NV) are done
+                    if (lane == 0 && J >= NV) r = wait_or_abort(&v_free[sv], ((J - NV) / NV) & 1, abort_v);
+                    if (!(ok = __shfl_sync(kFullMask, r ? 1 : 0, 0) != 0)) break;
+                    if (lane == 0) mbar_arrive_expect_tx(&v_full[sv], live * kHalves * 2048);
+                    __syncwarp();
+                    if (id >= 0) tma_load_4d(vst(sv) + lane * kHalves * 2048, &vmap, &v_full[sv], 0, id * 16, 0, it.g);
+                    v_last[sv] = J;
+                }
             }
-            ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+            if (!ok && lane == 0) *abort_v = 1;
             next_item(it);
         }
-        if ((!ok || *abort_v) && lane == 0) {
-            // this loader's copies still in flight: each stage's last issued phase
-            for (int t = max(0, k_total - NK); t < k_total; ++t) (void)mbar_wait(&k_full[t % NK], (t / NK) & 1);
-            for (int t = max(0, v_total - NV); t < v_total; ++t) (void)mbar_wait(&v_full[t % NV], (t / NV) & 1);
+        if (__any_sync(kFullMask, !ok || *abort_v) && lane == 0) {
+            // this loader's copies still in flight: the last phase of each stage it filled
+            for (int s = 0; s < NK; ++s)
+                if (k_last[s] >= 0) (void)mbar_wait(&k_full[s], (k_last[s] / NK) & 1);
+            for (int s = 0; s < NV; ++s)
+                if (v_last[s] >= 0) (void)mbar_wait(&v_full[s], (v_last[s] / NV) & 1);
         }
     }
     tc_fence_before_sync();
