@@ -135,6 +135,40 @@ def test_fp8_chunks_that_do_not_fit_the_copy_are_skipped():
     assert np.all(got[skipped] == 7.0)
 
 
+def test_fp8_bad_block_id_in_a_chunk_is_masked_and_flagged():
+    """A live table entry outside the pool in a long chunk's cached prefix:
+    its copy block is marked not loaded, the prefill kernel masks it and sets
+    PA_DEVERR_BLOCK_ID, the chunk's rows stay finite, and the other rows match
+    the oracle."""
+    lens, qlens = [300, 1000, 50, 700], [300, 37, 1, 1]
+    w = W.build_workload(name="f8bad", seq_lens=lens, q_lens=qlens, num_q_heads=16, num_kv_heads=4,
+                         head_dim=128, dtype="bf16", seed=23, device=DEV, poison=True, pool_slack=0.3,
+                         cache_dtype="fp8")
+    sc = w.meta["kv_scale"]
+    bt = torch.from_numpy(w.block_tables).to(DEV)
+    sl = torch.from_numpy(w.seq_lens).to(DEV)
+    cu = torch.from_numpy(w.cu_q_lens).to(DEV)
+    k_ref, v_ref = u8(w.k_cache), u8(w.v_cache)
+    slots = pa.slot_mapping(bt, sl, cu, w.num_tokens, w.num_blocks)
+    pa.paged_kv_write_fp8(w.key, w.value, w.k_cache, w.v_cache, slots, sc, sc)
+    oracle.kv_write_fp8(bits(w.key), bits(w.value), k_ref, v_ref,
+                        oracle.slot_mapping(w.block_tables, w.seq_lens, w.q_lens, 16, w.num_blocks), w.dtype, sc, sc)
+    tables = w.block_tables.copy()
+    tables[1, 10] = w.num_blocks + 3                # tokens 160-175 of the 1000-token sequence (its prefix)
+    pa.device_error()
+    out = pa.paged_attention_prefill_fp8(w.q, w.k_cache, w.v_cache, torch.from_numpy(tables).to(DEV), sl, cu,
+                                         w.scale, sc, sc, w.max_q_len, w.max_seq_len)
+    torch.cuda.synchronize()
+    assert pa.device_error() == 1                   # PA_DEVERR_BLOCK_ID
+    got = out.double().cpu().numpy()
+    cu_np = w.cu_q_lens
+    assert np.all(np.isfinite(got[cu_np[1]:cu_np[2]]))
+    ref = oracle.paged_attention_prefill_fp8(bits(w.q), k_ref, v_ref, w.block_tables, w.seq_lens, w.q_lens,
+                                             w.scale, w.dtype, sc, sc)
+    others = np.r_[cu_np[0]:cu_np[1], cu_np[2]:cu_np[4]]
+    assert float(np.max(np.abs(got[others] - ref[others]))) <= TOL["bf16"]
+
+
 def test_fp8_prefill_rejects_other_head_dims():
     q = torch.zeros(4, 4, 64, device=DEV, dtype=torch.float16)
     kc = torch.zeros(4, 4, 16, 64, device=DEV, dtype=torch.uint8)

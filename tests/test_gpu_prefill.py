@@ -93,6 +93,34 @@ def test_chunk_outside_the_rows_is_flagged(last_q, past):
     assert max_err(out[torch.from_numpy(rows).to(DEV)], ref) <= TOL["bf16"]
 
 
+def test_bad_block_id_in_a_chunk_is_masked_and_flagged():
+    """A live table entry outside the pool in a long chunk's cached prefix:
+    the tensor-core kernel neither loads nor reads that block (its keys are
+    masked, its V rows cleared), sets PA_DEVERR_BLOCK_ID and keeps the chunk's
+    rows finite; the other sequences' rows match the oracle."""
+    q_lens, seq_lens = [40, 1, 130, 9], [90, 21, 400, 35]
+    w = W.build_workload(name="badpre", seq_lens=seq_lens, q_lens=q_lens, num_q_heads=8, num_kv_heads=2,
+                         head_dim=128, dtype="bf16", seed=29, device=DEV, poison=True, pool_slack=0.2)
+    seqs = np.array([0, 1, 3])
+    snap = snapshot(w, seqs)
+    bt = torch.from_numpy(w.block_tables).to(DEV)
+    sl = torch.from_numpy(w.seq_lens).to(DEV)
+    cu = torch.from_numpy(w.cu_q_lens).to(DEV)
+    slots = pa.slot_mapping(bt, sl, cu, w.num_tokens, w.num_blocks)
+    pa.paged_kv_write(w.key, w.value, w.k_cache, w.v_cache, slots)
+    tables = w.block_tables.copy()
+    tables[2, 3] = w.num_blocks + 7                 # tokens 48-63 of the 400-token sequence (its prefix)
+    pa.device_error()
+    out = pa.paged_attention_prefill(w.q, w.k_cache, w.v_cache, torch.from_numpy(tables).to(DEV), sl, cu,
+                                     w.scale, w.max_q_len, w.max_seq_len)
+    torch.cuda.synchronize()
+    assert pa.device_error() == 1                   # PA_DEVERR_BLOCK_ID
+    bad_rows = out[int(w.cu_q_lens[2]):int(w.cu_q_lens[3])]
+    assert bool(torch.isfinite(bad_rows.float()).all())
+    rows, ref = oracle_rows(w, seqs, snap)
+    assert max_err(out[torch.from_numpy(rows).to(DEV)], ref) <= TOL["bf16"]
+
+
 def test_mixed_step_small():
     w = W.make("mixed", device=DEV, poison=True, n_prefill=3, chunk=150, n_decode=40, prefix_hi=700,
                dec_lo=1, dec_hi=900)
