@@ -180,16 +180,19 @@ def test_fp8_prefill_rejects_other_head_dims():
 
 
 @pytest.mark.slow
-def test_fp8_full_mixed_step_sampled():
+@pytest.mark.parametrize("name", ["mixed_fp8", "prefill_fp8"])
+def test_fp8_full_step_sampled(name):
     """The continuous-batching workload (4 chunks of 1536 on prefixes up to
-    4096 and 2048 decodes, 32/8 heads) with an E4M3 cache: the whole step on
-    the GPU; the oracle checks the slots and written codes bit for bit and a
+    4096 and 2048 decodes, 32/8 heads) and the prefill-only one (16 chunks)
+    with an E4M3 cache, as the benchmark times them: the whole step on the
+    GPU; the oracle checks the slots and written codes bit for bit and a
     sample of rows (spread over every chunk, and 64 decodes) within tolerance."""
-    w = W.make("mixed_fp8", device=DEV)
+    w = W.make(name, device=DEV)
     sc = w.meta["kv_scale"]
     rng = np.random.default_rng(14)
     pre = np.nonzero(w.q_lens > 1)[0]
-    dec = np.sort(rng.choice(np.nonzero(w.q_lens == 1)[0], 64, replace=False))
+    decs = np.nonzero(w.q_lens == 1)[0]
+    dec = np.sort(rng.choice(decs, 64, replace=False)) if decs.size else decs
     seqs = np.sort(np.concatenate([pre, dec]))
     # compact copy of the blocks those sequences use (their tables renumbered)
     used = np.unique(np.concatenate([w.block_tables[b, : -(-int(w.seq_lens[b]) // 16)] for b in seqs]))

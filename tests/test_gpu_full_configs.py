@@ -67,6 +67,30 @@ def test_full_mixed_step():
     torch.cuda.empty_cache()
 
 
+def test_full_prefill():
+    """The prefill-only workload the benchmark times (16 chunks of 1536 on
+    prefixes up to 4096; the tcgen05 kernel alone on the GPU, items in the
+    cost-sorted snake order): chunk edges, tile edges and random rows of every
+    chunk against the oracle."""
+    w = W.make("prefill", device=DEV)
+    seqs = np.arange(w.batch)
+    snap = snapshot(w, seqs)
+    slots, out = gpu_step(w)
+    _check_cache(w, slots)
+
+    def pick(b, ql):
+        fixed = [0, 1, 31, 32, 63, 64, 127, 128, ql // 2, ql - 33, ql - 32, ql - 2, ql - 1]
+        extra = np.random.default_rng(100 + b).choice(ql, 4, replace=False).tolist()
+        return sorted(set(fixed + extra))
+
+    rows, ref = oracle_rows(w, seqs, snap, q_rows_per_seq=pick)
+    err = max_err(out[torch.from_numpy(rows).to(DEV)], ref)
+    assert err <= TOL["bf16"], err
+    assert pa.device_error() == 0
+    del w
+    torch.cuda.empty_cache()
+
+
 def test_full_spec_verify():
     # 64 verify rows of 4 queries (3 drafts) on contexts up to 4K: every row
     w = W.make("spec_verify", device=DEV)
