@@ -24,10 +24,11 @@
 // Tensor memory (512 columns): S_A | S_B (128 columns each) | O_A | O_B.
 // Per key tile j and query tile X:
 //   S_X(j) = Q_X K(j)^T   M=128 N=128, eight MMAs of K=16;
-//   softmax_X(j)          one tcgen05.ld wait for the S row, its maximum, the
-//                          running reference m_ref and sum l, exponentials
-//                          with paired fp32 instructions; P (bf16/fp16) is
-//                          stored over the row's S;
+//   softmax_X(j)          one tcgen05.ld wait for the S row, exponentials
+//                          against the running reference m_ref with paired
+//                          fp32 instructions and the sum l (the row maximum
+//                          only when the reference may have to move); P
+//                          (bf16/fp16) is stored over the row's S;
 //   O_X += P_X(j) V(j)    M=128 N=D, eight MMAs of K=16, A read from tensor
 //                          memory.
 // 128-key tiles (N=128 for S) halve the instructions, barrier waits and
@@ -67,6 +68,7 @@ constexpr int kTcKeys = 128;                                         // keys per
 constexpr int kTcBlocks = kTcKeys / 16;                               // cache blocks per tile
 constexpr uint32_t kTmemCols = 512;  // S_A | S_B (128 each) | O_A | O_B
 constexpr float kRescaleLog2 = 8.f;
+constexpr float kPLazyMax = 256.f;   // 2^kRescaleLog2: a tile's sum of P below it needs no row maximum
 constexpr unsigned kFullMask = 0xffffffffu;
 
 template <int D>
@@ -652,90 +654,115 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc_fence_after_sync();
                     const int key0 = j * kTcKeys;
-                    // the row's 128 scores, all in flight before one wait
+                    // The row maximum only decides the lazy rescale below, so a
+                    // first pass takes the exponentials against the current
+                    // reference m_ref without it.  When the tile's sum of P stays
+                    // below 2^8, so does every P: the maximum is then at most
+                    // m_ref + 8, the rule would keep m_ref, and the tile is done.
+                    // Otherwise (and on an item's first tile, or while a row has
+                    // no reference yet) a second pass reloads S, which stays in
+                    // tensor memory until P is stored, and takes the maximum
+                    // first.  Either way P is what taking the maximum every time
+                    // gives.  (Warp-wide decisions: tcgen05.ld/st are collective.)
+                    bool need_max = __any_sync(kFullMask, m_ref == -INFINITY);
                     float sv[kTcKeys];
-                    {
-                        uint32_t r0[32], r1[32], r2[32], r3[32];
-                        tmem_ld32(s_tm, r0);
-                        tmem_ld32(s_tm + 32, r1);
-                        tmem_ld32(s_tm + 64, r2);
-                        tmem_ld32(s_tm + 96, r3);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            sv[c] = __uint_as_float(r0[c]);
-                            sv[32 + c] = __uint_as_float(r1[c]);
-                            sv[64 + c] = __uint_as_float(r2[c]);
-                            sv[96 + c] = __uint_as_float(r3[c]);
-                        }
-                    }
-                    // A positive scale is applied after the row maximum (the
-                    // maximum of the scaled scores is the scaled maximum, as
-                    // rounding is monotonic), fused with the subtraction of
-                    // the exponent.
-                    if (!fold) {
-#pragma unroll
-                        for (int c = 0; c < kTcKeys; c += 2) mul2(sv[c], sv[c + 1], p.scale_log2);
-                    }
-                    if ((key0 + kTcKeys - 1 > pos_lo) || bad) {
-#pragma unroll
-                        for (int c = 0; c < kTcKeys; ++c) {
-                            const bool dead = key0 + c > pos_row || ((bad >> (c >> 4)) & 1u);
-                            sv[c] = dead ? -INFINITY : sv[c];
-                        }
-                    }
-                    // the row maximum: four chains of three-input maxima
-                    float mx;
-                    {
-                        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                        for (int c = 0; c < kTcKeys; c += 8) {
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) mq[u] = fmax3(mq[u], sv[c + 2 * u], sv[c + 2 * u + 1]);
-                        }
-                        mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
-                        if (fold) mx *= p.scale_log2;
-                    }
-                    // lazy rescale: move the reference only when the maximum has
-                    // grown by more than 2^8 (warp-wide: tcgen05.ld/st are
-                    // collective).  P V(j-1) is complete (S(j) was issued after
-                    // it), so O can be rescaled in place.
-                    if (__any_sync(kFullMask, mx > m_ref + kRescaleLog2)) {
-                        const float new_ref = fmaxf(m_ref, mx);
-                        const float alpha = new_ref == -INFINITY ? 1.f : fast_exp2(m_ref - new_ref);
-                        if (j > 0) {
+                    float l_tile;
 #pragma unroll 1
-                            for (int c0 = 0; c0 < D / 32; ++c0) {   // (rare: kept rolled)
-                                uint32_t rr[32];
-                                tmem_ld32(o_tm + static_cast<uint32_t>(c0 * 32), rr);
-                                tmem_ld_wait();
+                    for (;;) {
+                        // the row's 128 scores, all in flight before one wait
+                        {
+                            uint32_t r0[32], r1[32], r2[32], r3[32];
+                            tmem_ld32(s_tm, r0);
+                            tmem_ld32(s_tm + 32, r1);
+                            tmem_ld32(s_tm + 64, r2);
+                            tmem_ld32(s_tm + 96, r3);
+                            tmem_ld_wait();
 #pragma unroll
-                                for (int u = 0; u < 32; ++u) rr[u] = __float_as_uint(__uint_as_float(rr[u]) * alpha);
-                                tmem_st32(o_tm + static_cast<uint32_t>(c0 * 32), rr);
+                            for (int c = 0; c < 32; ++c) {
+                                sv[c] = __uint_as_float(r0[c]);
+                                sv[32 + c] = __uint_as_float(r1[c]);
+                                sv[64 + c] = __uint_as_float(r2[c]);
+                                sv[96 + c] = __uint_as_float(r3[c]);
                             }
-                            tmem_st_wait();
                         }
-                        l_run *= alpha;
-                        m_ref = new_ref;
+                        // A positive scale is applied after the row maximum (the
+                        // maximum of the scaled scores is the scaled maximum, as
+                        // rounding is monotonic), fused with the subtraction of
+                        // the exponent.
+                        if (!fold) {
+#pragma unroll
+                            for (int c = 0; c < kTcKeys; c += 2) mul2(sv[c], sv[c + 1], p.scale_log2);
+                        }
+                        if ((key0 + kTcKeys - 1 > pos_lo) || bad) {
+#pragma unroll
+                            for (int c = 0; c < kTcKeys; ++c) {
+                                const bool dead = key0 + c > pos_row || ((bad >> (c >> 4)) & 1u);
+                                sv[c] = dead ? -INFINITY : sv[c];
+                            }
+                        }
+                        if (need_max) {
+                            // the row maximum: four chains of three-input maxima
+                            float mx;
+                            {
+                                float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                                for (int c = 0; c < kTcKeys; c += 8) {
+#pragma unroll
+                                    for (int u = 0; u < 4; ++u)
+                                        mq[u] = fmax3(mq[u], sv[c + 2 * u], sv[c + 2 * u + 1]);
+                                }
+                                mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
+                                if (fold) mx *= p.scale_log2;
+                            }
+                            // lazy rescale: move the reference only when the
+                            // maximum has grown by more than 2^8.  P V(j-1) is
+                            // complete (S(j) was issued after it), so O can be
+                            // rescaled in place.
+                            if (__any_sync(kFullMask, mx > m_ref + kRescaleLog2)) {
+                                const float new_ref = fmaxf(m_ref, mx);
+                                const float alpha = new_ref == -INFINITY ? 1.f : fast_exp2(m_ref - new_ref);
+                                if (j > 0) {
+#pragma unroll 1
+                                    for (int c0 = 0; c0 < D / 32; ++c0) {   // (rare: kept rolled)
+                                        uint32_t rr[32];
+                                        tmem_ld32(o_tm + static_cast<uint32_t>(c0 * 32), rr);
+                                        tmem_ld_wait();
+#pragma unroll
+                                        for (int u = 0; u < 32; ++u)
+                                            rr[u] = __float_as_uint(__uint_as_float(rr[u]) * alpha);
+                                        tmem_st32(o_tm + static_cast<uint32_t>(c0 * 32), rr);
+                                    }
+                                    tmem_st_wait();
+                                }
+                                l_run *= alpha;
+                                m_ref = new_ref;
+                            }
+                        }
+                        // P = 2^(s - m_ref) (in place) and its sum
+                        {
+                            const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+                            // s * 1 + (-ref) rounds once, like s - ref: one loop for both
+                            const float mul = fold ? p.scale_log2 : 1.f;
+#pragma unroll
+                            for (int c = 0; c < kTcKeys; c += 2) fma2(sv[c], sv[c + 1], mul, -ref);
+#pragma unroll
+                            for (int c = 0; c < kTcKeys; ++c) sv[c] = fast_exp2(sv[c]);
+                            float sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                            for (int c = 0; c < kTcKeys; c += 4) {
+                                add2(sq[0], sq[1], sv[c], sv[c + 1]);
+                                add2(sq[2], sq[3], sv[c + 2], sv[c + 3]);
+                            }
+                            l_tile = (sq[0] + sq[1]) + (sq[2] + sq[3]);
+                        }
+                        // (a NaN sum also takes the second pass)
+                        if (need_max || !__any_sync(kFullMask, !(l_tile < kPLazyMax))) break;
+                        need_max = true;
                     }
-                    // P = 2^(s - m_ref) and its sum; P goes over the row's
-                    // first 64 columns (two 16-bit values per column, keys in
-                    // order)
+                    l_run += l_tile;
+                    // P goes over the row's first 64 columns (two 16-bit values
+                    // per column, keys in order)
                     {
-                        const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-                        // s * 1 + (-ref) rounds once, like s - ref: one loop for both
-                        const float mul = fold ? p.scale_log2 : 1.f;
-#pragma unroll
-                        for (int c = 0; c < kTcKeys; c += 2) fma2(sv[c], sv[c + 1], mul, -ref);
-#pragma unroll
-                        for (int c = 0; c < kTcKeys; ++c) sv[c] = fast_exp2(sv[c]);
-                        float sq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int c = 0; c < kTcKeys; c += 4) {
-                            add2(sq[0], sq[1], sv[c], sv[c + 1]);
-                            add2(sq[2], sq[3], sv[c + 2], sv[c + 3]);
-                        }
-                        l_run += (sq[0] + sq[1]) + (sq[2] + sq[3]);
                         uint32_t pw0[32], pw1[32];
 #pragma unroll
                         for (int c = 0; c < 32; ++c) {
