@@ -59,6 +59,51 @@ def test_prefill_any_scale(scale):
     assert pa.device_error() == 0
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_prefill_reference_moves_in_a_later_key_tile(dtype):
+    """Keys grow key tile by key tile (K of tile i scaled by 2^i, exact in
+    16-bit), so a later tile's scores pass the running reference by more than
+    2^8: the kernel must notice it from the tile's sum of P, take the row
+    maximum and rescale O and l.  The precondition is checked on the inputs."""
+    Hq, Hkv, D, prefix, q_len = 8, 2, 128, 440, 200
+    w = W.build_workload(name="pre_grow", seq_lens=[prefix + q_len], q_lens=[q_len], num_q_heads=Hq,
+                         num_kv_heads=Hkv, head_dim=D, dtype=dtype, seed=123, device=DEV, poison=True,
+                         pool_slack=0.2)
+    n = prefix + q_len
+    factor = torch.tensor([2.0 ** (t // 128) for t in range(n)], dtype=torch.float32)
+    for t in range(prefix):
+        blk = int(w.block_tables[0, t // 16])
+        w.k_cache[blk, t % 16] *= float(factor[t])
+    w.key[:q_len] *= factor[prefix:].to(DEV, w.key.dtype).view(q_len, 1, 1)
+    # precondition: some query row sees a key tile whose maximum passes the
+    # running maximum of the earlier tiles by more than 8 (log2 units)
+    k_all = torch.empty(n, Hkv, D, dtype=torch.float64)
+    for t in range(prefix):
+        k_all[t] = w.k_cache[int(w.block_tables[0, t // 16]), t % 16].double().cpu()
+    k_all[prefix:] = w.key[:q_len].double().cpu()
+    q = w.q[:q_len].double().cpu()
+    G = Hq // Hkv
+    jump = 0.0
+    for i in range(0, q_len, 37):
+        pos = prefix + i
+        for h in range(Hq):
+            s = (k_all[: pos + 1, h // G] @ q[i, h]).numpy() * w.scale * np.log2(np.e)
+            run = -np.inf
+            for k0 in range(0, pos + 1, 128):
+                mx = s[k0:k0 + 128].max()
+                if np.isfinite(run):
+                    jump = max(jump, mx - run)
+                run = max(run, mx)
+    assert jump > 8.0, jump
+    seqs = np.arange(w.batch)
+    snap = snapshot(w, seqs)
+    _, out = gpu_step(w, prefill=True)
+    rows, ref = oracle_rows(w, seqs, snap)
+    err = max_err(out[torch.from_numpy(rows).to(DEV)], ref)
+    assert err <= TOL[dtype], err
+    assert pa.device_error() == 0
+
+
 @pytest.mark.parametrize("last_q,past", [(100, 50), (3, 1)])
 def test_chunk_outside_the_rows_is_flagged(last_q, past):
     """The last chunk's rows run past the call's num_tokens rows (cu_q_lens
