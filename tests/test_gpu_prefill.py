@@ -59,13 +59,13 @@ def test_prefill_any_scale(scale):
     assert pa.device_error() == 0
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_prefill_reference_moves_in_a_later_key_tile(dtype):
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (128, "f16"), (64, "bf16")])
+def test_prefill_reference_moves_in_a_later_key_tile(D, dtype):
     """Keys grow key tile by key tile (K of tile i scaled by 2^i, exact in
     16-bit), so a later tile's scores pass the running reference by more than
     2^8: the kernel must notice it from the tile's sum of P, take the row
     maximum and rescale O and l.  The precondition is checked on the inputs."""
-    Hq, Hkv, D, prefix, q_len = 8, 2, 128, 440, 200
+    Hq, Hkv, prefix, q_len = 8, 2, 440, 200
     w = W.build_workload(name="pre_grow", seq_lens=[prefix + q_len], q_lens=[q_len], num_q_heads=Hq,
                          num_kv_heads=Hkv, head_dim=D, dtype=dtype, seed=123, device=DEV, poison=True,
                          pool_slack=0.2)
